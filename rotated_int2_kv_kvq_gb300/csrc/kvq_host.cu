@@ -1,0 +1,380 @@
+// kvq_host.cu — the C ABI of libkvq (include/kvq.h): argument validation,
+// handle lifetime, the rotation bank, launches, the device status word and the
+// kernel-timing record.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "kvq_internal.cuh"
+
+struct kvq_handle {
+  kvq_layout L;
+  int G = 4;
+  float sm_scale = 0.f;
+  int device = 0;
+  int num_sms = 1;
+  int ctas_int2 = 1, ctas_bf16 = 1;
+  uint32_t* status = nullptr;      // device
+  float* bank = nullptr;           // device: R [2][Hkv][D][D], RVt [Hkv][D][D], mu [Hkv][D]
+  bool ready = false;
+  // kernel timing
+  bool prof = false;
+  static constexpr int kSlots = 256;
+  cudaEvent_t ev[kSlots][2] = {};
+  bool pending[kSlots] = {};
+  int next = 0;
+  double total_ms = 0.0;
+  int launches = 0;
+};
+
+namespace {
+
+using kvq::kDim;
+using kvq::kPage;
+
+bool layout_ok(const kvq_layout* L) {
+  if (!L) return false;
+  if (L->head_dim != kDim || L->group != kDim || L->page_size != kPage) return false;
+  if (L->num_kv_heads < 1 || L->num_kv_heads > 64) return false;
+  if (L->num_heads < 1 || L->num_heads % L->num_kv_heads != 0) return false;
+  const int G = L->num_heads / L->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4) return false;
+  if (!(L->clip_k > 0.f && L->clip_k <= 1.f) || !(L->clip_v > 0.f && L->clip_v <= 1.f))
+    return false;
+  if (!(L->sm_scale == L->sm_scale)) return false;        // NaN
+  if (L->flags & ~KVQ_OUT_ROTATED) return false;
+  return true;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA; }
+
+cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+size_t rot_floats(int Hkv) {
+  return static_cast<size_t>(3) * Hkv * kDim * kDim + static_cast<size_t>(Hkv) * kDim;
+}
+
+// Splits for `batch` sequences: enough CTAs for about four full waves of the
+// GPU, never fewer than 8 pages per split when max_pages is known.
+int splits_cap(const kvq_handle* h, int batch, bool int2) {
+  const long units = static_cast<long>(batch) * h->L.num_kv_heads;
+  const long slots = static_cast<long>(h->num_sms) * (int2 ? h->ctas_int2 : h->ctas_bf16);
+  long s = (4 * slots + units - 1) / units;
+  if (s < 1) s = 1;
+  if (s > kvq::kMaxSplits) s = kvq::kMaxSplits;
+  return static_cast<int>(s);
+}
+
+int choose_splits(const kvq_handle* h, int batch, int max_pages, bool int2) {
+  int s = splits_cap(h, batch, int2);
+  const int by_pages = (max_pages + 7) / 8;
+  if (s > by_pages) s = by_pages;
+  return s < 1 ? 1 : s;
+}
+
+void prof_begin(kvq_handle* h, cudaStream_t st, int* slot) {
+  *slot = -1;
+  if (!h->prof) return;
+  const int k = h->next;
+  h->next = (h->next + 1) % kvq_handle::kSlots;
+  if (h->pending[k]) {          // fold the slot's previous (long finished) pair in
+    float ms = 0.f;
+    cudaEventSynchronize(h->ev[k][1]);
+    if (cudaEventElapsedTime(&ms, h->ev[k][0], h->ev[k][1]) == cudaSuccess) h->total_ms += ms;
+    h->pending[k] = false;
+  }
+  if (!h->ev[k][0]) {
+    if (cudaEventCreate(&h->ev[k][0]) != cudaSuccess || cudaEventCreate(&h->ev[k][1]) != cudaSuccess)
+      return;
+  }
+  cudaEventRecord(h->ev[k][0], st);
+  *slot = k;
+}
+
+void prof_end(kvq_handle* h, cudaStream_t st, int slot) {
+  if (slot < 0) return;
+  cudaEventRecord(h->ev[slot][1], st);
+  h->pending[slot] = true;
+  h->launches += 1;
+}
+
+int check_decode_args(kvq_handle* h, const void* pool, int num_pool_pages, const uint16_t* q,
+                      const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                      int batch, float* out, void* workspace, int num_splits) {
+  if (!h || !pool || !q || !page_table || !seq_lens || !out || !workspace) return KVQ_EINVAL;
+  if (num_pool_pages < 1 || max_pages < 1 || batch < 1 || batch > 65535) return KVQ_EINVAL;
+  if (num_splits < 0 || num_splits > kvq::kMaxSplits) return KVQ_EINVAL;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return KVQ_EINVAL;
+  if (reinterpret_cast<uintptr_t>(pool) % 16 != 0) return KVQ_EINVAL;
+  if (reinterpret_cast<uintptr_t>(q) % 4 != 0) return KVQ_EINVAL;
+  return KVQ_OK;
+}
+
+int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages,
+                  const uint16_t* q, const int32_t* page_table, int max_pages,
+                  const int32_t* seq_lens, int batch, float* out, void* workspace,
+                  size_t ws_bytes, int num_splits, void* stream) {
+  int rc = check_decode_args(h, pool, num_pool_pages, q, page_table, max_pages, seq_lens, batch,
+                             out, workspace, num_splits);
+  if (rc != KVQ_OK) return rc;
+  if (int2 && !h->ready) return KVQ_ENOTREADY;
+  const int splits = num_splits ? num_splits : choose_splits(h, batch, max_pages, int2);
+  const kvq::DecodeWs w =
+      kvq::decode_ws_layout(batch, h->L.num_kv_heads, h->L.num_heads, splits, int2);
+  if (ws_bytes < w.total) return KVQ_ENOSPACE;
+  if (cudaSetDevice(h->device) != cudaSuccess) return KVQ_ECUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  kvq::DecodeArgs a;
+  a.pool = static_cast<const uint8_t*>(pool);
+  a.num_pool_pages = num_pool_pages;
+  a.q = q;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.H = h->L.num_heads;
+  a.Hkv = h->L.num_kv_heads;
+  a.G = h->G;
+  a.splits = splits;
+  a.chunk_pages = (max_pages + splits - 1) / splits;
+  a.qfrag = reinterpret_cast<const uint32_t*>(ws + w.qfrag_off);
+  a.qmeta = reinterpret_cast<const float*>(ws + w.qmeta_off);
+  a.part = reinterpret_cast<float*>(ws + w.part_off);
+  a.status = h->status;
+  a.log2_scale = h->sm_scale * 1.4426950408889634f;
+  cudaStream_t st = S(stream);
+  cudaError_t e;
+  if (int2) {
+    e = kvq::launch_qprep(a, h->bank, h->sm_scale, st);
+    if (e != cudaSuccess) return KVQ_ECUDA;
+  }
+  int slot;
+  prof_begin(h, st, &slot);
+  e = int2 ? kvq::launch_decode_int2(a, st) : kvq::launch_decode_bf16(a, st);
+  prof_end(h, st, slot);
+  if (e != cudaSuccess) return KVQ_ECUDA;
+  const float* RVt = h->bank ? h->bank + static_cast<size_t>(2) * a.Hkv * kDim * kDim : nullptr;
+  const bool rotate = int2 && !(h->L.flags & KVQ_OUT_ROTATED);
+  e = kvq::launch_combine(a, RVt, rotate, out, st);
+  return cuda_rc(e);
+}
+
+int append_common(kvq_handle* h, bool int2, void* pool, int num_pool_pages, const uint16_t* K,
+                  const uint16_t* V, const int32_t* seq_idx, const int32_t* positions, int n,
+                  const int32_t* page_table, int batch, int max_pages, void* stream) {
+  if (!h || n < 0) return KVQ_EINVAL;
+  if (n == 0) return KVQ_OK;
+  if (!pool || !K || !V || !seq_idx || !positions || !page_table) return KVQ_EINVAL;
+  if (num_pool_pages < 1 || batch < 1 || max_pages < 1) return KVQ_EINVAL;
+  if (reinterpret_cast<uintptr_t>(K) % 16 || reinterpret_cast<uintptr_t>(V) % 16 ||
+      reinterpret_cast<uintptr_t>(pool) % 16)
+    return KVQ_EINVAL;
+  if (int2 && !h->ready) return KVQ_ENOTREADY;
+  if (cudaSetDevice(h->device) != cudaSuccess) return KVQ_ECUDA;
+  kvq::AppendArgs a;
+  a.pool = static_cast<uint8_t*>(pool);
+  a.num_pool_pages = num_pool_pages;
+  a.K = K;
+  a.V = V;
+  a.seq_idx = seq_idx;
+  a.positions = positions;
+  a.n = n;
+  a.page_table = page_table;
+  a.batch = batch;
+  a.max_pages = max_pages;
+  a.Hkv = h->L.num_kv_heads;
+  a.R = h->bank;
+  a.mu = h->bank ? h->bank + static_cast<size_t>(3) * a.Hkv * kDim * kDim : nullptr;
+  a.clip_k = h->L.clip_k;
+  a.clip_v = h->L.clip_v;
+  a.status = h->status;
+  cudaError_t e = int2 ? kvq::launch_append_int2(a, h->num_sms, S(stream))
+                       : kvq::launch_append_bf16(a, S(stream));
+  return cuda_rc(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvq_create(const kvq_layout* layout, kvq_handle** out) {
+  if (!out) return KVQ_EINVAL;
+  *out = nullptr;
+  if (!layout_ok(layout)) return KVQ_EINVAL;
+  kvq_handle* h = new (std::nothrow) kvq_handle();
+  if (!h) return KVQ_ECUDA;
+  h->L = *layout;
+  h->G = layout->num_heads / layout->num_kv_heads;
+  h->sm_scale = layout->sm_scale > 0.f ? layout->sm_scale : 1.0f / sqrtf(static_cast<float>(kDim));
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
+      cudaMalloc(&h->status, sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) {
+    if (h->status) cudaFree(h->status);
+    delete h;
+    return KVQ_ECUDA;
+  }
+  h->ctas_int2 = kvq::decode_int2_ctas_per_sm();
+  h->ctas_bf16 = kvq::decode_bf16_ctas_per_sm();
+  *out = h;
+  return KVQ_OK;
+}
+
+int kvq_destroy(kvq_handle* h) {
+  if (!h) return KVQ_OK;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  for (int k = 0; k < kvq_handle::kSlots; ++k) {
+    if (h->ev[k][0]) cudaEventDestroy(h->ev[k][0]);
+    if (h->ev[k][1]) cudaEventDestroy(h->ev[k][1]);
+  }
+  if (h->bank) cudaFree(h->bank);
+  if (h->status) cudaFree(h->status);
+  delete h;
+  return KVQ_OK;
+}
+
+size_t kvq_page_bytes(const kvq_handle* h) {
+  return h ? static_cast<size_t>(h->L.num_kv_heads) * KVQ_INT2_RECORD_BYTES : 0;
+}
+
+size_t kvq_bf16_page_bytes(const kvq_handle* h) {
+  return h ? static_cast<size_t>(h->L.num_kv_heads) * KVQ_BF16_RECORD_BYTES : 0;
+}
+
+int kvq_set_rotation(kvq_handle* h, const float* R, const float* mu, void* stream) {
+  if (!h || !R || !mu) return KVQ_EINVAL;
+  if (cudaSetDevice(h->device) != cudaSuccess) return KVQ_ECUDA;
+  const int Hkv = h->L.num_kv_heads;
+  if (!h->bank && cudaMalloc(&h->bank, rot_floats(Hkv) * sizeof(float)) != cudaSuccess) {
+    h->bank = nullptr;
+    return KVQ_ECUDA;
+  }
+  cudaStream_t st = S(stream);
+  const size_t mat = static_cast<size_t>(kDim) * kDim;
+  float* RVt = h->bank + 2 * Hkv * mat;
+  float* mub = h->bank + 3 * Hkv * mat;
+  if (cudaMemcpyAsync(h->bank, R, 2 * Hkv * mat * sizeof(float), cudaMemcpyDeviceToDevice, st) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(mub, mu, static_cast<size_t>(Hkv) * kDim * sizeof(float),
+                      cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return KVQ_ECUDA;
+  if (kvq::launch_transpose(h->bank + Hkv * mat, RVt, Hkv, st) != cudaSuccess) return KVQ_ECUDA;
+  h->ready = true;
+  return KVQ_OK;
+}
+
+int kvq_append(kvq_handle* h, void* pool, int num_pool_pages, const uint16_t* K,
+               const uint16_t* V, const int32_t* seq_idx, const int32_t* positions, int n,
+               const int32_t* page_table, int batch, int max_pages, void* stream) {
+  return append_common(h, true, pool, num_pool_pages, K, V, seq_idx, positions, n, page_table,
+                       batch, max_pages, stream);
+}
+
+int kvq_bf16_append(kvq_handle* h, void* pool, int num_pool_pages, const uint16_t* K,
+                    const uint16_t* V, const int32_t* seq_idx, const int32_t* positions, int n,
+                    const int32_t* page_table, int batch, int max_pages, void* stream) {
+  return append_common(h, false, pool, num_pool_pages, K, V, seq_idx, positions, n, page_table,
+                       batch, max_pages, stream);
+}
+
+size_t kvq_workspace_bytes(const kvq_handle* h, int batch, int num_splits) {
+  if (!h || batch < 1 || num_splits < 0 || num_splits > kvq::kMaxSplits) return 0;
+  const int s = num_splits ? num_splits : splits_cap(h, batch, true);
+  return kvq::decode_ws_layout(batch, h->L.num_kv_heads, h->L.num_heads, s, true).total;
+}
+
+size_t kvq_bf16_workspace_bytes(const kvq_handle* h, int batch, int num_splits) {
+  if (!h || batch < 1 || num_splits < 0 || num_splits > kvq::kMaxSplits) return 0;
+  const int s = num_splits ? num_splits : splits_cap(h, batch, false);
+  return kvq::decode_ws_layout(batch, h->L.num_kv_heads, h->L.num_heads, s, false).total;
+}
+
+int kvq_auto_splits(const kvq_handle* h, int batch, int max_pages) {
+  if (!h || batch < 1 || max_pages < 1) return 0;
+  return choose_splits(h, batch, max_pages, true);
+}
+
+int kvq_decode(kvq_handle* h, const void* pool, int num_pool_pages, const uint16_t* q,
+               const int32_t* page_table, int max_pages, const int32_t* seq_lens, int batch,
+               float* out, void* workspace, size_t ws_bytes, int num_splits, void* stream) {
+  return decode_common(h, true, pool, num_pool_pages, q, page_table, max_pages, seq_lens, batch,
+                       out, workspace, ws_bytes, num_splits, stream);
+}
+
+int kvq_bf16_decode(kvq_handle* h, const void* pool, int num_pool_pages, const uint16_t* q,
+                    const int32_t* page_table, int max_pages, const int32_t* seq_lens, int batch,
+                    float* out, void* workspace, size_t ws_bytes, int num_splits, void* stream) {
+  if (h && num_splits == 0) num_splits = choose_splits(h, batch, max_pages, false);
+  return decode_common(h, false, pool, num_pool_pages, q, page_table, max_pages, seq_lens, batch,
+                       out, workspace, ws_bytes, num_splits, stream);
+}
+
+int kvq_dequant(kvq_handle* h, const void* pool, int num_pool_pages, const int32_t* page_table,
+                int max_pages, int seq, int start, int len, float* K_out, float* V_out,
+                void* stream) {
+  if (!h || !pool || !page_table || len < 0 || seq < 0 || start < 0) return KVQ_EINVAL;
+  if (num_pool_pages < 1 || max_pages < 1) return KVQ_EINVAL;
+  if (len == 0 || (!K_out && !V_out)) return KVQ_OK;
+  if (cudaSetDevice(h->device) != cudaSuccess) return KVQ_ECUDA;
+  return cuda_rc(kvq::launch_dequant(static_cast<const uint8_t*>(pool), num_pool_pages,
+                                     page_table, max_pages, h->L.num_kv_heads, seq, start, len,
+                                     K_out, V_out, h->status, S(stream)));
+}
+
+int kvq_get_status(kvq_handle* h, uint32_t* bits, void* stream) {
+  if (!h || !bits) return KVQ_EINVAL;
+  if (cudaSetDevice(h->device) != cudaSuccess) return KVQ_ECUDA;
+  cudaStream_t st = S(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, h->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(h->status, 0, sizeof(uint32_t), st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return KVQ_ECUDA;
+  *bits = v;
+  return KVQ_OK;
+}
+
+int kvq_profile_enable(kvq_handle* h, int enable) {
+  if (!h) return KVQ_EINVAL;
+  h->prof = enable != 0;
+  h->total_ms = 0.0;
+  h->launches = 0;
+  for (int k = 0; k < kvq_handle::kSlots; ++k) h->pending[k] = false;
+  h->next = 0;
+  return KVQ_OK;
+}
+
+int kvq_profile_read(kvq_handle* h, double* total_ms, int* launches) {
+  if (!h || !total_ms || !launches) return KVQ_EINVAL;
+  for (int k = 0; k < kvq_handle::kSlots; ++k) {
+    if (!h->pending[k]) continue;
+    float ms = 0.f;
+    if (cudaEventSynchronize(h->ev[k][1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, h->ev[k][0], h->ev[k][1]) != cudaSuccess)
+      return KVQ_ECUDA;
+    h->total_ms += ms;
+    h->pending[k] = false;
+  }
+  *total_ms = h->total_ms;
+  *launches = h->launches;
+  h->total_ms = 0.0;
+  h->launches = 0;
+  h->next = 0;
+  return KVQ_OK;
+}
+
+const char* kvq_strerror(int code) {
+  switch (code) {
+    case KVQ_OK: return "ok";
+    case KVQ_EINVAL: return "invalid argument or unsupported layout";
+    case KVQ_ENOSPACE: return "workspace too small";
+    case KVQ_ECUDA: return "CUDA runtime error or kernel launch failure";
+    case KVQ_ENOTREADY: return "rotation bank not set (call kvq_set_rotation first)";
+    default: return "unknown kvq error code";
+  }
+}
+
+}  // extern "C"

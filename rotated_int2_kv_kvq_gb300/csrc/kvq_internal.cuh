@@ -1,0 +1,182 @@
+// kvq_internal.cuh — shared declarations of the CUDA side of libkvq (sm_103a).
+//
+// Nothing here is part of the public ABI (include/kvq.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kDim = 128;          // head_dim
+constexpr int kPage = 16;          // tokens per page
+constexpr int kInt2Rec = KVQ_INT2_RECORD_BYTES;   // bytes per (page, kv head)
+constexpr int kBf16Rec = KVQ_BF16_RECORD_BYTES;
+constexpr int kMaxG = 4;           // query heads per KV head handled per CTA
+constexpr int kPartStride = 132;   // floats per split partial: m, l, 2 pad, o[128]
+constexpr int kQFragWords = 32 * 16;   // uint32 per (b, kv): 32 lanes x 16 B-fragment regs
+constexpr int kMaxSplits = 1024;
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeThreads = kDecodeWarps * 32;
+constexpr int kProfMax = 65536;
+
+// Workspace layout of one decode call (offsets in bytes, each 256-aligned).
+struct DecodeWs {
+  size_t qfrag_off, qmeta_off, part_off, total;
+};
+DecodeWs decode_ws_layout(int batch, int Hkv, int H, int splits, bool int2);
+
+struct DecodeArgs {
+  const uint8_t* pool;
+  int num_pool_pages;
+  const uint16_t* q;
+  const int32_t* page_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  int batch;
+  int H, Hkv, G;
+  int splits, chunk_pages;
+  const uint32_t* qfrag;     // [B][Hkv][32][16]
+  const float* qmeta;        // [B][Hkv][4][2]: kappa, zeta per head
+  float* part;               // [B][H][splits][kPartStride]
+  uint32_t* status;
+  float log2_scale;          // sm_scale * log2(e)
+};
+
+struct AppendArgs {
+  uint8_t* pool;
+  int num_pool_pages;
+  const uint16_t* K;
+  const uint16_t* V;
+  const int32_t* seq_idx;
+  const int32_t* positions;
+  int n;
+  const int32_t* page_table;
+  int batch, max_pages, Hkv;
+  const float* R;            // [2][Hkv][D][D]
+  const float* mu;           // [Hkv][D]
+  float clip_k, clip_v;
+  uint32_t* status;
+};
+
+// ---- launchers (defined in the .cu files) --------------------------------
+cudaError_t launch_append_int2(const AppendArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_append_bf16(const AppendArgs& a, cudaStream_t st);
+cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, float sm_scale, cudaStream_t st);
+cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_combine(const DecodeArgs& a, const float* RVt, bool rotate_out, float* out,
+                           cudaStream_t st);
+cudaError_t launch_dequant(const uint8_t* pool, int num_pool_pages, const int32_t* page_table,
+                           int max_pages, int Hkv, int seq, int start, int len, float* K_out,
+                           float* V_out, uint32_t* status, cudaStream_t st);
+cudaError_t launch_transpose(const float* in, float* out, int count, cudaStream_t st);
+int decode_int2_ctas_per_sm();
+int decode_bf16_ctas_per_sm();
+
+// ---- device helpers -------------------------------------------------------
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after a bounded number of
+// attempts (each attempt may itself suspend for a hardware-defined time).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < (1u << 22); ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// One-dimensional bulk copy global -> shared (TMA, no tensor map), completing
+// `bytes` of transaction count on `bar`.  dst, src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^x via the SFU (ex2.approx.ftz): 2^-inf = 0, 2^0 = 1.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float half_lo(uint32_t h2) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t h2) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace kvq

@@ -96,11 +96,12 @@ def _rng(*key) -> np.random.Generator:
 
 
 def to_bf16_bits(x) -> np.ndarray:
-    """float array -> bf16 bit patterns (uint16), round to nearest even."""
+    """float array -> bf16 bit patterns (uint16), round to nearest even (finite
+    and infinite inputs; no NaNs are generated)."""
     f = np.ascontiguousarray(x, dtype=np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    u = u + 0x7FFF + ((u >> 16) & 1)
-    return (u >> 16).astype(np.uint16)
+    u = f.view(np.uint32)
+    u = u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))
+    return (u >> np.uint32(16)).astype(np.uint16)
 
 
 def bf16_bits_to_float(b) -> np.ndarray:
@@ -132,16 +133,17 @@ def _key_params(wl: Workload, layer: int):
 
 
 def _draw_keys(wl: Workload, layer: int, g: np.random.Generator, n: int) -> np.ndarray:
+    """float32 [n, Hkv, D] keys (before bf16 rounding)."""
     offsets, outliers = _key_params(wl, layer)
-    noise = g.standard_normal((n, wl.num_kv_heads, D), dtype=np.float32).astype(np.float64)
-    k = noise + offsets[None]
+    k = g.standard_normal((n, wl.num_kv_heads, D), dtype=np.float32)
+    k += offsets.astype(np.float32)[None]
     for kv in range(wl.num_kv_heads):
         ch = outliers[kv]
         if wl.key_kind == "gauss_x8":
-            k[:, kv, ch] = 8.0 * k[:, kv, ch]
+            k[:, kv, ch] *= np.float32(8.0)
         else:
             t = g.standard_t(3, size=(n, len(ch)))
-            k[:, kv, ch] = offsets[kv, ch][None] + 8.0 * t
+            k[:, kv, ch] = (offsets[kv, ch][None] + 8.0 * t).astype(np.float32)
     return k
 
 
@@ -175,6 +177,19 @@ def tokens(wl: Workload, layer: int, seq: int, which: int, start: int, n: int) -
         out[pos - start:pos - start + take] = _block(wl, layer, seq, which, blk)[off:off + take]
         pos += take
     return out
+
+
+def tokens_many(wl: Workload, layer: int, seqs, which: int, start, n, workers: int = 8):
+    """[len(seqs)] arrays of tokens(), drawn in parallel threads (numpy releases
+    the GIL while drawing).  start and n may be scalars or per-sequence lists."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    seqs = list(seqs)
+    st = start if hasattr(start, "__len__") else [start] * len(seqs)
+    nn = n if hasattr(n, "__len__") else [n] * len(seqs)
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(lambda i: tokens(wl, layer, seqs[i], which, int(st[i]), int(nn[i])),
+                           range(len(seqs))))
 
 
 def token_at(wl: Workload, layer: int, seq: int, which: int, pos: int) -> np.ndarray:

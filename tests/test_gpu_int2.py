@@ -1,0 +1,260 @@
+"""GPU parity of the INT2 path through the C ABI against the CPU oracle.
+
+* appended bytes (codes, page placement, fp16 scale/zero): bit-exact; a code
+  may differ only where the oracle's pre-rounding value lies within 1 ulp of a
+  rounding boundary, and such cases are counted;
+* dequantisation export: bit-exact (same fp32 fmaf on both sides);
+* decode attention: within 1e-3 relative L2 and 5e-3 max-abs of the float64
+  oracle run on the GPU's own pool bytes.
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kvq_testlib import Cache, assert_close_attention, compare_codes, i32, u16
+from rotated_int2_kv_kvq_gb300 import kvq as K
+from rotated_int2_kv_kvq_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _block_fn(wl, layer):
+    @functools.lru_cache(maxsize=256)
+    def blk(seq, which, b):
+        return W.tokens(wl, layer, seq, which, b * 1024, 1024)
+
+    return (lambda s, p: blk(s, 0, p // 1024)[p % 1024],
+            lambda s, p: blk(s, 1, p // 1024)[p % 1024])
+
+
+# ---------------------------------------------------------------------------
+# tiny workload: everything checked exhaustively
+# ---------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def tiny():
+    wl = W.WORKLOADS["tiny_1k"]
+    c = Cache(wl)
+    Ks, Vs = c.append_range([0], 0, wl.ctx)
+    return c, Ks[0], Vs[0]
+
+
+def test_tiny_append_bitexact(tiny):
+    c, Kt, Vt = tiny
+    pool = c.pool_host()
+    ref = np.zeros_like(pool)
+    n = Kt.shape[0]
+    oracle.append_int2(ref, c.npool, 1, Kt, Vt, np.zeros(n), np.arange(n), c.pt_np, c.R, c.mu,
+                       c.wl.clip_k, c.wl.clip_v)
+    if not np.array_equal(pool, ref):
+        # only boundary cases may differ: check token by token
+        Ktok, Vtok = (lambda s, p: Kt[p]), (lambda s, p: Vt[p])
+        near = compare_codes(c, pool, [(0, p, 0) for p in range(n)], Ktok, Vtok)
+        print("boundary-case code differences:", near)
+    assert c.status() == 0
+
+
+def test_tiny_dequant_bitexact(tiny):
+    c, _, _ = tiny
+    n = c.wl.ctx
+    Ko = torch.empty((n, 1, 128), dtype=torch.float32, device="cuda")
+    Vo = torch.empty_like(Ko)
+    K.kvq_dequant(c.h, c.pool, c.npool, c.pt, 0, 0, n, Ko, Vo)
+    Kr, Vr = oracle.dequant_int2(c.pool_host(), c.npool, 1, c.pt_np, 0, 0, n)
+    assert np.array_equal(Ko.cpu().numpy(), Kr) and np.array_equal(Vo.cpu().numpy(), Vr)
+
+
+@pytest.mark.parametrize("seq_len", [1, 2, 15, 16, 17, 100, 333, 1023, 1024])
+@pytest.mark.parametrize("splits", [0, 1, 2, 7, 64])
+def test_tiny_decode(tiny, seq_len, splits):
+    c, _, _ = tiny
+    q = W.queries(c.wl, 0, seq_len)
+    got = c.decode(q, [seq_len], splits)
+    want = c.oracle_decode(c.pool_host(), q, [seq_len], [[0, h] for h in range(4)])
+    assert_close_attention(got[0], want, f"len {seq_len} splits {splits}")
+
+
+def test_tiny_decode_empty_context(tiny):
+    c, _, _ = tiny
+    got = c.decode(W.queries(c.wl), [0], 3)
+    assert not np.any(got)
+    assert c.status() == 0
+
+
+def test_split_count_invariance(tiny):
+    c, _, _ = tiny
+    q = W.queries(c.wl, 0, 5)
+    outs = [c.decode(q, [1000], s) for s in (1, 2, 7, 63, 64)]
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= 1e-5 * max(1.0, np.abs(outs[0]).max())
+
+
+def test_out_rotated_flag(tiny):
+    c, Kt, Vt = tiny
+    c2 = Cache(c.wl, out_rotated=True)
+    c2.append(Kt, Vt, np.zeros(Kt.shape[0]), np.arange(Kt.shape[0]))
+    q = W.queries(c.wl, 0, 9)
+    rot = c2.decode(q, [500], 4)[0]
+    plain = c.decode(q, [500], 4)[0]
+    RV = c.R[1, 0].astype(np.float64)
+    assert np.allclose(rot @ RV.T, plain, rtol=0, atol=1e-4 * np.abs(plain).max())
+    want = c2.oracle_decode(c2.pool_host(), q, [500], [[0, h] for h in range(4)])
+    assert_close_attention(rot, want, "rotated output")
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_gqa_group_sizes(G):
+    wl = W.WORKLOADS["tiny_1k"]
+    c = Cache(wl, num_heads=G, num_kv_heads=1)
+    c.append_range([0], 0, 300)
+    q = W.queries(wl, 0, 11)[:, :G].copy()
+    got = c.decode(q, [300], 3)
+    want = c.oracle_decode(c.pool_host(), q, [300], [[0, h] for h in range(G)])
+    assert_close_attention(got[0], want, f"G={G}")
+
+
+def test_multi_sequence_interleaved_append():
+    """Tokens of several sequences in one call, in shuffled order, including
+    several tokens of one page: every byte still lands where the oracle puts it."""
+    wl = W.WORKLOADS["qwen3_8b_32k"]
+    B, n_per = 3, 70
+    pt = np.arange(B * 5, dtype=np.int32).reshape(B, 5)[:, ::-1].copy()
+    c = Cache(wl, page_table=pt, num_pool_pages=B * 5)
+    seqs = np.repeat(np.arange(B), n_per).astype(np.int32)
+    pos = np.tile(np.arange(n_per), B).astype(np.int32)
+    perm = np.random.default_rng(0).permutation(B * n_per)
+    seqs, pos = seqs[perm], pos[perm]
+    Kt = np.stack([W.token_at(wl, 0, s, 0, p) for s, p in zip(seqs, pos)])
+    Vt = np.stack([W.token_at(wl, 0, s, 1, p) for s, p in zip(seqs, pos)])
+    c.append(Kt, Vt, seqs, pos)
+    ref = np.zeros(c.npool * 8 * 1152, np.uint8)
+    oracle.append_int2(ref, c.npool, 8, Kt, Vt, seqs, pos, pt, c.R, c.mu, wl.clip_k, wl.clip_v)
+    pool = c.pool_host()
+    if not np.array_equal(pool, ref):
+        near = compare_codes(c, pool, [(s, p, kv) for s, p in zip(seqs, pos) for kv in range(8)],
+                             lambda s, p: Kt[np.nonzero((seqs == s) & (pos == p))[0][0]],
+                             lambda s, p: Vt[np.nonzero((seqs == s) & (pos == p))[0][0]])
+        print("boundary-case code differences:", near)
+    q = W.queries(wl, 0, 1, batch=B)
+    got = c.decode(q, [n_per] * B, 2)
+    pairs = [[b, h] for b in range(B) for h in range(0, 32, 5)]
+    want = c.oracle_decode(pool, q, [n_per] * B, pairs)
+    assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled outputs
+# ---------------------------------------------------------------------------
+
+def _sample_tokens(rng, lens, Hkv, n):
+    out = []
+    for _ in range(n):
+        s = int(rng.integers(0, len(lens)))
+        out.append((s, int(rng.integers(0, lens[s])), int(rng.integers(0, Hkv))))
+    return out
+
+
+@pytest.fixture(scope="module")
+def qwen32k():
+    wl = W.WORKLOADS["qwen3_8b_32k"]
+    c = Cache(wl)
+    for g0 in range(0, wl.batch, 4):
+        c.append_range(range(g0, g0 + 4), 0, wl.ctx)
+    return c
+
+
+def test_qwen32k_codes_sampled(qwen32k):
+    c = qwen32k
+    rng = np.random.default_rng(21)
+    samples = _sample_tokens(rng, [c.wl.ctx] * c.wl.batch, 8, 1500)
+    samples += [(0, 0, 0), (15, 32767, 7), (3, 16, 2), (9, 32752, 5)]
+    Ktok, Vtok = _block_fn(c.wl, 0)
+    near = compare_codes(c, c.pool_host(), samples, Ktok, Vtok)
+    print("boundary-case code differences:", near)
+    assert c.status() == 0
+
+
+def test_qwen32k_decode_sampled(qwen32k):
+    c = qwen32k
+    q = W.queries(c.wl)
+    lens = [c.wl.ctx] * c.wl.batch
+    got = c.decode(q, lens, 0)          # the automatic split choice, as the bench runs it
+    rng = np.random.default_rng(22)
+    pairs = [[int(rng.integers(0, 16)), int(rng.integers(0, 32))] for _ in range(12)]
+    pairs += [[0, 0], [15, 31]]
+    want = c.oracle_decode(c.pool_host(), q, lens, pairs)
+    assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want, "qwen32k")
+
+
+@pytest.mark.parametrize("splits", [64, 128, 256])
+def test_long_128k_decode(splits, long128k):
+    c = long128k
+    q = W.queries(c.wl, 0, splits)
+    got = c.decode(q, [c.wl.ctx], splits)
+    pairs = [[0, h] for h in (0, 7, 13, 22, 31)]
+    want = c.oracle_decode(c.pool_host(), q, [c.wl.ctx], pairs)
+    assert_close_attention(got[0, [p[1] for p in pairs]], want, f"128k splits {splits}")
+
+
+@pytest.fixture(scope="module")
+def long128k():
+    wl = W.WORKLOADS["long_128k"]
+    c = Cache(wl)
+    for s0 in range(0, wl.ctx, 32768):
+        c.append_range([0], s0, 32768)
+    return c
+
+
+def test_ragged_batch_decode():
+    wl = W.WORKLOADS["ragged_64"]
+    c = Cache(wl)
+    lens = W.seq_lens(wl)
+    for g0 in range(0, wl.batch, 8):
+        c.append_range(range(g0, g0 + 8), 0, [int(x) for x in lens[g0:g0 + 8]])
+    q = W.queries(wl)
+    got = c.decode(q, lens, 0)
+    rng = np.random.default_rng(23)
+    pairs = [[int(b), int(rng.integers(0, 32))] for b in
+             [int(np.argmax(lens)), int(np.argmin(lens))] + list(rng.integers(0, 64, 8))]
+    want = c.oracle_decode(c.pool_host(), q, lens, pairs)
+    assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want, "ragged")
+    Ktok, Vtok = _block_fn(wl, 0)
+    near = compare_codes(c, c.pool_host(), _sample_tokens(rng, lens, 8, 400), Ktok, Vtok)
+    print("boundary-case code differences:", near)
+    assert c.status() == 0
+
+
+@pytest.mark.parametrize("layer", [0, 17, 35])
+def test_full_stack_sampled_layers(layer):
+    """Prefill 8192 tokens per sequence for batch 8, then 128 decode steps, each
+    appending one token and decoding; outputs checked at steps 0, 63, 127."""
+    wl = W.WORKLOADS["full_stack_36l"]
+    c = Cache(wl, layer=layer)
+    c.append_range(range(wl.batch), 0, wl.prefill)
+    B = wl.batch
+    Knew = W.tokens_many(wl, layer, range(B), 0, wl.prefill, wl.decode_steps)
+    Vnew = W.tokens_many(wl, layer, range(B), 1, wl.prefill, wl.decode_steps)
+    checked = 0
+    for step in range(wl.decode_steps):
+        pos = wl.prefill + step
+        c.append(np.stack([Knew[b][step] for b in range(B)]), np.stack([Vnew[b][step] for b in range(B)]),
+                 np.arange(B), np.full(B, pos))
+        q = W.queries(wl, layer, step)
+        lens = [pos + 1] * B
+        got = c.decode(q, lens, 0)
+        if step in (0, 63, 127):
+            pairs = [[b, (7 * b + step) % 32] for b in range(B)]
+            want = c.oracle_decode(c.pool_host(), q, lens, pairs)
+            assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want,
+                                   f"layer {layer} step {step}")
+            checked += 1
+    assert checked == 3
+    Ktok, Vtok = _block_fn(wl, layer)
+    rng = np.random.default_rng(24 + layer)
+    near = compare_codes(c, c.pool_host(), _sample_tokens(rng, [wl.prefill + 128] * B, 8, 300),
+                         Ktok, Vtok)
+    print("boundary-case code differences:", near)
+    assert c.status() == 0
