@@ -122,7 +122,9 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
       for (int e = 0; e < 8; ++e) Cs[(ch * 8 + e) * kTile + k] = v[e];
     }
     if (!r_ready) {
-      if (!mbar_wait_bounded(bar_a, 0)) {
+      // every thread waits (bounded); the CTA leaves together if any gave up
+      const bool ok = mbar_wait_bounded(bar_a, 0);
+      if (__syncthreads_or(!ok)) {
         if (tid == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
         return;      // nothing was written for this CTA
       }
