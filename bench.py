@@ -1,0 +1,403 @@
+"""Benchmark of the rotated INT2 KV-cache decode step on GB300.
+
+One step = the whole hot path for one batch: quantise-and-append one new K/V
+token per sequence (centre, rotate, clip, INT2 pack into its page) and one
+split-K INT2 decode-attention call over the paged cache (query rotation, scores,
+online softmax, P.V, log-sum-exp combine, inverse value rotation).
+
+Workload (default): Qwen3-8B-shaped layer, batch 16, 32 query / 8 KV heads,
+head_dim 128, context 32768 per sequence in 16-token pages over a shuffled pool.
+The cache is built once before timing; each step appends the token at position
+32767 (rewriting that slot) and decodes over all 32768 positions.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead.
+Under torchrun (N > 1) every rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rotated_int2_kv_kvq_gb300 import workloads as W  # noqa: E402
+
+METRIC = "INT2 decode-attn cache GB/s (% of HBM peak) & decode steps/s at 32K ctx"
+UNIT = "GB/s"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_int2_qwen3_8b_32k.md")
+DECODE_SRC = os.path.join(ROOT, "rotated_int2_kv_kvq_gb300", "csrc", "kvq_decode.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_32k")
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison kernel")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary,
+    or None if the summary is missing or was taken on a different kernel source."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kvq_decode\.cu sha256\[:16\]:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != source_hash(DECODE_SRC):
+        return None
+    return float(m.group(1))
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kvq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.remove(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_setup(wl, seq=0, kv=0):
+    """One (sequence, KV head) of the workload, built by the oracle alone."""
+    import oracle
+
+    ctx = wl.ctx
+    pages = ctx // 16
+    pt = np.arange(pages, dtype=np.int32)[None, :]
+    pool = np.zeros(pages * 1152, np.uint8)
+    R = W.rotations(wl)[:, kv:kv + 1].copy()
+    mu = W.key_mean(wl)[kv:kv + 1].copy()
+    Kt = W.tokens(wl, 0, seq, 0, 0, ctx)[:, kv:kv + 1].copy()
+    Vt = W.tokens(wl, 0, seq, 1, 0, ctx)[:, kv:kv + 1].copy()
+    oracle.append_int2(pool, pages, 1, Kt, Vt, np.zeros(ctx), np.arange(ctx), pt, R, mu,
+                       wl.clip_k, wl.clip_v)
+    G = wl.num_heads // wl.num_kv_heads
+    q = W.queries(wl)[seq:seq + 1, kv * G:(kv + 1) * G].copy()
+    return dict(pool=pool, pages=pages, pt=pt, R=R, mu=mu, K=Kt[-1:], V=Vt[-1:], q=q, G=G)
+
+
+def oracle_step(wl, s):
+    """Append the last token again and decode the G query heads of the sample."""
+    import oracle
+
+    ctx = wl.ctx
+    oracle.append_int2(s["pool"], s["pages"], 1, s["K"], s["V"], [0], [ctx - 1], s["pt"], s["R"],
+                       s["mu"], wl.clip_k, wl.clip_v)
+    oracle.decode_pairs("int2", s["pool"], s["pages"], s["G"], 1, s["q"], s["pt"], [ctx],
+                        [[0, h] for h in range(s["G"])], R=s["R"])
+
+
+def cpu_oracle_rate(wl, min_seconds=10.0, max_steps=None, warmup=0):
+    """Cache GB/s of the oracle on (sequence 0, KV head 0): each step reads that
+    head's whole context once for its G query heads."""
+    s = oracle_sample_setup(wl)
+    for _ in range(warmup):
+        oracle_step(wl, s)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(wl, s)
+        n += 1
+        el = time.perf_counter() - t0
+        if (max_steps is not None and n >= max_steps) or (max_steps is None and el >= min_seconds):
+            break
+    bytes_per_step = wl.ctx * W.cache_bytes_per_token_head("int2")
+    return bytes_per_step * n / el / 1e9, n, el
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = W.WORKLOADS[args.workload]
+    gbs, n, el = cpu_oracle_rate(wl, max_steps=max(1, args.steps), warmup=max(0, args.warmup))
+    sample = (f"float64 oracle, sequence 0 / KV head 0 of {wl.name}: per step re-quantise one "
+              f"token and decode {wl.num_heads // wl.num_kv_heads} query heads over {wl.ctx} "
+              f"tokens ({n} steps, {el:.1f} s)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": n, "warmup": args.warmup, "ms_per_step": el / n * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "ctx": wl.ctx,
+                   "heads": wl.num_heads, "kv_heads": wl.num_kv_heads, "head_dim": 128,
+                   "page": 16},
+        "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    from rotated_int2_kv_kvq_gb300 import kvq as K
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    K.load_library()
+    wl = W.WORKLOADS[args.workload]
+    B, H, Hkv, ctx = wl.batch, wl.num_heads, wl.num_kv_heads, wl.ctx
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+    lens = W.seq_lens(wl)
+    pt_np, npool = W.page_table(wl)
+    pt = i32(pt_np)
+    max_pages = pt_np.shape[1]
+    layout = K.make_layout(H, Hkv, wl.clip_k, wl.clip_v)
+    h = K.kvq_create(layout)
+    K.kvq_set_rotation(h, torch.from_numpy(W.rotations(wl)).cuda(),
+                       torch.from_numpy(W.key_mean(wl)).cuda())
+    pool = torch.zeros(npool * K.kvq_page_bytes(h), dtype=torch.uint8, device="cuda")
+    bf16_pool = None
+    if not args.no_bf16:
+        bf16_pool = torch.zeros(npool * K.kvq_bf16_page_bytes(h), dtype=torch.uint8,
+                                device="cuda")
+    # build the cache: positions [0, len-1) of every sequence
+    t_build = time.perf_counter()
+    for g0 in range(0, B, 4):
+        seqs = list(range(g0, min(B, g0 + 4)))
+        n = [int(lens[s]) - 1 for s in seqs]
+        Ks = W.tokens_many(wl, 0, seqs, 0, 0, n)
+        Vs = W.tokens_many(wl, 0, seqs, 1, 0, n)
+        for s, k, v, m in zip(seqs, Ks, Vs, n):
+            sid, pos = i32(np.full(m, s)), i32(np.arange(m))
+            kd, vd = dev(k), dev(v)
+            K.kvq_append(h, pool, npool, kd, vd, sid, pos, pt)
+            if bf16_pool is not None:
+                K.kvq_bf16_append(h, bf16_pool, npool, kd, vd, sid, pos, pt)
+    torch.cuda.synchronize()
+    t_build = time.perf_counter() - t_build
+    # step inputs: the token at position len-1 of every sequence, and the queries
+    k_new = np.stack([W.token_at(wl, 0, b, 0, int(lens[b]) - 1) for b in range(B)])
+    v_new = np.stack([W.token_at(wl, 0, b, 1, int(lens[b]) - 1) for b in range(B)])
+    q_np = W.queries(wl)
+    kd_new, vd_new, qd = dev(k_new), dev(v_new), dev(q_np)
+    sid, pos = i32(np.arange(B)), i32(lens - 1)
+    seq_lens = i32(lens)
+    splits = args.splits or K.kvq_auto_splits(h, B, max_pages)
+    ws = torch.empty(K.kvq_workspace_bytes(h, B, splits), dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, H, 128), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        K.kvq_append(h, pool, npool, kd_new, vd_new, sid, pos, pt)
+        K.kvq_decode(h, pool, npool, qd, pt, seq_lens, out, ws, splits)
+
+    def timed(fn, steps, warmup, profile=False):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        if profile:
+            K.kvq_profile_enable(h, True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        kern = K.kvq_profile_read(h) if profile else None
+        if profile:
+            K.kvq_profile_enable(h, False)
+        if dist is not None:
+            t = torch.tensor([ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, kern
+
+    clocks = Clocks(local)
+    clocks.start()
+    ms, kern = timed(step, args.steps, args.warmup, profile=True)
+    clk = clocks.stop()
+    assert K.kvq_get_status(h) == 0, "device status bits set during the benchmark"
+    ms_step = ms / args.steps
+    cache_bytes = int(lens.sum()) * Hkv * W.cache_bytes_per_token_head("int2")
+    gbs_rank = cache_bytes / (ms_step * 1e-3) / 1e9
+    value = gbs_rank * world
+    peak, peak_kind = measured_peaks()
+    kern_ms = kern[0] / max(1, kern[1]) if kern else None
+    achieved = cache_bytes / (kern_ms * 1e-3) / 1e9 if kern_ms else None
+    traffic = profiled_traffic()
+
+    # e2e: the same step through the public API with pinned host buffers: copy this
+    # step's inputs (q and the new K/V token) in and the attention output out.
+    q_h = torch.from_numpy(q_np.view(np.int16)).pin_memory()
+    k_h = torch.from_numpy(k_new.view(np.int16)).pin_memory()
+    v_h = torch.from_numpy(v_new.view(np.int16)).pin_memory()
+    out_h = torch.empty((B, H, 128), dtype=torch.float32).pin_memory()
+    qd2, kd2, vd2 = torch.empty_like(qd), torch.empty_like(kd_new), torch.empty_like(vd_new)
+
+    def e2e_step():
+        qd2.copy_(q_h, non_blocking=True)
+        kd2.copy_(k_h, non_blocking=True)
+        vd2.copy_(v_h, non_blocking=True)
+        K.kvq_append(h, pool, npool, kd2, vd2, sid, pos, pt)
+        K.kvq_decode(h, pool, npool, qd2, pt, seq_lens, out, ws, splits)
+        out_h.copy_(out, non_blocking=True)
+
+    e2e_ms, _ = timed(e2e_step, args.steps, max(3, args.warmup // 2))
+    e2e_gbs = cache_bytes / (e2e_ms / args.steps * 1e-3) / 1e9 * world
+    h2d = q_h.numel() * 2 + k_h.numel() * 2 + v_h.numel() * 2
+    d2h = out_h.numel() * 4
+
+    # BF16 comparison kernel: same step on the BF16 cache
+    bf16 = None
+    if bf16_pool is not None:
+        ws16 = torch.empty(K.kvq_bf16_workspace_bytes(h, B, 0), dtype=torch.uint8, device="cuda")
+
+        def bf16_step():
+            K.kvq_bf16_append(h, bf16_pool, npool, kd_new, vd_new, sid, pos, pt)
+            K.kvq_bf16_decode(h, bf16_pool, npool, qd, pt, seq_lens, out, ws16, 0)
+
+        bsteps = max(3, args.steps // 4)
+        bms, bkern = timed(bf16_step, bsteps, max(3, args.warmup // 4), profile=True)
+        bbytes = int(lens.sum()) * Hkv * W.cache_bytes_per_token_head("bf16")
+        bkern_ms = bkern[0] / max(1, bkern[1])
+        bf16 = {"steps_per_s": bsteps / (bms * 1e-3), "ms_per_step": bms / bsteps,
+                "cache_bytes_per_step": bbytes,
+                "kernel_gbs": bbytes / (bkern_ms * 1e-3) / 1e9,
+                "kernel_frac_of_peak": bbytes / (bkern_ms * 1e-3) / 1e9 / peak,
+                "int2_speedup_steps": (args.steps / (ms * 1e-3)) / (bsteps / (bms * 1e-3))}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        gbs_cpu, n_cpu, el_cpu = cpu_oracle_rate(wl, min_seconds=10.0)
+        cpu = {"value": gbs_cpu, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"float64 oracle on sequence 0 / KV head 0: re-quantise one token and "
+                         f"decode {H // Hkv} query heads over {ctx} tokens per step, "
+                         f"{n_cpu} steps in {el_cpu:.1f} s"}
+
+    launches = 4 * args.steps       # append, q-rotation, split-K attention, split merge
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int2 codes, fp16 mma, fp32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "batch": B, "ctx": ctx, "heads": H, "kv_heads": Hkv,
+                   "head_dim": 128, "page": 16, "splits": splits,
+                   "l2": f"inputs larger than L2: {cache_bytes / 1e6:.0f} MB INT2 cache read per "
+                         f"step, no flush",
+                   "cache_build_s": round(t_build, 1)},
+        "steps_per_s": world * args.steps / (ms * 1e-3),
+        "pct_of_hbm_peak": 100.0 * gbs_rank / peak,
+        "effective_bits": W.effective_bits(128),
+        "cache_bytes_per_step": cache_bytes,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                     "kernel": "decode_int2_kernel", "peak_kind": peak_kind,
+                     "kernel_ms": kern_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_gbs, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "bf16_comparison": bf16,
+        "clocks": clk,
+        "gpu_launches": launches,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

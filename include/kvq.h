@@ -259,7 +259,8 @@ int kvq_get_status(kvq_handle* h, uint32_t* bits, void* stream);
 int kvq_auto_splits(const kvq_handle* h, int batch, int max_pages);
 
 /* Kernel timing: while enabled, each kvq_decode / kvq_bf16_decode records a
- * CUDA event pair around its split-K attention kernel (only that kernel).
+ * CUDA event pair around its split-K attention kernel (only that kernel; it
+ * includes the log-sum-exp merge, done by the last CTA of each (b, kv head)).
  * kvq_profile_read synchronises on the last event and returns the summed
  * milliseconds and the number of launches since the last enable, then clears
  * the record.  At most 65536 launches are recorded per enable. */

@@ -13,19 +13,28 @@
 //
 // How the INT2 kernel maps onto sm_103a
 // -------------------------------------
-// One CTA = 4 warps = one (split, KV head, sequence).  Each warp streams every
-// 4th page of the split through its own ring of shared-memory stages filled by
-// 1-D TMA bulk copies (cp.async.bulk, mbarrier completion).  A page record
-// (1152 B) holds the 16 tokens' codes in tensor-core fragment order, so each lane
-// takes its whole share with one 16-byte shared load and hands the codes to
-// mma.sync.m16n8k16 without any shuffling:
+// One CTA = 8 warps = one (split, group of HPC KV heads, sequence); warp w
+// serves KV head w / (8/HPC) of the group.  The pool stores the records of all
+// KV heads of a page next to each other, so one 1-D TMA bulk copy
+// (cp.async.bulk, mbarrier completion) brings a page for all the CTA's heads.
+// A stage holds 2 * (8/HPC) pages; every warp takes two pages from each stage
+// (two independent tensor-core chains in flight).  The last warp to finish a
+// stage (a shared-memory arrival counter) refills it, so no warp waits for a
+// free slot.  A page record (1152 B per head) holds the 16 tokens' codes in
+// tensor-core fragment order, so each lane takes its share of a page with one
+// 16-byte shared load and hands it to mma.sync.m16n8k16 without shuffling:
 //   scores  S[token][col] = Kcode[token][dim] . B[dim][col]     (M = 16 tokens)
 //   values  O^T[dim][col] += Vcode^T[dim][token] . P[token][col] (M = 16 dims)
 // with col = 2*head + {hi, lo}: each operand that is not a code is split into an
-// fp16 high part and an fp16 residual, which keeps products at fp32 accuracy.
-// Codes become fp16 operands with one AND: a 2-bit field at bits [2p, 2p+1] of
-// a 16-bit half is the subnormal fp16 number code * 2^(2p-24), exactly; the
-// power of two is folded into B (scores) or removed in the epilogue (values).
+// fp16 high part and an fp16 residual (scaled by 2^11 so it stays a normal
+// number), which keeps products at fp32 accuracy.  Codes become fp16 operands
+// with one shift and one AND: a 2-bit field moved to bits 8-9 of a 16-bit half
+// is the fp16 number code * 2^-16, exactly; the power of two is folded into the
+// score constants and removed in the value epilogue.
+//
+// Kernel chain of one decode call: qprep -> decode -> combine, each launched as
+// a programmatic dependent of the previous kernel (griddepcontrol), so each one
+// is resident and waiting when its predecessor finishes.
 #include "kvq_internal.cuh"
 
 #include <math.h>
@@ -49,113 +58,486 @@ DecodeWs decode_ws_layout(int batch, int Hkv, int H, int splits, bool int2) {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kStagesInt2 = 4;
 constexpr int kStagesBf16 = 3;
 
-// ---------------------------------------------------------------------------
-// Query preparation: q_rot = q R_K for the G query heads of one (b, kv), then
-// the scores' B fragments.  B[row][col] for k-block w holds q_rot[head][16w+row]
-// * 2^(e_head) * 2^(beta_w), split into fp16 hi / lo by col parity, where
-// 2^e_head brings max|q_rot| into [16, 32) and 2^beta_w cancels the code scale of
-// position w (see the file comment).  Per head also: kappa = sm_scale*log2e *
-// 2^(14 - e) and zeta = sm_scale*log2e * sum(q_rot).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* __restrict__ RK,
-                                                    float log2_scale) {
-  __shared__ float qs[kMaxG][kDim];
-  __shared__ float qr[kMaxG][kDim];
-  __shared__ float red_sum[kMaxG][4], red_max[kMaxG][4];
-  __shared__ int e_sh[kMaxG];
-  const int b = blockIdx.x, kv = blockIdx.y, i = threadIdx.x;
-  const int G = a.G;
-  const float* R = RK + static_cast<size_t>(kv) * kDim * kDim;
-  for (int h = 0; h < kMaxG; ++h) {
-    float v = 0.0f;
-    if (h < G) {
-      const uint16_t bits = a.q[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + i];
-      v = __uint_as_float(static_cast<uint32_t>(bits) << 16);
-    }
-    qs[h][i] = v;
-  }
-  __syncthreads();
-  float acc[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int j = 0; j < kDim; ++j) {
-    const float r = R[j * kDim + i];
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h) acc[h] = fmaf(qs[h][j], r, acc[h]);
-  }
-  const int warp = i >> 5, lane = i & 31;
-#pragma unroll
-  for (int h = 0; h < kMaxG; ++h) {
-    qr[h][i] = acc[h];
-    float s = acc[h], m = fabsf(acc[h]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      s += __shfl_xor_sync(0xffffffffu, s, off);
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    }
-    if (lane == 0) {
-      red_sum[h][warp] = s;
-      red_max[h][warp] = m;
-    }
-  }
-  __syncthreads();
-  if (i < kMaxG) {
-    const int h = i;
-    const float s = red_sum[h][0] + red_sum[h][1] + red_sum[h][2] + red_sum[h][3];
-    const float m = fmaxf(fmaxf(red_max[h][0], red_max[h][1]), fmaxf(red_max[h][2], red_max[h][3]));
-    int e = 0;
-    if (m > 0.0f && m < INFINITY) {
-      int E;
-      frexpf(m, &E);             // m = f * 2^E, f in [0.5, 1)
-      e = 5 - E;                 // m * 2^e in [16, 32)
-    }
-    e_sh[h] = e;
-    float* qm = const_cast<float*>(a.qmeta) + (static_cast<size_t>(b) * a.Hkv + kv) * 8;
-    qm[2 * h] = (h < G) ? log2_scale * ldexpf(1.0f, 14 - e) : 0.0f;
-    qm[2 * h + 1] = (h < G) ? log2_scale * s : 0.0f;
-  }
-  __syncthreads();
-  // 32 lanes x 16 registers; thread i writes registers 4*(i&3) .. +3 of lane i>>2
-  const int L = i >> 2, g = L >> 2, t = L & 3;
-  const int head = g >> 1, part = g & 1;
-  uint32_t* dst = const_cast<uint32_t*>(a.qfrag) + ((static_cast<size_t>(b) * a.Hkv + kv) * 32 + L) * 16;
-  uint32_t out[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int r = 4 * (i & 3) + k;
-    const int w = r >> 1, which = r & 1;
-    const int row = 16 * w + 2 * t + 8 * which;
-    const int beta = (w <= 4) ? (10 - 2 * w) : (20 - 2 * w);
-    float v[2] = {0.0f, 0.0f};
-    if (head < G) {
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const float x = ldexpf(qr[head][row + u], e_sh[head] + beta);
-        const __half hi = __float2half_rn(x);
-        v[u] = part ? (x - __half2float(hi)) : __half2float(hi);
-      }
-    }
-    out[k] = pack_half2(v[0], v[1]);
-  }
-  *reinterpret_cast<uint4*>(dst + 4 * (i & 3)) = make_uint4(out[0], out[1], out[2], out[3]);
+// Programmatic dependent launch (no-ops when the kernel is launched normally).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Per-warp page-id supply: lane j holds the page id of the warp's page 32*blk + j.
-struct PageIds {
-  int cur, nxt, blk;
+// ---------------------------------------------------------------------------
+// Query preparation: q_rot = q R_K for the G query heads of kQB sequences and one
+// KV head per CTA (R_K staged once in shared memory by a bulk copy), then the
+// scores' B fragments.  B[row][col] for k-block w holds x = q_rot[head][16w+row]
+// * 2^(e_head), where 2^e_head brings max|q_rot| into [2^13, 2^14): column
+// 2*head is fp16(x), column 2*head+1 the residual (x - fp16(x)) * 2^11.  With
+// codes entering as code * 2^-16 (see the file comment) the score of a token is
+// q_rot . c = 2^(16 - e) * (hi + 2^-11 lo).  Per head also: kappa =
+// sm_scale*log2e * 2^(16 - e) and zeta = sm_scale*log2e * sum(q_rot).
+// Launched as a programmatic dependent of the preceding kernel: it reads only
+// q and R_K, so it may run while a preceding append is still writing pages; it
+// waits for that kernel before it exits, so the decode kernel that waits for
+// this one also sees the appended pages.
+// ---------------------------------------------------------------------------
+constexpr int kQB = 4;                       // sequences per qprep CTA
+constexpr int kQVec = kQB * kMaxG;           // query vectors per qprep CTA
+struct QprepSmem {
+  float R[kDim * kDim];
+  float qs[kQVec][kDim];
+  float qr[kQVec][kDim];
+  float red_sum[kQVec][4], red_max[kQVec][4];
+  int e[kQVec];
+  uint64_t bar;
 };
 
-__device__ __forceinline__ int load_page_id(const int32_t* ptab, int p0, int warp, int count,
-                                            int blk, int lane) {
-  const int i = 32 * blk + lane;
-  return (i < count) ? ptab[p0 + warp + kDecodeWarps * i] : -1;
+__global__ void __launch_bounds__(256) qprep_kernel(DecodeArgs a, const float* __restrict__ RK,
+                                                    float log2_scale) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  QprepSmem& sm = *reinterpret_cast<QprepSmem*>(smem_raw);
+  const int b0 = blockIdx.x * kQB, kv = blockIdx.y, tid = threadIdx.x;
+  const int G = a.G;
+  griddep_launch_dependents();
+  const uint32_t bar = smem_u32(&sm.bar);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, kDim * kDim * 4);
+    bulk_g2s(smem_u32(sm.R), RK + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
+  }
+  for (int idx = tid; idx < kQVec * kDim; idx += 256) {
+    const int v = idx / kDim, j = idx % kDim;
+    const int b = b0 + v / kMaxG, h = v % kMaxG;
+    float x = 0.0f;
+    if (b < a.batch && h < G) {
+      const uint16_t bits = a.q[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + j];
+      x = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+    }
+    sm.qs[v][j] = x;
+  }
+  const bool ok = mbar_wait_bounded(bar, 0);
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+    griddep_wait();
+    return;
+  }
+  // thread: output element i of vectors half*8 .. half*8+7
+  {
+    const int i = tid & (kDim - 1), half = tid >> 7;
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+#pragma unroll 4
+    for (int j = 0; j < kDim; ++j) {
+      const float r = sm.R[j * kDim + i];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = fmaf(sm.qs[half * 8 + k][j], r, acc[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) sm.qr[half * 8 + k][i] = acc[k];
+  }
+  __syncthreads();
+  // per-vector sum and max|.|: warp w handles vectors 2w, 2w+1
+  {
+    const int w = tid >> 5, lane = tid & 31;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int v = 2 * w + u;
+      float s = 0.0f, m = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float x = sm.qr[v][lane + 32 * k];
+        s += x;
+        m = fmaxf(m, fabsf(x));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, off);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      }
+      if (lane == 0) {
+        int e = 0;
+        if (m > 0.0f && m < INFINITY) {
+          int E;
+          frexpf(m, &E);         // m = f * 2^E, f in [0.5, 1)
+          e = 14 - E;            // m * 2^e in [2^13, 2^14)
+        }
+        sm.e[v] = e;
+        const int b = b0 + v / kMaxG, h = v % kMaxG;
+        if (b < a.batch) {
+          float* qm = const_cast<float*>(a.qmeta) + (static_cast<size_t>(b) * a.Hkv + kv) * 8;
+          qm[2 * h] = (h < G) ? log2_scale * ldexpf(1.0f, 16 - e) : 0.0f;
+          qm[2 * h + 1] = (h < G) ? log2_scale * s : 0.0f;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // B fragments: per sequence 32 lanes x 16 registers; thread writes 8 registers
+  for (int idx = tid; idx < kQB * 32 * 4; idx += 256) {
+    const int bb = idx / 128, L = (idx / 4) % 32, quad = idx % 4;
+    const int b = b0 + bb;
+    if (b >= a.batch) continue;
+    const int g = L >> 2, t = L & 3, head = g >> 1, part = g & 1;
+    const int v = bb * kMaxG + head;
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = 4 * quad + k;
+      const int w = r >> 1, which = r & 1;
+      const int row = 16 * w + 2 * t + 8 * which;
+      float x2[2] = {0.0f, 0.0f};
+      if (head < G) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float x = ldexpf(sm.qr[v][row + u], sm.e[v]);
+          const __half hi = __float2half_rn(x);
+          x2[u] = part ? (x - __half2float(hi)) * 2048.0f : __half2float(hi);
+        }
+      }
+      out[k] = pack_half2(x2[0], x2[1]);
+    }
+    uint32_t* dst = const_cast<uint32_t*>(a.qfrag) +
+                    ((static_cast<size_t>(b) * a.Hkv + kv) * 32 + L) * 16 + 4 * quad;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+  griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
-// Shared epilogue: reduce l and the z-term over the 8 lanes of a head, hand the
-// warp's (m, l, o[128]) per head to shared memory, merge the 4 warps and write
-// the CTA's split partial.
+// INT2 split-K decode kernel.
+// ---------------------------------------------------------------------------
+
+// fp16x2 operand of code position P (0..7) of a fragment word: the fields at
+// bits [2P, 2P+1] and [16+2P, 17+2P] moved to bits 8-9 of their half, i.e. the
+// fp16 numbers code * 2^-16 (subnormal for code 1, top mantissa bits).  Tensor
+// cores keep full product precision for such operands; a field left at the low
+// mantissa bits would lose up to ~13 bits of the product.
+template <int P>
+__device__ __forceinline__ uint32_t code_op(uint32_t w) {
+  constexpr uint32_t kM = 0x03000300u;
+  if constexpr (P < 4) return (w << (8 - 2 * P)) & kM;
+  else return (w >> (2 * P - 8)) & kM;
+}
+
+// Scores of one page for this lane: tokens g and g+8 of head t (qc, before the
+// per-token scale/zero).  kw: the lane's K-code words {tok g h0, tok g h1,
+// tok g+8 h0, tok g+8 h1}; A fragment = {tok g lo dims, tok g+8 lo, tok g hi,
+// tok g+8 hi}.
+__device__ __forceinline__ void page_scores(const uint4& kw, const uint32_t (&qf)[16],
+                                            float (&s)[4]) {
+  // two accumulators (even / odd k-blocks) halve the dependent tensor-core chain
+  float e[4] = {0.0f, 0.0f, 0.0f, 0.0f}, o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#define KVQ_KSTEP(ACC, P) \
+  mma_f16(ACC, code_op<P>(kw.x), code_op<P>(kw.z), code_op<P>(kw.y), code_op<P>(kw.w), \
+          qf[2 * (P)], qf[2 * (P) + 1])
+  KVQ_KSTEP(e, 0); KVQ_KSTEP(o, 1); KVQ_KSTEP(e, 2); KVQ_KSTEP(o, 3);
+  KVQ_KSTEP(e, 4); KVQ_KSTEP(o, 5); KVQ_KSTEP(e, 6); KVQ_KSTEP(o, 7);
+#undef KVQ_KSTEP
+#pragma unroll
+  for (int k = 0; k < 4; ++k) s[k] = e[k] + o[k];
+}
+
+// O^T[dims][cols] += Vcode^T . P for one page.  vw: the lane's V-code words
+// {toks 2t|2t+1 dim g, dim g+8, toks 2t+8|2t+9 dim g, dim g+8}.
+__device__ __forceinline__ void page_values(const uint4& vw, uint32_t pb0, uint32_t pb1,
+                                            float (&acc)[8][4]) {
+#define KVQ_VSTEP(P) \
+  mma_f16(acc[P], code_op<P>(vw.x), code_op<P>(vw.y), code_op<P>(vw.z), code_op<P>(vw.w), pb0, pb1)
+  KVQ_VSTEP(0); KVQ_VSTEP(1); KVQ_VSTEP(2); KVQ_VSTEP(3);
+  KVQ_VSTEP(4); KVQ_VSTEP(5); KVQ_VSTEP(6); KVQ_VSTEP(7);
+#undef KVQ_VSTEP
+}
+
+// B fragments of the value product from this lane's weights of tokens g and
+// g+8 (head t): column 2*head holds the fp16 weight, column 2*head+1 the
+// residual scaled by 2^11.  Lane (g, t) needs head g>>1, tokens 2t, 2t+1,
+// 2t+8, 2t+9, held by lanes 4*(2t) + (g>>1) and 4*(2t+1) + (g>>1).
+__device__ __forceinline__ void weights_to_b(float P0, float P1, int g, int t, uint32_t& pb0,
+                                             uint32_t& pb1) {
+  const uint32_t X = pack_half2(P0, P1);
+  const uint32_t Y = pack_half2((P0 - half_lo(X)) * 2048.0f, (P1 - half_hi(X)) * 2048.0f);
+  const int src0 = 4 * (2 * t) + (g >> 1);
+  const uint32_t xa = __shfl_sync(0xffffffffu, X, src0);
+  const uint32_t ya = __shfl_sync(0xffffffffu, Y, src0);
+  const uint32_t xb = __shfl_sync(0xffffffffu, X, src0 + 4);
+  const uint32_t yb = __shfl_sync(0xffffffffu, Y, src0 + 4);
+  const uint32_t va = (g & 1) ? ya : xa;
+  const uint32_t vb = (g & 1) ? yb : xb;
+  pb0 = __byte_perm(va, vb, 0x5410);
+  pb1 = __byte_perm(va, vb, 0x7632);
+}
+
+constexpr int kW = kInt2Warps;                 // warps per CTA
+constexpr int kNS = 4;                         // pipeline stages
+constexpr int kStageBytes = 2 * kW * kInt2Rec; // 2 pages x (8/HPC) x HPC heads
+constexpr int kMaxIds = 1024;                  // page ids staged per sub-chunk
+
+struct Int2Smem {
+  uint8_t ring[kNS][kStageBytes];
+  uint64_t full[kNS];
+  int cnt[kNS];
+  int ids[kMaxIds];
+  float o[kW][kMaxG][kDim];
+  float m[kW][kMaxG];
+  float l[kW][kMaxG];
+};
+
+// Weights are kept <= 2^kLazy relative to the running max before it is raised.
+constexpr float kLazy = 8.0f;
+
+// Fill stage `k` of the current sub-chunk (single thread).
+__device__ __forceinline__ void issue_stage(Int2Smem& sm, const DecodeArgs& a, int k, int slot,
+                                            int nsub, int PPS, int HPC, int hg) {
+  const uint32_t rec_bytes = static_cast<uint32_t>(HPC) * kInt2Rec;
+  uint32_t bytes = 0;
+  for (int u = 0; u < PPS; ++u) {
+    const int li = k * PPS + u;
+    if (li < nsub && sm.ids[li] >= 0) bytes += rec_bytes;
+  }
+  const uint32_t bar = smem_u32(&sm.full[slot]);
+  if (bytes == 0) {
+    mbar_arrive(bar);
+    return;
+  }
+  mbar_arrive_expect_tx(bar, bytes);
+  for (int u = 0; u < PPS; ++u) {
+    const int li = k * PPS + u;
+    if (li >= nsub) break;
+    const int id = sm.ids[li];
+    if (id < 0) continue;
+    bulk_g2s(smem_u32(&sm.ring[slot][u * rec_bytes]),
+             a.pool + (static_cast<size_t>(id) * a.Hkv + static_cast<size_t>(hg) * HPC) * kInt2Rec,
+             rec_bytes, bar);
+  }
+}
+
+__global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Int2Smem& sm = *reinterpret_cast<Int2Smem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int split = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  const int HPC = a.hpc, GPH = kW / HPC, PPS = 2 * GPH;
+  const int hl = warp / GPH, gi = warp % GPH;
+  const int kv = hg * HPC + hl;
+
+  if (tid == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      sm.cnt[s] = 0;
+    }
+    fence_mbar_init();
+  }
+  griddep_wait();      // inputs (pool, tables, rotated queries) come from predecessors
+
+  int seq_len = a.seq_lens[b];
+  if (seq_len < 0 || seq_len > a.max_pages * kPage) {
+    if (tid == 0 && split == 0 && hg == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
+    seq_len = 0;
+  }
+  const int n_pages = (seq_len + kPage - 1) / kPage;
+  const int p0 = split * a.chunk_pages;
+  const int npg = max(0, min(p0 + a.chunk_pages, n_pages) - p0);
+  const int32_t* ptab = a.page_table + static_cast<size_t>(b) * a.max_pages;
+
+  // B fragments of the rotated query and the head's logit constants
+  uint32_t qf[16];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.qfrag + ((static_cast<size_t>(b) * a.Hkv + kv) * 32 + lane) * 16);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint4 v = src[r];
+      qf[4 * r] = v.x; qf[4 * r + 1] = v.y; qf[4 * r + 2] = v.z; qf[4 * r + 3] = v.w;
+    }
+  }
+  const float kappa = a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * 8 + 2 * t];
+  const float zeta = a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * 8 + 2 * t + 1];
+
+  float acc[8][4];
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[mb][k] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f, z_run = 0.0f;
+
+  int gs = 0;            // stages consumed so far (ring phase)
+  bool timed_out = false;
+  for (int sub = 0; sub < npg && !timed_out; sub += kMaxIds) {
+    const int nsub = min(kMaxIds, npg - sub);
+    for (int i = tid; i < nsub; i += kW * 32) {
+      const int id = ptab[p0 + sub + i];
+      const bool ok = id >= 0 && id < a.num_pool_pages;
+      if (!ok) atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+      sm.ids[i] = ok ? id : -1;
+    }
+    __syncthreads();
+    const int nst = (nsub + PPS - 1) / PPS;
+    if (tid == 0)
+      for (int k = 0; k < kNS && k < nst; ++k) issue_stage(sm, a, k, (gs + k) % kNS, nsub, PPS, HPC, hg);
+
+    for (int k = 0; k < nst; ++k) {
+      const int slot = (gs + k) % kNS;
+      if (!mbar_wait_bounded(smem_u32(&sm.full[slot]), ((gs + k) / kNS) & 1)) {
+        if (lane == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+        timed_out = true;
+        break;
+      }
+      const int ua = k * PPS + gi, ub = ua + GPH;
+      const bool oka = ua < nsub && sm.ids[ua] >= 0;
+      const bool okb = ub < nsub && sm.ids[ub] >= 0;
+      const uint8_t* sta = &sm.ring[slot][(gi * HPC + hl) * kInt2Rec];
+      const uint8_t* stb = &sm.ring[slot][((GPH + gi) * HPC + hl) * kInt2Rec];
+      const uint4 kwa = *reinterpret_cast<const uint4*>(sta + 16 * lane);
+      const uint4 vwa = *reinterpret_cast<const uint4*>(sta + 512 + 16 * lane);
+      const uint4 mta = *reinterpret_cast<const uint4*>(sta + 1024 + 16 * g);
+      const uint4 kwb = *reinterpret_cast<const uint4*>(stb + 16 * lane);
+      const uint4 vwb = *reinterpret_cast<const uint4*>(stb + 512 + 16 * lane);
+      const uint4 mtb = *reinterpret_cast<const uint4*>(stb + 1024 + 16 * g);
+      __syncwarp();
+      if (lane == 0) {
+        // release the stage; the last of the kW warps refills it
+        __threadfence_block();
+        const int prev = atomicAdd(&sm.cnt[slot], 1);
+        if (prev == kW - 1) {
+          sm.cnt[slot] = 0;
+          if (k + kNS < nst) {
+            fence_proxy_async();
+            issue_stage(sm, a, k + kNS, slot, nsub, PPS, HPC, hg);
+          }
+        }
+      }
+      const int posa = (p0 + sub + ua) * kPage, posb = (p0 + sub + ub) * kPage;
+      const bool va0 = oka && (posa + g < seq_len), va1 = oka && (posa + g + 8 < seq_len);
+      const bool vb0 = okb && (posb + g < seq_len), vb1 = okb && (posb + g + 8 < seq_len);
+
+      // ---- scores of both pages (independent tensor-core chains)
+      float sa4[4], sb4[4];
+      page_scores(kwa, qf, sa4);
+      page_scores(kwb, qf, sb4);
+      // logit (log2 units) = kappa * s_k * qc + zeta * z_k; qc = hi col + 2^-11 lo col
+      const float la0 = va0 ? fmaf(kappa * half_lo(mta.x), fmaf(sa4[1], 1.0f / 2048.0f, sa4[0]),
+                                   zeta * half_hi(mta.x)) : -INFINITY;
+      const float la1 = va1 ? fmaf(kappa * half_lo(mta.y), fmaf(sa4[3], 1.0f / 2048.0f, sa4[2]),
+                                   zeta * half_hi(mta.y)) : -INFINITY;
+      const float lb0 = vb0 ? fmaf(kappa * half_lo(mtb.x), fmaf(sb4[1], 1.0f / 2048.0f, sb4[0]),
+                                   zeta * half_hi(mtb.x)) : -INFINITY;
+      const float lb1 = vb1 ? fmaf(kappa * half_lo(mtb.y), fmaf(sb4[3], 1.0f / 2048.0f, sb4[2]),
+                                   zeta * half_hi(mtb.y)) : -INFINITY;
+
+      // ---- online softmax.  The value weights P = p * s_v feed fp16 operands, so
+      // the running max m is kept over lv = logit + log2(s_v) and raised only when
+      // some lv exceeds m + kLazy: then p * s_v <= 2^kLazy for every token seen and
+      // P * 2^(14 - kLazy) stays below 2^14.  p = 2^(logit - m) itself may be large
+      // (at most 2^(kLazy + 24)); it is only summed in fp32.
+      const float sva0 = half_lo(mta.z), sva1 = half_lo(mta.w);
+      const float svb0 = half_lo(mtb.z), svb1 = half_lo(mtb.w);
+      const float lva0 = la0 + fmaxf(fast_log2(sva0), -24.0f);
+      const float lva1 = la1 + fmaxf(fast_log2(sva1), -24.0f);
+      const float lvb0 = lb0 + fmaxf(fast_log2(svb0), -24.0f);
+      const float lvb1 = lb1 + fmaxf(fast_log2(svb1), -24.0f);
+      const float lmax = fmaxf(fmaxf(lva0, lva1), fmaxf(lvb0, lvb1));
+      if (__any_sync(0xffffffffu, lmax > m_run + kLazy)) {
+        float pm = lmax;
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+        if (pm > m_run) {
+          const float f = fast_exp2(m_run - pm);
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[mb][q] *= f;
+          l_run *= f;
+          z_run *= f;
+          m_run = pm;
+        }
+      }
+      const float pa0 = va0 ? fast_exp2(la0 - m_run) : 0.0f;
+      const float pa1 = va1 ? fast_exp2(la1 - m_run) : 0.0f;
+      const float pb0v = vb0 ? fast_exp2(lb0 - m_run) : 0.0f;
+      const float pb1v = vb1 ? fast_exp2(lb1 - m_run) : 0.0f;
+      l_run += (pa0 + pa1) + (pb0v + pb1v);
+      constexpr float kWScale = 64.0f;      // 2^(14 - kLazy)
+      float Pa0 = 0.0f, Pa1 = 0.0f, Pb0 = 0.0f, Pb1 = 0.0f;
+      if (va0) { Pa0 = pa0 * (sva0 * kWScale); z_run = fmaf(pa0, half_hi(mta.z), z_run); }
+      if (va1) { Pa1 = pa1 * (sva1 * kWScale); z_run = fmaf(pa1, half_hi(mta.w), z_run); }
+      if (vb0) { Pb0 = pb0v * (svb0 * kWScale); z_run = fmaf(pb0v, half_hi(mtb.z), z_run); }
+      if (vb1) { Pb1 = pb1v * (svb1 * kWScale); z_run = fmaf(pb1v, half_hi(mtb.w), z_run); }
+
+      // ---- values of both pages
+      uint32_t fa0, fa1, fb0, fb1;
+      weights_to_b(Pa0, Pa1, g, t, fa0, fa1);
+      weights_to_b(Pb0, Pb1, g, t, fb0, fb1);
+      page_values(vwa, fa0, fa1, acc);
+      page_values(vwb, fb0, fb1, acc);
+    }
+    gs += nst;
+    __syncthreads();     // sm.ids is reloaded for the next sub-chunk
+  }
+  if (timed_out) {
+    // A wait gave up: let the copies already issued land (bounded) before the
+    // CTA can exit, so no bulk copy targets freed shared memory.
+    for (int s = 0; s < kNS; ++s) mbar_wait_bounded(smem_u32(&sm.full[s]), 0);
+  }
+  griddep_launch_dependents();
+
+  // ---- warp epilogue: (m, l, o) of the warp's KV head for its G query heads
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
+    z_run += __shfl_xor_sync(0xffffffffu, z_run, off);
+  }
+  if (t < a.G) {
+    // undo the code scale 2^-16 and the weight scale 2^(14 - kLazy) = 2^6;
+    // the residual column carries a further 2^11
+    constexpr float kInv = 1024.0f;       // 2^(16 - 6)
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      sm.o[warp][t][16 * mb + g] = fmaf(fmaf(acc[mb][1], 1.0f / 2048.0f, acc[mb][0]), kInv, z_run);
+      sm.o[warp][t][16 * mb + g + 8] = fmaf(fmaf(acc[mb][3], 1.0f / 2048.0f, acc[mb][2]), kInv, z_run);
+    }
+    if (g == 0) {
+      sm.m[warp][t] = m_run;
+      sm.l[warp][t] = l_run;
+    }
+  }
+  __syncthreads();
+  // ---- merge the 8/HPC warps of each head and write the split partials
+  for (int idx = tid; idx < HPC * kDim; idx += kW * 32) {
+    const int h2 = idx / kDim, d = idx % kDim;
+    for (int h = 0; h < a.G; ++h) {
+      float M = -INFINITY;
+      for (int u = 0; u < GPH; ++u) M = fmaxf(M, sm.m[h2 * GPH + u][h]);
+      float L = 0.0f, o = 0.0f;
+      if (M > -INFINITY) {
+        for (int u = 0; u < GPH; ++u) {
+          const int w = h2 * GPH + u;
+          if (sm.m[w][h] == -INFINITY) continue;
+          const float f = fast_exp2(sm.m[w][h] - M);
+          L = fmaf(f, sm.l[w][h], L);
+          o = fmaf(f, sm.o[w][h][d], o);
+        }
+      }
+      float* p = a.part + ((static_cast<size_t>(b) * a.H + (hg * HPC + h2) * a.G + h) * a.splits + split) *
+                              kPartStride;
+      p[4 + d] = o;
+      if (d == 0) {
+        p[0] = M;
+        p[1] = L;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// BF16 split-K decode kernel (comparison point): per-warp rings of whole
+// pages, bf16 operands read straight from the staged page, plain logits
+// q.k * sm_scale.  The 4 warps of a CTA take every 4th page of the split.
 // ---------------------------------------------------------------------------
 struct CtaCombineSmem {
   float o[kDecodeWarps][kMaxG][kDim];
@@ -163,8 +545,8 @@ struct CtaCombineSmem {
   float l[kDecodeWarps][kMaxG];
 };
 
-__device__ __forceinline__ void cta_combine_and_store(CtaCombineSmem& cs, const DecodeArgs& a,
-                                                      int b, int kv, int split) {
+__device__ __forceinline__ void write_partial_bf16(CtaCombineSmem& cs, const DecodeArgs& a, int b,
+                                                   int kv, int split) {
   __syncthreads();
   const int d = threadIdx.x;
   for (int h = 0; h < a.G; ++h) {
@@ -190,223 +572,17 @@ __device__ __forceinline__ void cta_combine_and_store(CtaCombineSmem& cs, const 
   }
 }
 
-// ---------------------------------------------------------------------------
-// INT2 split-K decode kernel.
-// ---------------------------------------------------------------------------
-struct Int2Smem {
-  uint8_t ring[kDecodeWarps][kStagesInt2][kInt2Rec];
-  uint64_t bar[kDecodeWarps][kStagesInt2];
-  int ids[kDecodeWarps][kStagesInt2];
-  CtaCombineSmem comb;
+// Per-warp page-id supply: lane j holds the page id of the warp's page 32*blk + j.
+struct PageIds {
+  int cur, nxt, blk;
 };
 
-__global__ void __launch_bounds__(kDecodeThreads, 4) decode_int2_kernel(DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  Int2Smem& sm = *reinterpret_cast<Int2Smem*>(smem_raw);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
-
-  int seq_len = a.seq_lens[b];
-  if (seq_len < 0 || seq_len > a.max_pages * kPage) {
-    if (threadIdx.x == 0 && split == 0 && kv == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
-    seq_len = 0;
-  }
-  const int n_pages = (seq_len + kPage - 1) / kPage;
-  const int p0 = split * a.chunk_pages;
-  const int p1 = min(p0 + a.chunk_pages, n_pages);
-  const int count = (p1 - p0 > warp) ? (p1 - p0 - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
-  const int32_t* ptab = a.page_table + static_cast<size_t>(b) * a.max_pages;
-  const uint8_t* pool_kv = a.pool + static_cast<size_t>(kv) * kInt2Rec;
-  const size_t page_stride = static_cast<size_t>(a.Hkv) * kInt2Rec;
-
-  if (lane == 0) {
-    for (int s = 0; s < kStagesInt2; ++s) mbar_init(smem_u32(&sm.bar[warp][s]), 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
-  PageIds ids;
-  ids.blk = 0;
-  ids.cur = load_page_id(ptab, p0, warp, count, 0, lane);
-  ids.nxt = load_page_id(ptab, p0, warp, count, 1, lane);
-
-  // issue page j of this warp (all lanes call; lane 0 copies)
-  auto issue = [&](int j) {
-    if ((j >> 5) != ids.blk) {
-      ids.blk = j >> 5;
-      ids.cur = ids.nxt;
-      ids.nxt = load_page_id(ptab, p0, warp, count, ids.blk + 1, lane);
-    }
-    const int id = __shfl_sync(0xffffffffu, ids.cur, j & 31);
-    if (lane == 0) {
-      const int slot = j % kStagesInt2;
-      const uint32_t bar = smem_u32(&sm.bar[warp][slot]);
-      const bool ok = id >= 0 && id < a.num_pool_pages;
-      sm.ids[warp][slot] = ok ? id : -1;
-      if (ok) {
-        mbar_arrive_expect_tx(bar, kInt2Rec);
-        bulk_g2s(smem_u32(sm.ring[warp][slot]), pool_kv + static_cast<size_t>(id) * page_stride,
-                 kInt2Rec, bar);
-      } else {
-        atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
-        mbar_arrive(bar);
-      }
-    }
-  };
-  for (int j = 0; j < kStagesInt2 && j < count; ++j) issue(j);
-  __syncwarp();
-
-  // B fragments of the rotated query and the head's logit constants
-  uint32_t qf[16];
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(
-        a.qfrag + ((static_cast<size_t>(b) * a.Hkv + kv) * 32 + lane) * 16);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint4 v = src[r];
-      qf[4 * r] = v.x; qf[4 * r + 1] = v.y; qf[4 * r + 2] = v.z; qf[4 * r + 3] = v.w;
-    }
-  }
-  const float kappa = a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * 8 + 2 * t];
-  const float zeta = a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * 8 + 2 * t + 1];
-
-  float acc[8][4];
-#pragma unroll
-  for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) acc[mb][k] = 0.0f;
-  float m_run = -INFINITY, l_run = 0.0f, z_run = 0.0f;
-
-  int i = 0;
-  for (; i < count; ++i) {
-    const int slot = i % kStagesInt2;
-    const uint32_t parity = (i / kStagesInt2) & 1;
-    if (!mbar_wait_bounded(smem_u32(&sm.bar[warp][slot]), parity)) {
-      if (lane == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
-      break;
-    }
-    const bool page_ok = sm.ids[warp][slot] >= 0;
-    const uint8_t* st = sm.ring[warp][slot];
-    const uint4 kw = *reinterpret_cast<const uint4*>(st + 16 * lane);
-    const uint4 vw = *reinterpret_cast<const uint4*>(st + 512 + 16 * lane);
-    const uint4 mt = *reinterpret_cast<const uint4*>(st + 1024 + 16 * g);
-    __syncwarp();
-    if (i + kStagesInt2 < count) {
-      if (lane == 0) fence_proxy_async();
-      issue(i + kStagesInt2);
-    }
-    const int pos0 = (p0 + warp + kDecodeWarps * i) * kPage;
-    const bool v0 = page_ok && (pos0 + g < seq_len);
-    const bool v1 = page_ok && (pos0 + g + 8 < seq_len);
-
-    // ---- scores: S[16 tokens][8 cols], k-block w = code position w
-    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int p = 0; p < 5; ++p) {
-      const uint32_t m = 0x00030003u << (2 * p);
-      mma_f16(s, kw.x & m, kw.z & m, kw.y & m, kw.w & m, qf[2 * p], qf[2 * p + 1]);
-    }
-    {
-      const uint32_t k0 = kw.x >> 10, k1 = kw.y >> 10, k2 = kw.z >> 10, k3 = kw.w >> 10;
-#pragma unroll
-      for (int p = 5; p < 8; ++p) {
-        const uint32_t m = 0x00030003u << (2 * (p - 5));
-        mma_f16(s, k0 & m, k2 & m, k1 & m, k3 & m, qf[2 * p], qf[2 * p + 1]);
-      }
-    }
-    // logit (log2 units) = kappa * s_k * (q.c) + zeta * z_k, tokens g and g+8, head t
-    const float l0 = v0 ? fmaf(kappa * half_lo(mt.x), s[0] + s[1], zeta * half_hi(mt.x)) : -INFINITY;
-    const float l1 = v1 ? fmaf(kappa * half_lo(mt.y), s[2] + s[3], zeta * half_hi(mt.y)) : -INFINITY;
-
-    // ---- online softmax over the 16 tokens of this page (lanes 4g+t share head t)
-    float pm = fmaxf(l0, l1);
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-    if (pm > m_run) {
-      const float f = fast_exp2(m_run - pm);
-#pragma unroll
-      for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) acc[mb][k] *= f;
-      l_run *= f;
-      z_run *= f;
-      m_run = pm;
-    }
-    const float p0v = v0 ? fast_exp2(l0 - m_run) : 0.0f;
-    const float p1v = v1 ? fast_exp2(l1 - m_run) : 0.0f;
-    l_run += p0v + p1v;
-    float P0 = 0.0f, P1 = 0.0f;
-    if (v0) {
-      P0 = p0v * half_lo(mt.z);
-      z_run = fmaf(p0v, half_hi(mt.z), z_run);
-    }
-    if (v1) {
-      P1 = p1v * half_lo(mt.w);
-      z_run = fmaf(p1v, half_hi(mt.w), z_run);
-    }
-    // ---- P (scaled by s_v) as B fragments of the value product, hi/lo fp16
-    const uint32_t X = pack_half2(P0, P1);
-    const uint32_t Y = pack_half2(P0 - half_lo(X), P1 - half_hi(X));
-    const int src0 = 4 * (2 * t) + (g >> 1);
-    const uint32_t xa = __shfl_sync(0xffffffffu, X, src0);
-    const uint32_t ya = __shfl_sync(0xffffffffu, Y, src0);
-    const uint32_t xb = __shfl_sync(0xffffffffu, X, src0 + 4);
-    const uint32_t yb = __shfl_sync(0xffffffffu, Y, src0 + 4);
-    const uint32_t va = (g & 1) ? ya : xa;
-    const uint32_t vb = (g & 1) ? yb : xb;
-    const uint32_t pb0 = __byte_perm(va, vb, 0x5410);
-    const uint32_t pb1 = __byte_perm(va, vb, 0x7632);
-
-    // ---- values: O^T[dims of m-block mb][8 cols] += Vcode^T . P
-#pragma unroll
-    for (int mb = 0; mb < 5; ++mb) {
-      const uint32_t m = 0x00030003u << (2 * mb);
-      mma_f16(acc[mb], vw.x & m, vw.y & m, vw.z & m, vw.w & m, pb0, pb1);
-    }
-    {
-      const uint32_t u0 = vw.x >> 10, u1 = vw.y >> 10, u2 = vw.z >> 10, u3 = vw.w >> 10;
-#pragma unroll
-      for (int mb = 5; mb < 8; ++mb) {
-        const uint32_t m = 0x00030003u << (2 * (mb - 5));
-        mma_f16(acc[mb], u0 & m, u1 & m, u2 & m, u3 & m, pb0, pb1);
-      }
-    }
-  }
-  if (i < count) {
-    // A wait gave up: let the copies already issued for this warp land (bounded)
-    // before the CTA can exit, so no bulk copy targets freed shared memory.
-    for (int j = i + 1; j < count && j < i + kStagesInt2; ++j)
-      mbar_wait_bounded(smem_u32(&sm.bar[warp][j % kStagesInt2]), (j / kStagesInt2) & 1);
-  }
-
-  // ---- warp epilogue
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
-    z_run += __shfl_xor_sync(0xffffffffu, z_run, off);
-  }
-  if (t < a.G) {
-#pragma unroll
-    for (int mb = 0; mb < 8; ++mb) {
-      const float inv_alpha = (mb <= 4) ? __int_as_float((127 + 24 - 2 * mb) << 23)
-                                        : __int_as_float((127 + 34 - 2 * mb) << 23);
-      sm.comb.o[warp][t][16 * mb + g] = fmaf(acc[mb][0] + acc[mb][1], inv_alpha, z_run);
-      sm.comb.o[warp][t][16 * mb + g + 8] = fmaf(acc[mb][2] + acc[mb][3], inv_alpha, z_run);
-    }
-    if (g == 0) {
-      sm.comb.m[warp][t] = m_run;
-      sm.comb.l[warp][t] = l_run;
-    }
-  }
-  cta_combine_and_store(sm.comb, a, b, kv, split);
+__device__ __forceinline__ int load_page_id(const int32_t* ptab, int p0, int warp, int count,
+                                            int blk, int lane) {
+  const int i = 32 * blk + lane;
+  return (i < count) ? ptab[p0 + warp + kDecodeWarps * i] : -1;
 }
 
-// ---------------------------------------------------------------------------
-// BF16 split-K decode kernel (comparison point): same skeleton, bf16 operands
-// read straight from the staged page, plain logits q.k * sm_scale.
-// ---------------------------------------------------------------------------
 struct Bf16Smem {
   uint8_t ring[kDecodeWarps][kStagesBf16][kBf16Rec];
   uint64_t bar[kDecodeWarps][kStagesBf16];
@@ -421,6 +597,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodeAr
   const int g = lane >> 2, t = lane & 3;
   const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
 
+  griddep_wait();
   int seq_len = a.seq_lens[b];
   if (seq_len < 0 || seq_len > a.max_pages * kPage) {
     if (threadIdx.x == 0 && split == 0 && kv == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
@@ -558,6 +735,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodeAr
     for (int j = i + 1; j < count && j < i + kStagesBf16; ++j)
       mbar_wait_bounded(smem_u32(&sm.bar[warp][j % kStagesBf16]), (j / kStagesBf16) & 1);
   }
+  griddep_launch_dependents();
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
   if (t < a.G) {
@@ -571,42 +749,63 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodeAr
       sm.comb.l[warp][t] = l_run;
     }
   }
-  cta_combine_and_store(sm.comb, a, b, kv, split);
+  write_partial_bf16(sm.comb, a, b, kv, split);
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp combine of the split partials, then out = o_rot R_V^T.
-// One CTA per (b, query head); thread d owns element d.
+// Log-sum-exp combine of the split partials of one (b, query head), then
+// out = o_rot R_V^T.  Thread d owns element d; the split weights are computed
+// once into shared memory and the partial rows are read with independent loads.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a, const float* __restrict__ RVt,
-                                                      int rotate_out, float* __restrict__ out) {
-  __shared__ float os[kDim];
-  const int bh = blockIdx.x;
-  const int h = bh % a.H, kv = h / a.G;
-  const int d = threadIdx.x;
-  const float* parts = a.part + static_cast<size_t>(bh) * a.splits * kPartStride;
-  float M = -INFINITY;
-  for (int j = 0; j < a.splits; ++j) M = fmaxf(M, parts[j * kPartStride]);
-  float L = 0.0f, o = 0.0f;
-  if (M > -INFINITY) {
-    for (int j = 0; j < a.splits; ++j) {
-      const float mj = parts[j * kPartStride];
-      if (mj == -INFINITY) continue;
-      const float f = fast_exp2(mj - M);
-      L = fmaf(f, parts[j * kPartStride + 1], L);
-      o = fmaf(f, parts[j * kPartStride + 4 + d], o);
-    }
+__device__ __forceinline__ float block_reduce_128(float x, float* red, bool is_max) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float y = __shfl_xor_sync(0xffffffffu, x, off);
+    x = is_max ? fmaxf(x, y) : x + y;
   }
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < 4; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
+  __shared__ float wsp[kMaxSplits];
+  __shared__ float os[kDim];
+  __shared__ float red[4];
+  griddep_wait();
+  const int bh = blockIdx.x, h = bh % a.H, kv = h / a.G, d = threadIdx.x;
+  const int S = a.splits;
+  const float* parts = a.part + static_cast<size_t>(bh) * S * kPartStride;
+  float M = -INFINITY;
+  for (int j = d; j < S; j += 128) M = fmaxf(M, parts[j * kPartStride]);
+  M = block_reduce_128(M, red, true);
+  float L = 0.0f;
+  for (int j = d; j < S; j += 128) {
+    const float mj = parts[j * kPartStride];
+    const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj - M);
+    wsp[j] = w;
+    L = fmaf(w, parts[j * kPartStride + 1], L);
+  }
+  L = block_reduce_128(L, red, false);     // its barriers also publish wsp
+  float o = 0.0f;
+#pragma unroll 8
+  for (int j = 0; j < S; ++j) o = fmaf(wsp[j], parts[j * kPartStride + 4 + d], o);
   o = (L > 0.0f) ? o / L : 0.0f;
-  if (rotate_out) {
+  if (a.rotate_out) {
     os[d] = o;
     __syncthreads();
-    const float* Rt = RVt + static_cast<size_t>(kv) * kDim * kDim;
+    const float* Rt = a.RVt + static_cast<size_t>(kv) * kDim * kDim;
     float r = 0.0f;
-    for (int j = 0; j < kDim; ++j) r = fmaf(os[j], Rt[j * kDim + d], r);
+#pragma unroll 8
+    for (int j = 0; j < kDim; ++j) r = fmaf(os[j], __ldg(Rt + j * kDim + d), r);
     o = r;
   }
-  out[static_cast<size_t>(bh) * kDim + d] = o;
+  a.out[static_cast<size_t>(bh) * kDim + d] = o;
 }
 
 // Dequantise positions [start, start+len) of one sequence: CTA per (position,
@@ -675,34 +874,53 @@ cudaError_t set_smem_attr(Kern kern) {
   return e;
 }
 
+// Launch as a programmatic dependent of the preceding kernel in the stream.
+template <typename... Args>
+cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace
 
 cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, float sm_scale, cudaStream_t st) {
-  dim3 grid(a.batch, a.Hkv);
-  qprep_kernel<<<grid, 128, 0, st>>>(a, RK, sm_scale * kLog2e);
-  return cudaGetLastError();
+  cudaError_t e = set_smem_attr<QprepSmem>(qprep_kernel);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.batch + kQB - 1) / kQB, a.Hkv);
+  e = launch_dependent(qprep_kernel, grid, dim3(256), sizeof(QprepSmem), st, a, RK,
+                       sm_scale * kLog2e);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t st) {
   cudaError_t e = set_smem_attr<Int2Smem>(decode_int2_kernel);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.splits, a.Hkv, a.batch);
-  decode_int2_kernel<<<grid, kDecodeThreads, sizeof(Int2Smem), st>>>(a);
-  return cudaGetLastError();
+  dim3 grid(a.splits, a.Hkv / a.hpc, a.batch);
+  e = launch_dependent(decode_int2_kernel, grid, dim3(kW * 32), sizeof(Int2Smem), st, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t st) {
   cudaError_t e = set_smem_attr<Bf16Smem>(decode_bf16_kernel);
   if (e != cudaSuccess) return e;
   dim3 grid(a.splits, a.Hkv, a.batch);
-  decode_bf16_kernel<<<grid, kDecodeThreads, sizeof(Bf16Smem), st>>>(a);
-  return cudaGetLastError();
+  e = launch_dependent(decode_bf16_kernel, grid, dim3(kDecodeThreads), sizeof(Bf16Smem), st, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_combine(const DecodeArgs& a, const float* RVt, bool rotate_out, float* out,
-                           cudaStream_t st) {
-  combine_kernel<<<a.batch * a.H, 128, 0, st>>>(a, RVt, rotate_out ? 1 : 0, out);
-  return cudaGetLastError();
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st) {
+  cudaError_t e = launch_dependent(combine_kernel, dim3(a.batch * a.H), dim3(128), 0, st, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_dequant(const uint8_t* pool, int num_pool_pages, const int32_t* page_table,
@@ -723,7 +941,7 @@ cudaError_t launch_transpose(const float* in, float* out, int count, cudaStream_
 int decode_int2_ctas_per_sm() {
   if (set_smem_attr<Int2Smem>(decode_int2_kernel) != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel, kDecodeThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel, kW * 32,
                                                     sizeof(Int2Smem)) != cudaSuccess || n < 1)
     return 1;
   return n;

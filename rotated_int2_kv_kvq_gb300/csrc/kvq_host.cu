@@ -56,22 +56,51 @@ size_t rot_floats(int Hkv) {
   return static_cast<size_t>(3) * Hkv * kDim * kDim + static_cast<size_t>(Hkv) * kDim;
 }
 
-// Splits for `batch` sequences: enough CTAs for about four full waves of the
-// GPU, never fewer than 8 pages per split when max_pages is known.
+// KV heads served by one INT2 decode CTA: the largest of 8, 4, 2, 1 dividing Hkv.
+int heads_per_cta(int Hkv) {
+  for (int c = kvq::kInt2Warps; c > 1; c >>= 1)
+    if (Hkv % c == 0) return c;
+  return 1;
+}
+
+long decode_units(const kvq_handle* h, int batch, bool int2) {
+  const int Hkv = h->L.num_kv_heads;
+  return static_cast<long>(batch) * (int2 ? Hkv / heads_per_cta(Hkv) : Hkv);
+}
+
+// Upper bound of the automatic split count for `batch` sequences (sizes the
+// workspace): up to four waves of CTAs.
 int splits_cap(const kvq_handle* h, int batch, bool int2) {
-  const long units = static_cast<long>(batch) * h->L.num_kv_heads;
+  const long units = decode_units(h, batch, int2);
   const long slots = static_cast<long>(h->num_sms) * (int2 ? h->ctas_int2 : h->ctas_bf16);
-  long s = (4 * slots + units - 1) / units;
+  long s = (4 * slots) / units;
   if (s < 1) s = 1;
   if (s > kvq::kMaxSplits) s = kvq::kMaxSplits;
   return static_cast<int>(s);
 }
 
+// Automatic split count: the number of full waves (1..4) of CTAs that fills the
+// GPU best, never with fewer than 8 pages per split.
 int choose_splits(const kvq_handle* h, int batch, int max_pages, bool int2) {
-  int s = splits_cap(h, batch, int2);
+  const long units = decode_units(h, batch, int2);
+  const long slots = static_cast<long>(h->num_sms) * (int2 ? h->ctas_int2 : h->ctas_bf16);
   const int by_pages = (max_pages + 7) / 8;
-  if (s > by_pages) s = by_pages;
-  return s < 1 ? 1 : s;
+  int best = 1;
+  double best_fill = -1.0;
+  for (int waves = 1; waves <= 4; ++waves) {
+    long s = (waves * slots) / units;
+    if (s < 1) s = 1;
+    if (s > by_pages) s = by_pages;
+    if (s > kvq::kMaxSplits) s = kvq::kMaxSplits;
+    const long ctas = s * units;
+    const long used_waves = (ctas + slots - 1) / slots;
+    const double fill = static_cast<double>(ctas) / static_cast<double>(used_waves * slots);
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = static_cast<int>(s);
+    }
+  }
+  return best < 1 ? 1 : best;
 }
 
 void prof_begin(kvq_handle* h, cudaStream_t st, int* slot) {
@@ -142,6 +171,10 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
   a.qfrag = reinterpret_cast<const uint32_t*>(ws + w.qfrag_off);
   a.qmeta = reinterpret_cast<const float*>(ws + w.qmeta_off);
   a.part = reinterpret_cast<float*>(ws + w.part_off);
+  a.hpc = heads_per_cta(a.Hkv);
+  a.out = out;
+  a.RVt = h->bank ? h->bank + static_cast<size_t>(2) * a.Hkv * kDim * kDim : nullptr;
+  a.rotate_out = (int2 && !(h->L.flags & KVQ_OUT_ROTATED)) ? 1 : 0;
   a.status = h->status;
   a.log2_scale = h->sm_scale * 1.4426950408889634f;
   cudaStream_t st = S(stream);
@@ -155,10 +188,7 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
   e = int2 ? kvq::launch_decode_int2(a, st) : kvq::launch_decode_bf16(a, st);
   prof_end(h, st, slot);
   if (e != cudaSuccess) return KVQ_ECUDA;
-  const float* RVt = h->bank ? h->bank + static_cast<size_t>(2) * a.Hkv * kDim * kDim : nullptr;
-  const bool rotate = int2 && !(h->L.flags & KVQ_OUT_ROTATED);
-  e = kvq::launch_combine(a, RVt, rotate, out, st);
-  return cuda_rc(e);
+  return cuda_rc(kvq::launch_combine(a, st));
 }
 
 int append_common(kvq_handle* h, bool int2, void* pool, int num_pool_pages, const uint16_t* K,

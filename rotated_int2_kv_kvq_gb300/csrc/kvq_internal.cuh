@@ -20,9 +20,9 @@ constexpr int kMaxG = 4;           // query heads per KV head handled per CTA
 constexpr int kPartStride = 132;   // floats per split partial: m, l, 2 pad, o[128]
 constexpr int kQFragWords = 32 * 16;   // uint32 per (b, kv): 32 lanes x 16 B-fragment regs
 constexpr int kMaxSplits = 1024;
-constexpr int kDecodeWarps = 4;
+constexpr int kDecodeWarps = 4;    // BF16 decode CTA
+constexpr int kInt2Warps = 8;      // INT2 decode CTA
 constexpr int kDecodeThreads = kDecodeWarps * 32;
-constexpr int kProfMax = 65536;
 
 // Workspace layout of one decode call (offsets in bytes, each 256-aligned).
 struct DecodeWs {
@@ -40,9 +40,13 @@ struct DecodeArgs {
   int batch;
   int H, Hkv, G;
   int splits, chunk_pages;
+  int hpc;                   // KV heads per INT2 decode CTA (1, 2, 4 or 8; divides Hkv)
   const uint32_t* qfrag;     // [B][Hkv][32][16]
   const float* qmeta;        // [B][Hkv][4][2]: kappa, zeta per head
   float* part;               // [B][H][splits][kPartStride]
+  float* out;                // [B][H][D]
+  const float* RVt;          // [Hkv][D][D] transposed value rotations
+  int rotate_out;            // 1: out = o_rot R_V^T, 0: out = o_rot
   uint32_t* status;
   float log2_scale;          // sm_scale * log2(e)
 };
@@ -69,8 +73,7 @@ cudaError_t launch_append_bf16(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, float sm_scale, cudaStream_t st);
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t st);
-cudaError_t launch_combine(const DecodeArgs& a, const float* RVt, bool rotate_out, float* out,
-                           cudaStream_t st);
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_dequant(const uint8_t* pool, int num_pool_pages, const int32_t* page_table,
                            int max_pages, int Hkv, int seq, int start, int len, float* K_out,
                            float* V_out, uint32_t* status, cudaStream_t st);
@@ -157,6 +160,13 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// log2(x) via the SFU (lg2.approx.ftz): log2(0) = -inf.
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
