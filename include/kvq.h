@@ -249,6 +249,31 @@ int kvq_bf16_decode(kvq_handle* h, const void* pool, int num_pool_pages,
                     const int32_t* seq_lens, int batch, float* out,
                     void* workspace, size_t ws_bytes, int num_splits, void* stream);
 
+/* ---- decode without a caller-supplied workspace ----------------------------
+ * The paper has no counterpart: this is a convenience of this library.
+ * kvq_decode needs a workspace that the caller allocates.  Callers that cannot
+ * allocate one (an integration whose attention-op signature has no workspace
+ * argument, or a serving process that reserves all device memory at start-up and
+ * forbids allocation on the decode path) can call this instead.  It computes
+ * exactly what kvq_decode computes, with its scratch taken from one fixed
+ * 16 MiB array in device global memory that every GPU loading the library holds
+ * until the process exits.  It calls no allocating routine.
+ *   - Arguments as for kvq_decode, without workspace / ws_bytes.
+ *   - num_splits == 0: the automatic choice, lowered until the scratch
+ *     (kvq_workspace_bytes(h, batch, splits)) fits in 16 MiB.  An explicit
+ *     num_splits whose scratch does not fit returns KVQ_ENOSPACE.
+ *   - The first call on a device looks up the array's device address (with the
+ *     handle's device made current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero: each call writes every part it
+ *     reads.  Calls whose kernels overlap on the GPU (other streams, other
+ *     threads, other handles) race on it: order them on one stream. */
+int kvq_decode_static(kvq_handle* h, const void* pool, int num_pool_pages,
+                      const uint16_t* q, const int32_t* page_table, int max_pages,
+                      const int32_t* seq_lens, int batch, float* out, int num_splits,
+                      void* stream);
+
 /* ---- status and diagnostics ---------------------------------------------- */
 
 /* Read and clear the handle's device status word (KVQ_STATUS_* bits).

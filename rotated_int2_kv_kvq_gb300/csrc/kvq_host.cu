@@ -227,6 +227,8 @@ int append_common(kvq_handle* h, bool int2, void* pool, int num_pool_pages, cons
 
 }  // namespace
 
+int kvq::handle_device(const kvq_handle* h) { return h ? h->device : -1; }
+
 extern "C" {
 
 int kvq_create(const kvq_layout* layout, kvq_handle** out) {

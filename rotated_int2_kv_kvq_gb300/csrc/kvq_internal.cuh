@@ -80,6 +80,7 @@ cudaError_t launch_dequant(const uint8_t* pool, int num_pool_pages, const int32_
 cudaError_t launch_transpose(const float* in, float* out, int count, cudaStream_t st);
 int decode_int2_ctas_per_sm();
 int decode_bf16_ctas_per_sm();
+int handle_device(const kvq_handle* h);   // CUDA device the handle was created on
 
 // ---- device helpers -------------------------------------------------------
 #if defined(__CUDACC__)

@@ -40,6 +40,7 @@ SIGNATURES = {
     "kvq_bf16_append": ([_P, _P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _P], _I),
     "kvq_bf16_workspace_bytes": ([_P, _I, _I], _SZ),
     "kvq_bf16_decode": ([_P, _P, _I, _P, _P, _I, _P, _I, _P, _P, _SZ, _I, _P], _I),
+    "kvq_decode_static": ([_P, _P, _I, _P, _P, _I, _P, _I, _P, _I, _P], _I),
     "kvq_get_status": ([_P, _P, _P], _I),
     "kvq_auto_splits": ([_P, _I, _I], _I),
     "kvq_profile_enable": ([_P, _I], _I),
@@ -219,6 +220,17 @@ def kvq_bf16_decode(h, pool, num_pool_pages, q, page_table, seq_lens, out, works
                     num_splits=0, stream=None):
     _decode("kvq_bf16_decode", h, pool, num_pool_pages, q, page_table, seq_lens, out, workspace,
             num_splits, stream)
+
+
+def kvq_decode_static(h, pool, num_pool_pages, q, page_table, seq_lens, out, num_splits=0,
+                      stream=None):
+    """kvq_decode with the library's fixed 16 MiB scratch array instead of a
+    caller-supplied workspace (for callers that cannot allocate one)."""
+    batch, max_pages = int(page_table.shape[0]), int(page_table.shape[1])
+    _check("kvq_decode_static", load_library().kvq_decode_static(
+        h.ptr, _ptr(pool, _U8, "pool"), int(num_pool_pages), _ptr(q, _BF16, "q"),
+        _ptr(page_table, _I32, "page_table"), max_pages, _ptr(seq_lens, _I32, "seq_lens"),
+        batch, _ptr(out, _F32, "out"), int(num_splits), _stream(stream)))
 
 
 def kvq_dequant(h, pool, num_pool_pages, page_table, seq, start, length, K_out=None, V_out=None,
