@@ -28,9 +28,9 @@
 // with col = 2*head + {hi, lo}: each operand that is not a code is split into an
 // fp16 high part and an fp16 residual (scaled by 2^11 so it stays a normal
 // number), which keeps products at fp32 accuracy.  Codes become fp16 operands
-// with one shift and one AND: a 2-bit field moved to bits 8-9 of a 16-bit half
-// is the fp16 number code * 2^-16, exactly; the power of two is folded into the
-// score constants and removed in the value epilogue.
+// with shifts and ANDs: a 2-bit field moved to bits 9-10 (or 7-8) of a 16-bit
+// half is the fp16 number code * 2^-15 (or code * 2^-17), exactly; the powers of
+// two are folded into the query operands and removed in the value epilogue.
 //
 // Kernel chain of one decode call: qprep -> decode -> combine, each launched as
 // a programmatic dependent of the previous kernel (griddepcontrol), so each one
@@ -67,122 +67,105 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 // ---------------------------------------------------------------------------
-// Query preparation: q_rot = q R_K for the G query heads of kQB sequences and one
-// KV head per CTA (R_K staged once in shared memory by a bulk copy), then the
+// Query preparation: q_rot = q R_K for the G query heads of one sequence and one
+// KV head per CTA (R_K staged in shared memory by a bulk copy), then the
 // scores' B fragments.  B[row][col] for k-block w holds x = q_rot[head][16w+row]
 // * 2^(e_head), where 2^e_head brings max|q_rot| into [2^13, 2^14): column
 // 2*head is fp16(x), column 2*head+1 the residual (x - fp16(x)) * 2^11.  With
 // codes entering as code * 2^-16 (see the file comment) the score of a token is
-// q_rot . c = 2^(16 - e) * (hi + 2^-11 lo).  Per head also: kappa =
+// q_rot . c = 2^(16 - e) * (hi + 2^-11 lo).  (Even k-blocks carry x * 2, odd ones
+// x / 2, matching the code scales 2^-17 and 2^-15 of code_op.)  Per head also: kappa =
 // sm_scale*log2e * 2^(16 - e) and zeta = sm_scale*log2e * sum(q_rot).
 // Launched as a programmatic dependent of the preceding kernel: it reads only
 // q and R_K, so it may run while a preceding append is still writing pages; it
 // waits for that kernel before it exits, so the decode kernel that waits for
 // this one also sees the appended pages.
 // ---------------------------------------------------------------------------
-constexpr int kQB = 4;                       // sequences per qprep CTA
-constexpr int kQVec = kQB * kMaxG;           // query vectors per qprep CTA
 struct QprepSmem {
   float R[kDim * kDim];
-  float qs[kQVec][kDim];
-  float qr[kQVec][kDim];
-  float red_sum[kQVec][4], red_max[kQVec][4];
-  int e[kQVec];
+  float qs[kMaxG][kDim];
+  float qr[kMaxG][kDim];
+  int e[kMaxG];
   uint64_t bar;
 };
 
-__global__ void __launch_bounds__(256) qprep_kernel(DecodeArgs a, const float* __restrict__ RK,
+// One CTA per (sequence, KV head); thread i computes element i of the G
+// rotated query vectors.
+__global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* __restrict__ RK,
                                                     float log2_scale) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   QprepSmem& sm = *reinterpret_cast<QprepSmem*>(smem_raw);
-  const int b0 = blockIdx.x * kQB, kv = blockIdx.y, tid = threadIdx.x;
+  const int b = blockIdx.x, kv = blockIdx.y, i = threadIdx.x;
   const int G = a.G;
   griddep_launch_dependents();
   const uint32_t bar = smem_u32(&sm.bar);
-  if (tid == 0) {
+  if (i == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) {
+  if (i == 0) {
     mbar_arrive_expect_tx(bar, kDim * kDim * 4);
     bulk_g2s(smem_u32(sm.R), RK + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
   }
-  for (int idx = tid; idx < kQVec * kDim; idx += 256) {
-    const int v = idx / kDim, j = idx % kDim;
-    const int b = b0 + v / kMaxG, h = v % kMaxG;
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) {
     float x = 0.0f;
-    if (b < a.batch && h < G) {
-      const uint16_t bits = a.q[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + j];
+    if (h < G) {
+      const uint16_t bits = a.q[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + i];
       x = __uint_as_float(static_cast<uint32_t>(bits) << 16);
     }
-    sm.qs[v][j] = x;
+    sm.qs[h][i] = x;
   }
   const bool ok = mbar_wait_bounded(bar, 0);
   if (__syncthreads_or(!ok)) {
-    if (tid == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+    if (i == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
     griddep_wait();
     return;
   }
-  // thread: output element i of vectors half*8 .. half*8+7
+  float acc[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 8
+  for (int j = 0; j < kDim; ++j) {
+    const float r = sm.R[j * kDim + i];
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) acc[h] = fmaf(sm.qs[h][j], r, acc[h]);
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) sm.qr[h][i] = acc[h];
+  __syncthreads();
+  // per-vector sum and max|.|: warp w handles vector w
   {
-    const int i = tid & (kDim - 1), half = tid >> 7;
-    float acc[8];
+    const int w = i >> 5, lane = i & 31;
+    float s = 0.0f, m = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-#pragma unroll 4
-    for (int j = 0; j < kDim; ++j) {
-      const float r = sm.R[j * kDim + i];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] = fmaf(sm.qs[half * 8 + k][j], r, acc[k]);
+    for (int k = 0; k < 4; ++k) {
+      const float x = sm.qr[w][lane + 32 * k];
+      s += x;
+      m = fmaxf(m, fabsf(x));
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) sm.qr[half * 8 + k][i] = acc[k];
-  }
-  __syncthreads();
-  // per-vector sum and max|.|: warp w handles vectors 2w, 2w+1
-  {
-    const int w = tid >> 5, lane = tid & 31;
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int v = 2 * w + u;
-      float s = 0.0f, m = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float x = sm.qr[v][lane + 32 * k];
-        s += x;
-        m = fmaxf(m, fabsf(x));
+    for (int off = 16; off > 0; off >>= 1) {
+      s += __shfl_xor_sync(0xffffffffu, s, off);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    }
+    if (lane == 0) {
+      int e = 0;
+      if (m > 0.0f && m < INFINITY) {
+        int E;
+        frexpf(m, &E);           // m = f * 2^E, f in [0.5, 1)
+        e = 14 - E;              // m * 2^e in [2^13, 2^14)
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, off);
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      }
-      if (lane == 0) {
-        int e = 0;
-        if (m > 0.0f && m < INFINITY) {
-          int E;
-          frexpf(m, &E);         // m = f * 2^E, f in [0.5, 1)
-          e = 14 - E;            // m * 2^e in [2^13, 2^14)
-        }
-        sm.e[v] = e;
-        const int b = b0 + v / kMaxG, h = v % kMaxG;
-        if (b < a.batch) {
-          float* qm = const_cast<float*>(a.qmeta) + (static_cast<size_t>(b) * a.Hkv + kv) * 8;
-          qm[2 * h] = (h < G) ? log2_scale * ldexpf(1.0f, 16 - e) : 0.0f;
-          qm[2 * h + 1] = (h < G) ? log2_scale * s : 0.0f;
-        }
-      }
+      sm.e[w] = e;
+      float* qm = const_cast<float*>(a.qmeta) + (static_cast<size_t>(b) * a.Hkv + kv) * 8;
+      qm[2 * w] = (w < G) ? log2_scale * ldexpf(1.0f, 16 - e) : 0.0f;
+      qm[2 * w + 1] = (w < G) ? log2_scale * s : 0.0f;
     }
   }
   __syncthreads();
-  // B fragments: per sequence 32 lanes x 16 registers; thread writes 8 registers
-  for (int idx = tid; idx < kQB * 32 * 4; idx += 256) {
-    const int bb = idx / 128, L = (idx / 4) % 32, quad = idx % 4;
-    const int b = b0 + bb;
-    if (b >= a.batch) continue;
+  // B fragments: 32 lanes x 16 registers; thread i writes 4 registers of lane i/4
+  {
+    const int L = i >> 2, quad = i & 3;
     const int g = L >> 2, t = L & 3, head = g >> 1, part = g & 1;
-    const int v = bb * kMaxG + head;
     uint32_t out[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -193,7 +176,9 @@ __global__ void __launch_bounds__(256) qprep_kernel(DecodeArgs a, const float* _
       if (head < G) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const float x = ldexpf(sm.qr[v][row + u], sm.e[v]);
+          // x * 2 for even k-blocks (codes enter as c * 2^-17), x / 2 for odd
+          // ones (c * 2^-15): every product is c * q * 2^(e - 16)
+          const float x = ldexpf(sm.qr[head][row + u], sm.e[head] + ((w & 1) ? -1 : 1));
           const __half hi = __float2half_rn(x);
           x2[u] = part ? (x - __half2float(hi)) * 2048.0f : __half2float(hi);
         }
@@ -212,15 +197,18 @@ __global__ void __launch_bounds__(256) qprep_kernel(DecodeArgs a, const float* _
 // ---------------------------------------------------------------------------
 
 // fp16x2 operand of code position P (0..7) of a fragment word: the fields at
-// bits [2P, 2P+1] and [16+2P, 17+2P] moved to bits 8-9 of their half, i.e. the
-// fp16 numbers code * 2^-16 (subnormal for code 1, top mantissa bits).  Tensor
-// cores keep full product precision for such operands; a field left at the low
-// mantissa bits would lose up to ~13 bits of the product.
+// bits [2P, 2P+1] and [16+2P, 17+2P] moved to bits 9-10 (odd P) or bits 7-8
+// (even P) of their half.  As fp16 numbers these are code * 2^-15 (bit 9 is the
+// top mantissa bit, bit 10 the lowest exponent bit: 0, 2^-15, 2^-14, 3*2^-15)
+// and code * 2^-17, exactly.  One shift serves two positions.  Tensor cores
+// keep (nearly) full product precision for such operands; a field left at the
+// low mantissa bits would lose up to ~13 bits of the product.
 template <int P>
 __device__ __forceinline__ uint32_t code_op(uint32_t w) {
-  constexpr uint32_t kM = 0x03000300u;
-  if constexpr (P < 4) return (w << (8 - 2 * P)) & kM;
-  else return (w >> (2 * P - 8)) & kM;
+  constexpr uint32_t kM = (P & 1) ? 0x06000600u : 0x01800180u;
+  constexpr int kShift = 7 - 2 * (P & ~1);     // left shift; negative = right shift
+  if constexpr (kShift >= 0) return (w << kShift) & kM;
+  else return (w >> (-kShift)) & kM;
 }
 
 // Scores of one page for this lane: tokens g and g+8 of head t (qc, before the
@@ -271,6 +259,90 @@ __device__ __forceinline__ void weights_to_b(float P0, float P1, int g, int t, u
   pb1 = __byte_perm(va, vb, 0x7632);
 }
 
+// Weights are kept <= 2^kLazy relative to the running max before it is raised.
+constexpr float kLazy = 8.0f;
+
+// Online-softmax update with the two pages (A, B) of one stage for this lane:
+// scores, running max, weights, value accumulation.  kMasked = false is the
+// common case of two full, valid pages: no per-token masks at all.
+struct WarpState {
+  float acc[8][4];
+  float m_run, l_run, z_run;
+};
+
+template <bool kMasked>
+__device__ __forceinline__ void process_pair(WarpState& st, const uint32_t (&qf)[16], float kappa,
+                                             float zeta, int g, int t, const uint4& kwa,
+                                             const uint4& vwa, const uint4& mta, const uint4& kwb,
+                                             const uint4& vwb, const uint4& mtb, bool va0, bool va1,
+                                             bool vb0, bool vb1) {
+  if (!kMasked) va0 = va1 = vb0 = vb1 = true;
+  float (&acc)[8][4] = st.acc;
+  float& m_run = st.m_run;
+  float& l_run = st.l_run;
+  float& z_run = st.z_run;
+    // ---- scores of both pages (independent tensor-core chains)
+    float sa4[4], sb4[4];
+    page_scores(kwa, qf, sa4);
+    page_scores(kwb, qf, sb4);
+    // logit (log2 units) = kappa * s_k * qc + zeta * z_k; qc = hi col + 2^-11 lo col
+    const float la0 = va0 ? fmaf(kappa * half_lo(mta.x), fmaf(sa4[1], 1.0f / 2048.0f, sa4[0]),
+                                 zeta * half_hi(mta.x)) : -INFINITY;
+    const float la1 = va1 ? fmaf(kappa * half_lo(mta.y), fmaf(sa4[3], 1.0f / 2048.0f, sa4[2]),
+                                 zeta * half_hi(mta.y)) : -INFINITY;
+    const float lb0 = vb0 ? fmaf(kappa * half_lo(mtb.x), fmaf(sb4[1], 1.0f / 2048.0f, sb4[0]),
+                                 zeta * half_hi(mtb.x)) : -INFINITY;
+    const float lb1 = vb1 ? fmaf(kappa * half_lo(mtb.y), fmaf(sb4[3], 1.0f / 2048.0f, sb4[2]),
+                                 zeta * half_hi(mtb.y)) : -INFINITY;
+
+    // ---- online softmax.  The value weights P = p * s_v feed fp16 operands, so
+    // the running max m is kept over lv = logit + log2(s_v) and raised only when
+    // some lv exceeds m + kLazy: then p * s_v <= 2^kLazy for every token seen and
+    // P * 2^(14 - kLazy) stays below 2^14.  p = 2^(logit - m) itself may be large
+    // (at most 2^(kLazy + 24)); it is only summed in fp32.
+    const float sva0 = half_lo(mta.z), sva1 = half_lo(mta.w);
+    const float svb0 = half_lo(mtb.z), svb1 = half_lo(mtb.w);
+    const float lva0 = la0 + fmaxf(fast_log2(sva0), -24.0f);
+    const float lva1 = la1 + fmaxf(fast_log2(sva1), -24.0f);
+    const float lvb0 = lb0 + fmaxf(fast_log2(svb0), -24.0f);
+    const float lvb1 = lb1 + fmaxf(fast_log2(svb1), -24.0f);
+    const float lmax = fmaxf(fmaxf(lva0, lva1), fmaxf(lvb0, lvb1));
+    if (__any_sync(0xffffffffu, lmax > m_run + kLazy)) {
+      float pm = lmax;
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+      if (pm > m_run) {
+        const float f = fast_exp2(m_run - pm);
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[mb][q] *= f;
+        l_run *= f;
+        z_run *= f;
+        m_run = pm;
+      }
+    }
+    const float pa0 = va0 ? fast_exp2(la0 - m_run) : 0.0f;
+    const float pa1 = va1 ? fast_exp2(la1 - m_run) : 0.0f;
+    const float pb0v = vb0 ? fast_exp2(lb0 - m_run) : 0.0f;
+    const float pb1v = vb1 ? fast_exp2(lb1 - m_run) : 0.0f;
+    l_run += (pa0 + pa1) + (pb0v + pb1v);
+    constexpr float kWScale = 64.0f;      // 2^(14 - kLazy)
+    float Pa0 = 0.0f, Pa1 = 0.0f, Pb0 = 0.0f, Pb1 = 0.0f;
+    if (va0) { Pa0 = pa0 * (sva0 * kWScale); z_run = fmaf(pa0, half_hi(mta.z), z_run); }
+    if (va1) { Pa1 = pa1 * (sva1 * kWScale); z_run = fmaf(pa1, half_hi(mta.w), z_run); }
+    if (vb0) { Pb0 = pb0v * (svb0 * kWScale); z_run = fmaf(pb0v, half_hi(mtb.z), z_run); }
+    if (vb1) { Pb1 = pb1v * (svb1 * kWScale); z_run = fmaf(pb1v, half_hi(mtb.w), z_run); }
+
+    // ---- values of both pages
+    uint32_t fa0, fa1, fb0, fb1;
+    weights_to_b(Pa0, Pa1, g, t, fa0, fa1);
+    weights_to_b(Pb0, Pb1, g, t, fb0, fb1);
+    page_values(vwa, fa0, fa1, acc);
+    page_values(vwb, fb0, fb1, acc);
+}
+
 constexpr int kW = kInt2Warps;                 // warps per CTA
 constexpr int kNS = 4;                         // pipeline stages
 constexpr int kStageBytes = 2 * kW * kInt2Rec; // 2 pages x (8/HPC) x HPC heads
@@ -286,8 +358,6 @@ struct Int2Smem {
   float l[kW][kMaxG];
 };
 
-// Weights are kept <= 2^kLazy relative to the running max before it is raised.
-constexpr float kLazy = 8.0f;
 
 // Fill stage `k` of the current sub-chunk (single thread).
 __device__ __forceinline__ void issue_stage(Int2Smem& sm, const DecodeArgs& a, int k, int slot,
@@ -358,24 +428,28 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   const float kappa = a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * 8 + 2 * t];
   const float zeta = a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * 8 + 2 * t + 1];
 
-  float acc[8][4];
+  WarpState ws;
 #pragma unroll
   for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) acc[mb][k] = 0.0f;
-  float m_run = -INFINITY, l_run = 0.0f, z_run = 0.0f;
+    for (int k = 0; k < 4; ++k) ws.acc[mb][k] = 0.0f;
+  ws.m_run = -INFINITY;
+  ws.l_run = 0.0f;
+  ws.z_run = 0.0f;
 
   int gs = 0;            // stages consumed so far (ring phase)
   bool timed_out = false;
   for (int sub = 0; sub < npg && !timed_out; sub += kMaxIds) {
     const int nsub = min(kMaxIds, npg - sub);
+    bool ids_ok = true;
     for (int i = tid; i < nsub; i += kW * 32) {
       const int id = ptab[p0 + sub + i];
       const bool ok = id >= 0 && id < a.num_pool_pages;
       if (!ok) atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
       sm.ids[i] = ok ? id : -1;
+      ids_ok = ids_ok && ok;
     }
-    __syncthreads();
+    const bool all_ids_ok = __syncthreads_and(ids_ok);
     const int nst = (nsub + PPS - 1) / PPS;
     if (tid == 0)
       for (int k = 0; k < kNS && k < nst; ++k) issue_stage(sm, a, k, (gs + k) % kNS, nsub, PPS, HPC, hg);
@@ -388,8 +462,9 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
         break;
       }
       const int ua = k * PPS + gi, ub = ua + GPH;
-      const bool oka = ua < nsub && sm.ids[ua] >= 0;
-      const bool okb = ub < nsub && sm.ids[ub] >= 0;
+      // both pages of every warp present, valid and full of context
+      const bool full = all_ids_ok && (k + 1) * PPS <= nsub &&
+                        (p0 + sub + (k + 1) * PPS) * kPage <= seq_len;
       const uint8_t* sta = &sm.ring[slot][(gi * HPC + hl) * kInt2Rec];
       const uint8_t* stb = &sm.ring[slot][((GPH + gi) * HPC + hl) * kInt2Rec];
       const uint4 kwa = *reinterpret_cast<const uint4*>(sta + 16 * lane);
@@ -411,70 +486,18 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
           }
         }
       }
-      const int posa = (p0 + sub + ua) * kPage, posb = (p0 + sub + ub) * kPage;
-      const bool va0 = oka && (posa + g < seq_len), va1 = oka && (posa + g + 8 < seq_len);
-      const bool vb0 = okb && (posb + g < seq_len), vb1 = okb && (posb + g + 8 < seq_len);
-
-      // ---- scores of both pages (independent tensor-core chains)
-      float sa4[4], sb4[4];
-      page_scores(kwa, qf, sa4);
-      page_scores(kwb, qf, sb4);
-      // logit (log2 units) = kappa * s_k * qc + zeta * z_k; qc = hi col + 2^-11 lo col
-      const float la0 = va0 ? fmaf(kappa * half_lo(mta.x), fmaf(sa4[1], 1.0f / 2048.0f, sa4[0]),
-                                   zeta * half_hi(mta.x)) : -INFINITY;
-      const float la1 = va1 ? fmaf(kappa * half_lo(mta.y), fmaf(sa4[3], 1.0f / 2048.0f, sa4[2]),
-                                   zeta * half_hi(mta.y)) : -INFINITY;
-      const float lb0 = vb0 ? fmaf(kappa * half_lo(mtb.x), fmaf(sb4[1], 1.0f / 2048.0f, sb4[0]),
-                                   zeta * half_hi(mtb.x)) : -INFINITY;
-      const float lb1 = vb1 ? fmaf(kappa * half_lo(mtb.y), fmaf(sb4[3], 1.0f / 2048.0f, sb4[2]),
-                                   zeta * half_hi(mtb.y)) : -INFINITY;
-
-      // ---- online softmax.  The value weights P = p * s_v feed fp16 operands, so
-      // the running max m is kept over lv = logit + log2(s_v) and raised only when
-      // some lv exceeds m + kLazy: then p * s_v <= 2^kLazy for every token seen and
-      // P * 2^(14 - kLazy) stays below 2^14.  p = 2^(logit - m) itself may be large
-      // (at most 2^(kLazy + 24)); it is only summed in fp32.
-      const float sva0 = half_lo(mta.z), sva1 = half_lo(mta.w);
-      const float svb0 = half_lo(mtb.z), svb1 = half_lo(mtb.w);
-      const float lva0 = la0 + fmaxf(fast_log2(sva0), -24.0f);
-      const float lva1 = la1 + fmaxf(fast_log2(sva1), -24.0f);
-      const float lvb0 = lb0 + fmaxf(fast_log2(svb0), -24.0f);
-      const float lvb1 = lb1 + fmaxf(fast_log2(svb1), -24.0f);
-      const float lmax = fmaxf(fmaxf(lva0, lva1), fmaxf(lvb0, lvb1));
-      if (__any_sync(0xffffffffu, lmax > m_run + kLazy)) {
-        float pm = lmax;
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-        if (pm > m_run) {
-          const float f = fast_exp2(m_run - pm);
-#pragma unroll
-          for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[mb][q] *= f;
-          l_run *= f;
-          z_run *= f;
-          m_run = pm;
-        }
+      if (full) {
+        process_pair<false>(ws, qf, kappa, zeta, g, t, kwa, vwa, mta, kwb, vwb, mtb, true, true,
+                            true, true);
+      } else {
+        const bool oka = ua < nsub && sm.ids[ua] >= 0;
+        const bool okb = ub < nsub && sm.ids[ub] >= 0;
+        const int posa = (p0 + sub + ua) * kPage, posb = (p0 + sub + ub) * kPage;
+        const bool va0 = oka && (posa + g < seq_len), va1 = oka && (posa + g + 8 < seq_len);
+        const bool vb0 = okb && (posb + g < seq_len), vb1 = okb && (posb + g + 8 < seq_len);
+        process_pair<true>(ws, qf, kappa, zeta, g, t, kwa, vwa, mta, kwb, vwb, mtb, va0, va1, vb0,
+                           vb1);
       }
-      const float pa0 = va0 ? fast_exp2(la0 - m_run) : 0.0f;
-      const float pa1 = va1 ? fast_exp2(la1 - m_run) : 0.0f;
-      const float pb0v = vb0 ? fast_exp2(lb0 - m_run) : 0.0f;
-      const float pb1v = vb1 ? fast_exp2(lb1 - m_run) : 0.0f;
-      l_run += (pa0 + pa1) + (pb0v + pb1v);
-      constexpr float kWScale = 64.0f;      // 2^(14 - kLazy)
-      float Pa0 = 0.0f, Pa1 = 0.0f, Pb0 = 0.0f, Pb1 = 0.0f;
-      if (va0) { Pa0 = pa0 * (sva0 * kWScale); z_run = fmaf(pa0, half_hi(mta.z), z_run); }
-      if (va1) { Pa1 = pa1 * (sva1 * kWScale); z_run = fmaf(pa1, half_hi(mta.w), z_run); }
-      if (vb0) { Pb0 = pb0v * (svb0 * kWScale); z_run = fmaf(pb0v, half_hi(mtb.z), z_run); }
-      if (vb1) { Pb1 = pb1v * (svb1 * kWScale); z_run = fmaf(pb1v, half_hi(mtb.w), z_run); }
-
-      // ---- values of both pages
-      uint32_t fa0, fa1, fb0, fb1;
-      weights_to_b(Pa0, Pa1, g, t, fa0, fa1);
-      weights_to_b(Pb0, Pb1, g, t, fb0, fb1);
-      page_values(vwa, fa0, fa1, acc);
-      page_values(vwb, fb0, fb1, acc);
     }
     gs += nst;
     __syncthreads();     // sm.ids is reloaded for the next sub-chunk
@@ -489,21 +512,23 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   // ---- warp epilogue: (m, l, o) of the warp's KV head for its G query heads
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
-    z_run += __shfl_xor_sync(0xffffffffu, z_run, off);
+    ws.l_run += __shfl_xor_sync(0xffffffffu, ws.l_run, off);
+    ws.z_run += __shfl_xor_sync(0xffffffffu, ws.z_run, off);
   }
   if (t < a.G) {
-    // undo the code scale 2^-16 and the weight scale 2^(14 - kLazy) = 2^6;
-    // the residual column carries a further 2^11
-    constexpr float kInv = 1024.0f;       // 2^(16 - 6)
+    // undo the code scale (2^-17 for even m-blocks, 2^-15 for odd ones) and the
+    // weight scale 2^(14 - kLazy) = 2^6; the residual column carries a further 2^11
+    constexpr float kInvEven = 2048.0f;   // 2^(17 - 6)
+    constexpr float kInvOdd = 512.0f;     // 2^(15 - 6)
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
-      sm.o[warp][t][16 * mb + g] = fmaf(fmaf(acc[mb][1], 1.0f / 2048.0f, acc[mb][0]), kInv, z_run);
-      sm.o[warp][t][16 * mb + g + 8] = fmaf(fmaf(acc[mb][3], 1.0f / 2048.0f, acc[mb][2]), kInv, z_run);
+      const float inv = (mb & 1) ? kInvOdd : kInvEven;
+      sm.o[warp][t][16 * mb + g] = fmaf(fmaf(ws.acc[mb][1], 1.0f / 2048.0f, ws.acc[mb][0]), inv, ws.z_run);
+      sm.o[warp][t][16 * mb + g + 8] = fmaf(fmaf(ws.acc[mb][3], 1.0f / 2048.0f, ws.acc[mb][2]), inv, ws.z_run);
     }
     if (g == 0) {
-      sm.m[warp][t] = m_run;
-      sm.l[warp][t] = l_run;
+      sm.m[warp][t] = ws.m_run;
+      sm.l[warp][t] = ws.l_run;
     }
   }
   __syncthreads();
@@ -753,59 +778,74 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodeAr
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp combine of the split partials of one (b, query head), then
-// out = o_rot R_V^T.  Thread d owns element d; the split weights are computed
-// once into shared memory and the partial rows are read with independent loads.
+// Log-sum-exp combine of the split partials of the G query heads of one
+// (sequence, KV head), then out = o_rot R_V^T.  R_V^T (static data) is staged
+// in shared memory by a bulk copy issued before the kernel waits for the decode
+// kernel, so the copy overlaps the decode tail.  Warp h reduces the split
+// maxima and weights of head h; thread (h, d) then forms element d of head h.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float block_reduce_128(float x, float* red, bool is_max) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float y = __shfl_xor_sync(0xffffffffu, x, off);
-    x = is_max ? fmaxf(x, y) : x + y;
-  }
-  if (lane == 0) red[warp] = x;
-  __syncthreads();
-  float r = red[0];
-#pragma unroll
-  for (int w = 1; w < 4; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
-  __syncthreads();
-  return r;
-}
+struct CombineSmem {
+  float Rt[kDim * kDim];
+  float w[kMaxG][kMaxSplits];
+  float o[kMaxG][kDim];
+  float linv[kMaxG];
+  uint64_t bar;
+};
+constexpr int kCombineThreads = kMaxG * kDim;   // 512
 
-__global__ void __launch_bounds__(128) combine_kernel(DecodeArgs a) {
-  __shared__ float wsp[kMaxSplits];
-  __shared__ float os[kDim];
-  __shared__ float red[4];
-  griddep_wait();
-  const int bh = blockIdx.x, h = bh % a.H, kv = h / a.G, d = threadIdx.x;
-  const int S = a.splits;
-  const float* parts = a.part + static_cast<size_t>(bh) * S * kPartStride;
-  float M = -INFINITY;
-  for (int j = d; j < S; j += 128) M = fmaxf(M, parts[j * kPartStride]);
-  M = block_reduce_128(M, red, true);
-  float L = 0.0f;
-  for (int j = d; j < S; j += 128) {
-    const float mj = parts[j * kPartStride];
-    const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj - M);
-    wsp[j] = w;
-    L = fmaf(w, parts[j * kPartStride + 1], L);
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  CombineSmem& sm = *reinterpret_cast<CombineSmem*>(smem_raw);
+  const int b = blockIdx.x, kv = blockIdx.y, tid = threadIdx.x;
+  const int h = tid / kDim, d = tid % kDim;       // thread (h, d)
+  const int warp = tid >> 5, lane = tid & 31;
+  const int S = a.splits, G = a.G;
+  const uint32_t bar = smem_u32(&sm.bar);
+  if (a.rotate_out && tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, kDim * kDim * 4);
+    bulk_g2s(smem_u32(sm.Rt), a.RVt + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
   }
-  L = block_reduce_128(L, red, false);     // its barriers also publish wsp
+  griddep_wait();       // the partials come from the decode kernel
+  if (warp < G) {
+    const float* parts = a.part + (static_cast<size_t>(b) * a.H + kv * G + warp) * S * kPartStride;
+    float M = -INFINITY;
+    for (int j = lane; j < S; j += 32) M = fmaxf(M, parts[j * kPartStride]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.0f;
+    for (int j = lane; j < S; j += 32) {
+      const float mj = parts[j * kPartStride];
+      const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj - M);
+      sm.w[warp][j] = w;
+      L = fmaf(w, parts[j * kPartStride + 1], L);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) sm.linv[warp] = (L > 0.0f) ? 1.0f / L : 0.0f;
+  }
+  __syncthreads();
   float o = 0.0f;
+  if (h < G) {
+    const float* parts = a.part + (static_cast<size_t>(b) * a.H + kv * G + h) * S * kPartStride;
 #pragma unroll 8
-  for (int j = 0; j < S; ++j) o = fmaf(wsp[j], parts[j * kPartStride + 4 + d], o);
-  o = (L > 0.0f) ? o / L : 0.0f;
+    for (int j = 0; j < S; ++j) o = fmaf(sm.w[h][j], parts[j * kPartStride + 4 + d], o);
+    o *= sm.linv[h];
+  }
   if (a.rotate_out) {
-    os[d] = o;
-    __syncthreads();
-    const float* Rt = a.RVt + static_cast<size_t>(kv) * kDim * kDim;
+    sm.o[h][d] = o;
+    const bool ok = mbar_wait_bounded(bar, 0);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+      return;
+    }
     float r = 0.0f;
 #pragma unroll 8
-    for (int j = 0; j < kDim; ++j) r = fmaf(os[j], __ldg(Rt + j * kDim + d), r);
+    for (int j = 0; j < kDim; ++j) r = fmaf(sm.o[h][j], sm.Rt[j * kDim + d], r);
     o = r;
   }
-  a.out[static_cast<size_t>(bh) * kDim + d] = o;
+  if (h < G) a.out[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + d] = o;
 }
 
 // Dequantise positions [start, start+len) of one sequence: CTA per (position,
@@ -896,8 +936,8 @@ cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_
 cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, float sm_scale, cudaStream_t st) {
   cudaError_t e = set_smem_attr<QprepSmem>(qprep_kernel);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.batch + kQB - 1) / kQB, a.Hkv);
-  e = launch_dependent(qprep_kernel, grid, dim3(256), sizeof(QprepSmem), st, a, RK,
+  dim3 grid(a.batch, a.Hkv);
+  e = launch_dependent(qprep_kernel, grid, dim3(128), sizeof(QprepSmem), st, a, RK,
                        sm_scale * kLog2e);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -919,7 +959,10 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st) {
-  cudaError_t e = launch_dependent(combine_kernel, dim3(a.batch * a.H), dim3(128), 0, st, a);
+  cudaError_t e = set_smem_attr<CombineSmem>(combine_kernel);
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(combine_kernel, dim3(a.batch, a.Hkv), dim3(kCombineThreads),
+                       sizeof(CombineSmem), st, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
