@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_32k")
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison kernel")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return ap.parse_args()
@@ -72,10 +74,29 @@ def profiled_traffic():
         return None
     text = open(PROFILE_SUMMARY).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    h = re.search(r"kvq_decode\.cu sha256\[:16\]:\s*([0-9a-f]+)", text)
+    h = re.search(r"kvq_decode\.cu`?\s*sha256\[:16\]:\s*([0-9a-f]+)", text)
     if not m or not h or h.group(1) != source_hash(DECODE_SRC):
         return None
     return float(m.group(1))
+
+
+def max_over_ranks(value, dist=None):
+    """Max of a float over all ranks of the default process group (the value
+    itself without one).  NCCL groups reduce a CUDA tensor, others a CPU one."""
+    if dist is None or not dist.is_available() or not dist.is_initialized():
+        return float(value)
+    import torch
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, max_ms, world):
+    """Weak scaling: every rank processes units_per_rank; the job takes the
+    slowest rank's time."""
+    return units_per_rank * world / (max_ms * 1e-3)
 
 
 class Clocks:
@@ -225,6 +246,10 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     K.load_library()
     wl = W.WORKLOADS[args.workload]
+    if args.batch:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, batch=args.batch)
     B, H, Hkv, ctx = wl.batch, wl.num_heads, wl.num_kv_heads, wl.ctx
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
@@ -291,10 +316,7 @@ def run_ours(args):
         kern = K.kvq_profile_read(h) if profile else None
         if profile:
             K.kvq_profile_enable(h, False)
-        if dist is not None:
-            t = torch.tensor([ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(ms, dist)
         return ms, kern
 
     clocks = Clocks(local)
@@ -305,7 +327,7 @@ def run_ours(args):
     ms_step = ms / args.steps
     cache_bytes = int(lens.sum()) * Hkv * W.cache_bytes_per_token_head("int2")
     gbs_rank = cache_bytes / (ms_step * 1e-3) / 1e9
-    value = gbs_rank * world
+    value = whole_job_rate(cache_bytes, ms_step, world) / 1e9
     peak, peak_kind = measured_peaks()
     kern_ms = kern[0] / max(1, kern[1]) if kern else None
     achieved = cache_bytes / (kern_ms * 1e-3) / 1e9 if kern_ms else None
