@@ -76,6 +76,9 @@ def _load():
     lib.kvqo_attend_f64.restype = None
     lib.kvqo_decode_pairs.argtypes = [i32, P, i32, i32, i32, P, P, i32, P, P, i32, P, f64, i32, P]
     lib.kvqo_decode_pairs.restype = i32
+    lib.kvqo_decode_window_pairs.argtypes = [P, i32, P, i32, P, i32, i32, P, P, i32, P, P, i32,
+                                             i32, i32, P, P, f64, i32, P]
+    lib.kvqo_decode_window_pairs.restype = i32
     _lib = lib
     return lib
 
@@ -244,4 +247,29 @@ def decode_pairs(kind, pool, num_pool_pages, H, Hkv, q, page_table, seq_lens, pa
     _load().kvqo_decode_pairs(0 if kind == "int2" else 1, _p(pool), num_pool_pages, H, Hkv,
                               _p(q), _p(pt), pt.shape[1], _p(sl), _p(pr), pr.shape[0], _p(Rm),
                               float(sm_scale), 1 if out_rotated else 0, _p(out))
+    return out
+
+
+def decode_window_pairs(pool, num_pool_pages, bf16_pool, bf16_num_pool_pages, bf16_page_table, H,
+                        Hkv, q, page_table, seq_lens, pairs, sink, recent, R, mu, sm_scale=None,
+                        out_rotated=False):
+    """Decode (b, hq) pairs with a BF16 window of `sink` first and `recent` last
+    tokens over an INT2 cache; float64 [npairs, D]."""
+    pool = _c(pool, np.uint8)
+    bp = _c(bf16_pool, np.uint8)
+    bpt = _c(bf16_page_table, np.int32)
+    q = _c(q, np.uint16)
+    pt = _c(page_table, np.int32)
+    assert bpt.shape == pt.shape
+    sl = _c(seq_lens, np.int32)
+    pr = _c(pairs, np.int32).reshape(-1, 2)
+    Rm = _c(R, np.float32)
+    m = _c(mu, np.float32)
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(DIM)
+    out = np.zeros((pr.shape[0], DIM), np.float64)
+    _load().kvqo_decode_window_pairs(_p(pool), num_pool_pages, _p(bp), bf16_num_pool_pages,
+                                     _p(bpt), H, Hkv, _p(q), _p(pt), pt.shape[1], _p(sl), _p(pr),
+                                     pr.shape[0], int(sink), int(recent), _p(Rm), _p(m),
+                                     float(sm_scale), 1 if out_rotated else 0, _p(out))
     return out

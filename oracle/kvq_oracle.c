@@ -468,8 +468,109 @@ int kvqo_decode_bf16_head(const uint8_t* pool, int num_pool_pages, int H, int Hk
   return skipped;
 }
 
+/* Decode with a BF16 window, for one (b, hq), float64.  [OptR] "Assumptions &
+ * free parameters": a BF16 window of sink tokens (the first ones) and recent
+ * tokens (the last ones) is kept at full precision; the rest of the context is
+ * read from the INT2 cache.  Positions [0, sink) and [len - recent, len) come
+ * from the BF16 pool (plain keys and values, plain query), the others from the
+ * INT2 pool (rotated centred keys with the rotated query, values rotated back).
+ * All logits are on one scale: the INT2 ones add back q . mu, the constant the
+ * key centring removed ("What carries the argument", mechanism 2).
+ *   bf16_pool / bf16_page_table: the BF16 cache ([batch][max_pages] table).
+ *   mu : fp32 [Hkv][D].  out_rotated: output times R_V (the rotated basis). */
+int kvqo_decode_window_head(const uint8_t* pool, int num_pool_pages, const uint8_t* bf16_pool,
+                            int bf16_num_pool_pages, const int32_t* bf16_page_table, int H,
+                            int Hkv, const uint16_t* q, const int32_t* page_table, int max_pages,
+                            int b, int seq_len, int hq, int sink, int recent, const float* R,
+                            const float* mu, double sm_scale, int out_rotated, double* out) {
+  int G = H / Hkv, kv = hq / G, skipped = 0;
+  const float* RK = R + ((size_t)0 * Hkv + kv) * DIM * DIM;
+  const float* RV = R + ((size_t)1 * Hkv + kv) * DIM * DIM;
+  double qd[DIM], qrot[DIM], qmu = 0.0;
+  for (int d = 0; d < DIM; ++d) qd[d] = (double)kvqo_bf16_to_f32(q[d]);
+  kvqo_rotate_f64(qd, RK, DIM, qrot);
+  for (int d = 0; d < DIM; ++d) qmu += qd[d] * (double)mu[(size_t)kv * DIM + d];
+  int n = seq_len > 0 ? seq_len : 1;
+  double* logit = (double*)malloc(sizeof(double) * (size_t)n);
+  double* vals = (double*)calloc((size_t)n * DIM, sizeof(double));
+  char* used = (char*)calloc((size_t)n, 1);
+  uint8_t codes[DIM];
+  uint16_t s16, z16;
+  double mx = -INFINITY;
+  for (int p = 0; p < seq_len; ++p) {
+    int in_window = (p < sink) || (p >= seq_len - recent);
+    double kk[DIM], vv[DIM];
+    if (in_window) {
+      const uint8_t* rec = record_of((uint8_t*)bf16_pool, BF16_REC, Hkv, bf16_num_pool_pages,
+                                     bf16_page_table, max_pages, b, p, kv);
+      if (!rec) { ++skipped; continue; }
+      for (int d = 0; d < DIM; ++d) {
+        int ok = kvqo_bf16_locate(0, p % PAGE, d), ov = kvqo_bf16_locate(1, p % PAGE, d);
+        kk[d] = kvqo_bf16_to_f32((uint16_t)(rec[ok] | (rec[ok + 1] << 8)));
+        vv[d] = kvqo_bf16_to_f32((uint16_t)(rec[ov] | (rec[ov + 1] << 8)));
+      }
+      double acc = 0.0;
+      for (int d = 0; d < DIM; ++d) acc += qd[d] * kk[d];
+      logit[p] = sm_scale * acc;
+    } else {
+      const uint8_t* rec = record_of((uint8_t*)pool, INT2_REC, Hkv, num_pool_pages, page_table,
+                                     max_pages, b, p, kv);
+      if (!rec) { ++skipped; continue; }
+      kvqo_int2_load(rec, 0, p % PAGE, codes, &s16, &z16);
+      double s = kvqo_f16_to_f32(s16), z = kvqo_f16_to_f32(z16);
+      double acc = 0.0;
+      for (int d = 0; d < DIM; ++d) acc += qrot[d] * ((double)codes[d] * s + z);
+      logit[p] = sm_scale * (acc + qmu);
+      kvqo_int2_load(rec, 1, p % PAGE, codes, &s16, &z16);
+      s = kvqo_f16_to_f32(s16);
+      z = kvqo_f16_to_f32(z16);
+      double vrot[DIM];
+      for (int d = 0; d < DIM; ++d) vrot[d] = (double)codes[d] * s + z;
+      kvqo_rotate_t_f64(vrot, RV, DIM, vv);
+    }
+    for (int d = 0; d < DIM; ++d) vals[(size_t)p * DIM + d] = vv[d];
+    used[p] = 1;
+    if (logit[p] > mx) mx = logit[p];
+  }
+  double o[DIM], sum = 0.0;
+  for (int d = 0; d < DIM; ++d) o[d] = 0.0;
+  for (int p = 0; p < seq_len; ++p) {
+    if (!used[p]) continue;
+    double w = exp(logit[p] - mx);
+    sum += w;
+    for (int d = 0; d < DIM; ++d) o[d] += w * vals[(size_t)p * DIM + d];
+  }
+  for (int d = 0; d < DIM; ++d) o[d] = sum > 0.0 ? o[d] / sum : 0.0;
+  if (out_rotated) {
+    kvqo_rotate_f64(o, RV, DIM, out);
+  } else {
+    for (int d = 0; d < DIM; ++d) out[d] = o[d];
+  }
+  free(logit);
+  free(vals);
+  free(used);
+  return skipped;
+}
+
 /* Decode a list of (b, hq) pairs.  pairs : int32 [npairs][2]; out : [npairs][D].
  * q : bf16 [batch][H][D]; seq_lens : [batch].  kind 0 = INT2, 1 = BF16. */
+int kvqo_decode_window_pairs(const uint8_t* pool, int num_pool_pages, const uint8_t* bf16_pool,
+                             int bf16_num_pool_pages, const int32_t* bf16_page_table, int H, int Hkv,
+                             const uint16_t* q, const int32_t* page_table, int max_pages,
+                             const int32_t* seq_lens, const int32_t* pairs, int npairs, int sink,
+                             int recent, const float* R, const float* mu, double sm_scale,
+                             int out_rotated, double* out) {
+  int skipped = 0;
+  for (int i = 0; i < npairs; ++i) {
+    int b = pairs[2 * i], hq = pairs[2 * i + 1];
+    skipped += kvqo_decode_window_head(pool, num_pool_pages, bf16_pool, bf16_num_pool_pages,
+                                       bf16_page_table, H, Hkv, q + ((size_t)b * H + hq) * DIM,
+                                       page_table, max_pages, b, seq_lens[b], hq, sink, recent, R,
+                                       mu, sm_scale, out_rotated, out + (size_t)i * DIM);
+  }
+  return skipped;
+}
+
 int kvqo_decode_pairs(int kind, const uint8_t* pool, int num_pool_pages, int H, int Hkv,
                       const uint16_t* q, const int32_t* page_table, int max_pages,
                       const int32_t* seq_lens, const int32_t* pairs, int npairs, const float* R,

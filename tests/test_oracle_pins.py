@@ -467,3 +467,61 @@ def test_bf16_append_and_decode(orc):
                            W.bf16_bits_to_float(V[:, 0]).astype(np.float64).tolist(),
                            1 / math.sqrt(D))
     assert np.allclose(out[0], ref, rtol=1e-11, atol=1e-11)
+
+
+# ---------------------------------------------------------------------------
+# BF16 sink + recent window ("Assumptions & free parameters": 64 sink and 256
+# recent tokens kept in BF16).
+# ---------------------------------------------------------------------------
+
+def _window_fixture(orc, ctx=150):
+    wl = W.WORKLOADS["tiny_1k"]
+    pool, npool, pt, K, V, R, mu = _small_int2_cache(orc, wl, ctx)
+    bpool = np.zeros(npool * 8192, np.uint8)
+    assert orc.append_bf16(bpool, npool, 1, K, V, np.zeros(ctx), np.arange(ctx), pt) == 0
+    return wl, pool, npool, pt, bpool, K, V, R, mu
+
+
+def test_window_reduces_to_the_plain_paths(orc):
+    wl, pool, npool, pt, bpool, K, V, R, mu = _window_fixture(orc)
+    q = W.queries(wl, 0, 3)
+    pairs = [[0, h] for h in range(4)]
+    for L in (1, 37, 150):
+        # empty window: the INT2 path (the added q.mu is one constant per query)
+        w0 = orc.decode_window_pairs(pool, npool, bpool, npool, pt, 4, 1, q, pt, [L], pairs, 0, 0,
+                                     R, mu)
+        i2 = orc.decode_pairs("int2", pool, npool, 4, 1, q, pt, [L], pairs, R=R)
+        assert np.allclose(w0, i2, rtol=0, atol=1e-12 * max(1.0, np.abs(i2).max()))
+        # window covering the whole context: plain BF16 attention
+        wa = orc.decode_window_pairs(pool, npool, bpool, npool, pt, 4, 1, q, pt, [L], pairs, 64,
+                                     256, R, mu)
+        bf = orc.decode_pairs("bf16", bpool, npool, 4, 1, q, pt, [L], pairs)
+        assert np.allclose(wa, bf, rtol=0, atol=1e-12 * max(1.0, np.abs(bf).max()))
+
+
+def test_window_mixed_context_matches_direct_formula(orc):
+    wl, pool, npool, pt, bpool, K, V, R, mu = _window_fixture(orc)
+    q = W.queries(wl, 0, 4)
+    L, sink, recent = 150, 16, 40
+    Kd, Vd = orc.dequant_int2(pool, npool, 1, pt, 0, 0, L)
+    RK, RV = R[0, 0].astype(np.float64), R[1, 0].astype(np.float64)
+    out = orc.decode_window_pairs(pool, npool, bpool, npool, pt, 4, 1, q, pt, [L],
+                                  [[0, h] for h in range(4)], sink, recent, R, mu)
+    outr = orc.decode_window_pairs(pool, npool, bpool, npool, pt, 4, 1, q, pt, [L],
+                                   [[0, h] for h in range(4)], sink, recent, R, mu,
+                                   out_rotated=True)
+    for h in range(4):
+        qf = W.bf16_bits_to_float(q[0, h]).astype(np.float64)
+        lg, vals = [], []
+        for p in range(L):
+            if p < sink or p >= L - recent:
+                lg.append(qf @ W.bf16_bits_to_float(K[p, 0]).astype(np.float64))
+                vals.append(W.bf16_bits_to_float(V[p, 0]).astype(np.float64))
+            else:
+                lg.append((qf @ RK) @ Kd[p, 0].astype(np.float64) + qf @ mu[0].astype(np.float64))
+                vals.append(Vd[p, 0].astype(np.float64) @ RV.T)
+        lg = np.array(lg) / math.sqrt(D)
+        w = np.exp(lg - lg.max())
+        want = (w / w.sum()) @ np.array(vals)
+        assert np.allclose(out[h], want, rtol=1e-6, atol=1e-6)
+        assert np.allclose(outr[h], want @ RV, rtol=1e-6, atol=1e-6)
