@@ -226,6 +226,36 @@ int kvq_decode(kvq_handle* h, const void* pool, int num_pool_pages,
                const int32_t* seq_lens, int batch, float* out,
                void* workspace, size_t ws_bytes, int num_splits, void* stream);
 
+/* ---- decode with a BF16 sink + recent window ----------------------------------
+ * The OptR setting ("Assumptions & free parameters" of the OptR page: a BF16
+ * window of 64 sink and 256 recent tokens beside the INT2 cache).  For every
+ * sequence b and query head h, with len = seq_lens[b], position t is a window
+ * position if t < sink or t >= len - recent; the others are INT2 positions:
+ *     logit_t = sm_scale * q . k_t                    window  (BF16 cache, plain q)
+ *     logit_t = sm_scale * (q_rot . k~_t + q . mu)    INT2    (centring undone)
+ *     value_t = v_t (window)  or  v~_t * R_V^T (INT2)
+ *     out     = softmax(logit) . value               (out * R_V if KVQ_OUT_ROTATED)
+ * One softmax spans both kinds; q . mu puts the INT2 logits on the scale of the
+ * window ones.  sink = recent = 0 equals kvq_decode (up to that constant,
+ * which softmax ignores); a window covering [0, len) equals kvq_bf16_decode.
+ *   pool, page_table        : the INT2 cache, read at INT2 positions only.
+ *   bf16_pool               : device, BF16 page records (kvq_bf16_append),
+ *                             16-byte aligned, bf16_num_pool_pages pages.
+ *   bf16_page_table         : device int32 [batch][max_pages] (same max_pages as
+ *                             page_table); only entries of pages that hold a
+ *                             window position are read, so a caller may keep
+ *                             BF16 pages for the window alone.
+ *   sink, recent            : >= 0, any values (not tied to the page size).
+ *   workspace               : as for kvq_decode (kvq_workspace_bytes).
+ * Other arguments, errors and status bits as for kvq_decode; a window page id
+ * out of range sets KVQ_STATUS_BAD_PAGE and the page is skipped. */
+int kvq_decode_window(kvq_handle* h, const void* pool, int num_pool_pages,
+                      const void* bf16_pool, int bf16_num_pool_pages,
+                      const int32_t* bf16_page_table, const uint16_t* q,
+                      const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                      int batch, int sink, int recent, float* out, void* workspace,
+                      size_t ws_bytes, int num_splits, void* stream);
+
 /* ---- test export -----------------------------------------------------------
  * Dequantise positions [start, start+len) of sequence `seq` to fp32 in the
  * rotated (and, for keys, centred) basis: K_out[i][kv][d] = fmaf(code, s, z),
@@ -283,12 +313,12 @@ int kvq_get_status(kvq_handle* h, uint32_t* bits, void* stream);
 /* The number of splits kvq_decode uses when num_splits == 0. */
 int kvq_auto_splits(const kvq_handle* h, int batch, int max_pages);
 
-/* Kernel timing: while enabled, each kvq_decode / kvq_bf16_decode records a
- * CUDA event pair around its split-K attention kernel (only that kernel; it
- * includes the log-sum-exp merge, done by the last CTA of each (b, kv head)).
- * kvq_profile_read synchronises on the last event and returns the summed
- * milliseconds and the number of launches since the last enable, then clears
- * the record.  At most 65536 launches are recorded per enable. */
+/* Kernel timing: while enabled, each decode call (kvq_decode, kvq_decode_window,
+ * kvq_decode_static, kvq_bf16_decode) records a CUDA event pair around its
+ * split-K attention kernel only (not the query preparation, nor the
+ * log-sum-exp combine, which are separate kernels).  kvq_profile_read
+ * synchronises on the recorded events and returns the summed milliseconds and
+ * the number of launches since the last enable, then clears the record. */
 int kvq_profile_enable(kvq_handle* h, int enable);
 int kvq_profile_read(kvq_handle* h, double* total_ms, int* launches);
 

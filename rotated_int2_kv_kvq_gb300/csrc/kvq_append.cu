@@ -58,6 +58,10 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
   const float* mu = which ? nullptr : a.mu + static_cast<size_t>(kv) * kDim;
   const uint16_t* X = which ? a.V : a.K;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // A following decode call's query preparation reads neither the pool nor
+  // this kernel's inputs: let it start now (it waits for this grid before it
+  // finishes, so the decode kernel still sees every appended page).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // Stage this head's rotation matrix with one bulk copy.
   const uint32_t bar_a = smem_u32(bar);
@@ -260,6 +264,7 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
 // BF16 comparison cache: store each element unchanged at its layout position.
 // One CTA per (token, KV head); thread d handles element d of K and of V.
 __global__ void __launch_bounds__(128) append_bf16_kernel(AppendArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tok = blockIdx.x, kv = blockIdx.y, d = threadIdx.x;
   const int b = a.seq_idx[tok];
   const int p = a.positions[tok];

@@ -48,7 +48,7 @@ DecodeWs decode_ws_layout(int batch, int Hkv, int H, int splits, bool int2) {
   w.qfrag_off = o;
   if (int2) o += up(static_cast<size_t>(batch) * Hkv * kQFragWords * 4);
   w.qmeta_off = o;
-  if (int2) o += up(static_cast<size_t>(batch) * Hkv * 8 * 4);
+  if (int2) o += up(static_cast<size_t>(batch) * Hkv * kQMeta * 4);
   w.part_off = o;
   o += up(static_cast<size_t>(batch) * H * splits * kPartStride * 4);
   w.total = o;
@@ -75,11 +75,14 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // codes entering as code * 2^-16 (see the file comment) the score of a token is
 // q_rot . c = 2^(16 - e) * (hi + 2^-11 lo).  (Even k-blocks carry x * 2, odd ones
 // x / 2, matching the code scales 2^-17 and 2^-15 of code_op.)  Per head also: kappa =
-// sm_scale*log2e * 2^(16 - e) and zeta = sm_scale*log2e * sum(q_rot).
-// Launched as a programmatic dependent of the preceding kernel: it reads only
-// q and R_K, so it may run while a preceding append is still writing pages; it
-// waits for that kernel before it exits, so the decode kernel that waits for
-// this one also sees the appended pages.
+// sm_scale*log2e * 2^(16 - e), zeta = sm_scale*log2e * sum(q_rot) and
+// qmu = sm_scale*log2e * (q . mu), the logit shift that centring the keys took
+// out ("What carries the argument", mechanism 2); only a decode that mixes INT2
+// and BF16 tokens in one softmax needs it back.
+// Launched as a programmatic dependent of the preceding kernel: the bulk copy
+// of R_K (set by kvq_set_rotation, complete before any decode call starts) is
+// issued before the kernel waits for its predecessor; q, which a preceding
+// kernel may still be writing, is read only after that wait.
 // ---------------------------------------------------------------------------
 struct QprepSmem {
   float R[kDim * kDim];
@@ -92,6 +95,7 @@ struct QprepSmem {
 // One CTA per (sequence, KV head); thread i computes element i of the G
 // rotated query vectors.
 __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* __restrict__ RK,
+                                                    const float* __restrict__ mu,
                                                     float log2_scale) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   QprepSmem& sm = *reinterpret_cast<QprepSmem*>(smem_raw);
@@ -108,6 +112,7 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
     mbar_arrive_expect_tx(bar, kDim * kDim * 4);
     bulk_g2s(smem_u32(sm.R), RK + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
   }
+  griddep_wait();      // q may come from the preceding kernel
 #pragma unroll
   for (int h = 0; h < kMaxG; ++h) {
     float x = 0.0f;
@@ -120,7 +125,6 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
   const bool ok = mbar_wait_bounded(bar, 0);
   if (__syncthreads_or(!ok)) {
     if (i == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
-    griddep_wait();
     return;
   }
   float acc[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -136,17 +140,19 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
   // per-vector sum and max|.|: warp w handles vector w
   {
     const int w = i >> 5, lane = i & 31;
-    float s = 0.0f, m = 0.0f;
+    float s = 0.0f, m = 0.0f, qm = 0.0f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float x = sm.qr[w][lane + 32 * k];
       s += x;
       m = fmaxf(m, fabsf(x));
+      qm = fmaf(sm.qs[w][lane + 32 * k], mu[static_cast<size_t>(kv) * kDim + lane + 32 * k], qm);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       s += __shfl_xor_sync(0xffffffffu, s, off);
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      qm += __shfl_xor_sync(0xffffffffu, qm, off);
     }
     if (lane == 0) {
       int e = 0;
@@ -156,9 +162,10 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
         e = 14 - E;              // m * 2^e in [2^13, 2^14)
       }
       sm.e[w] = e;
-      float* qm = const_cast<float*>(a.qmeta) + (static_cast<size_t>(b) * a.Hkv + kv) * 8;
-      qm[2 * w] = (w < G) ? log2_scale * ldexpf(1.0f, 16 - e) : 0.0f;
-      qm[2 * w + 1] = (w < G) ? log2_scale * s : 0.0f;
+      float* meta = const_cast<float*>(a.qmeta) + (static_cast<size_t>(b) * a.Hkv + kv) * kQMeta;
+      meta[2 * w] = (w < G) ? log2_scale * ldexpf(1.0f, 16 - e) : 0.0f;
+      meta[2 * w + 1] = (w < G) ? log2_scale * s : 0.0f;
+      meta[8 + w] = (w < G) ? log2_scale * qm : 0.0f;
     }
   }
   __syncthreads();
@@ -189,7 +196,6 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
                     ((static_cast<size_t>(b) * a.Hkv + kv) * 32 + L) * 16 + 4 * quad;
     *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
   }
-  griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -409,9 +415,13 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     if (tid == 0 && split == 0 && hg == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
     seq_len = 0;
   }
-  const int n_pages = (seq_len + kPage - 1) / kPage;
-  const int p0 = split * a.chunk_pages;
-  const int npg = max(0, min(p0 + a.chunk_pages, n_pages) - p0);
+  // INT2 tokens: positions [lo, hi); with a BF16 window the first win_sink and
+  // the last win_recent positions are left to the window pass.
+  const int lo = a.win_sink;
+  const int hi = max(seq_len - a.win_recent, 0);
+  const int n_pages = (hi + kPage - 1) / kPage;
+  const int p0 = max(split * a.chunk_pages, lo / kPage);
+  const int npg = max(0, min(split * a.chunk_pages + a.chunk_pages, n_pages) - p0);
   const int32_t* ptab = a.page_table + static_cast<size_t>(b) * a.max_pages;
 
   // B fragments of the rotated query and the head's logit constants
@@ -425,8 +435,8 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
       qf[4 * r] = v.x; qf[4 * r + 1] = v.y; qf[4 * r + 2] = v.z; qf[4 * r + 3] = v.w;
     }
   }
-  const float kappa = a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * 8 + 2 * t];
-  const float zeta = a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * 8 + 2 * t + 1];
+  const float kappa = a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * kQMeta + 2 * t];
+  const float zeta = a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * kQMeta + 2 * t + 1];
 
   WarpState ws;
 #pragma unroll
@@ -462,9 +472,10 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
         break;
       }
       const int ua = k * PPS + gi, ub = ua + GPH;
-      // both pages of every warp present, valid and full of context
+      // both pages of every warp present, valid and all their tokens in [lo, hi)
       const bool full = all_ids_ok && (k + 1) * PPS <= nsub &&
-                        (p0 + sub + (k + 1) * PPS) * kPage <= seq_len;
+                        (p0 + sub + (k + 1) * PPS) * kPage <= hi &&
+                        (p0 + sub + k * PPS) * kPage >= lo;
       const uint8_t* sta = &sm.ring[slot][(gi * HPC + hl) * kInt2Rec];
       const uint8_t* stb = &sm.ring[slot][((GPH + gi) * HPC + hl) * kInt2Rec];
       const uint4 kwa = *reinterpret_cast<const uint4*>(sta + 16 * lane);
@@ -493,8 +504,10 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
         const bool oka = ua < nsub && sm.ids[ua] >= 0;
         const bool okb = ub < nsub && sm.ids[ub] >= 0;
         const int posa = (p0 + sub + ua) * kPage, posb = (p0 + sub + ub) * kPage;
-        const bool va0 = oka && (posa + g < seq_len), va1 = oka && (posa + g + 8 < seq_len);
-        const bool vb0 = okb && (posb + g < seq_len), vb1 = okb && (posb + g + 8 < seq_len);
+        const bool va0 = oka && posa + g >= lo && posa + g < hi;
+        const bool va1 = oka && posa + g + 8 >= lo && posa + g + 8 < hi;
+        const bool vb0 = okb && posb + g >= lo && posb + g < hi;
+        const bool vb1 = okb && posb + g + 8 >= lo && posb + g + 8 < hi;
         process_pair<true>(ws, qf, kappa, zeta, g, t, kwa, vwa, mta, kwb, vwb, mtb, va0, va1, vb0,
                            vb1);
       }
@@ -597,6 +610,64 @@ __device__ __forceinline__ void write_partial_bf16(CtaCombineSmem& cs, const Dec
   }
 }
 
+// B fragments of the plain query for the BF16 score product: column g =
+// 2*head + part; part 0 carries q (bf16, exact), part 1 is 0.
+__device__ __forceinline__ void bf16_q_frags(const DecodeArgs& a, int b, int kv, int g, int t,
+                                             uint32_t (&qf)[16]) {
+  const int head = g >> 1;
+  const bool use = ((g & 1) == 0) && head < a.G;
+  const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+      a.q + (static_cast<size_t>(b) * a.H + kv * a.G + (head < a.G ? head : 0)) * kDim);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    qf[2 * w] = use ? qrow[(16 * w + 2 * t) >> 1] : 0u;
+    qf[2 * w + 1] = use ? qrow[(16 * w + 2 * t + 8) >> 1] : 0u;
+  }
+}
+
+// Online-softmax update of one BF16 page for this lane: s = raw scores of
+// tokens g, g+8 (columns 2t, 2t+1 / rows g, g+8 of the C fragment), vf = the
+// lane's value A fragments, v0 / v1 = token masks.  The weights enter the value
+// product as a bf16 part plus a bf16 residual (columns 2*head, 2*head+1), so
+// acc[.][0] + acc[.][1] is the fp32-accurate P.V.
+__device__ __forceinline__ void bf16_page_update(const float (&s)[4], const uint4 (&vf)[8],
+                                                 bool v0, bool v1, float kappa, int g, int t,
+                                                 float (&acc)[8][4], float& m_run, float& l_run) {
+  const float l0 = v0 ? kappa * (s[0] + s[1]) : -INFINITY;
+  const float l1 = v1 ? kappa * (s[2] + s[3]) : -INFINITY;
+  float pm = fmaxf(l0, l1);
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+  pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+  if (pm > m_run) {
+    const float f = fast_exp2(m_run - pm);
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[mb][k] *= f;
+    l_run *= f;
+    m_run = pm;
+  }
+  const float P0 = v0 ? fast_exp2(l0 - m_run) : 0.0f;
+  const float P1 = v1 ? fast_exp2(l1 - m_run) : 0.0f;
+  l_run += P0 + P1;
+  const uint32_t X = pack_bf162(P0, P1);
+  const float x0 = __uint_as_float(X << 16), x1 = __uint_as_float(X & 0xffff0000u);
+  const uint32_t Y = pack_bf162(P0 - x0, P1 - x1);
+  const int src0 = 4 * (2 * t) + (g >> 1);
+  const uint32_t xa = __shfl_sync(0xffffffffu, X, src0);
+  const uint32_t ya = __shfl_sync(0xffffffffu, Y, src0);
+  const uint32_t xb = __shfl_sync(0xffffffffu, X, src0 + 4);
+  const uint32_t yb = __shfl_sync(0xffffffffu, Y, src0 + 4);
+  const uint32_t va = (g & 1) ? ya : xa;
+  const uint32_t vb = (g & 1) ? yb : xb;
+  const uint32_t pb0 = __byte_perm(va, vb, 0x5410);
+  const uint32_t pb1 = __byte_perm(va, vb, 0x7632);
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb)
+    mma_bf16(acc[mb], vf[mb].x, vf[mb].y, vf[mb].z, vf[mb].w, pb0, pb1);
+}
+
 // Per-warp page-id supply: lane j holds the page id of the warp's page 32*blk + j.
 struct PageIds {
   int cur, nxt, blk;
@@ -671,19 +742,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodeAr
   for (int j = 0; j < kStagesBf16 && j < count; ++j) issue(j);
   __syncwarp();
 
-  // B fragments: col g = 2*head + part; part 0 carries q (bf16, exact), part 1 is 0
   uint32_t qf[16];
-  {
-    const int head = g >> 1;
-    const bool use = ((g & 1) == 0) && head < a.G;
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        a.q + (static_cast<size_t>(b) * a.H + kv * a.G + (head < a.G ? head : 0)) * kDim);
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      qf[2 * w] = use ? qrow[(16 * w + 2 * t) >> 1] : 0u;
-      qf[2 * w + 1] = use ? qrow[(16 * w + 2 * t + 8) >> 1] : 0u;
-    }
-  }
+  bf16_q_frags(a, b, kv, g, t, qf);
   const float kappa = a.log2_scale;
 
   float acc[8][4];
@@ -722,39 +782,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodeAr
       if (lane == 0) fence_proxy_async();
       issue(i + kStagesBf16);
     }
-    const float l0 = v0 ? kappa * (s[0] + s[1]) : -INFINITY;
-    const float l1 = v1 ? kappa * (s[2] + s[3]) : -INFINITY;
-    float pm = fmaxf(l0, l1);
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-    if (pm > m_run) {
-      const float f = fast_exp2(m_run - pm);
-#pragma unroll
-      for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) acc[mb][k] *= f;
-      l_run *= f;
-      m_run = pm;
-    }
-    const float P0 = v0 ? fast_exp2(l0 - m_run) : 0.0f;
-    const float P1 = v1 ? fast_exp2(l1 - m_run) : 0.0f;
-    l_run += P0 + P1;
-    const uint32_t X = pack_bf162(P0, P1);
-    const float x0 = __uint_as_float(X << 16), x1 = __uint_as_float(X & 0xffff0000u);
-    const uint32_t Y = pack_bf162(P0 - x0, P1 - x1);
-    const int src0 = 4 * (2 * t) + (g >> 1);
-    const uint32_t xa = __shfl_sync(0xffffffffu, X, src0);
-    const uint32_t ya = __shfl_sync(0xffffffffu, Y, src0);
-    const uint32_t xb = __shfl_sync(0xffffffffu, X, src0 + 4);
-    const uint32_t yb = __shfl_sync(0xffffffffu, Y, src0 + 4);
-    const uint32_t va = (g & 1) ? ya : xa;
-    const uint32_t vb = (g & 1) ? yb : xb;
-    const uint32_t pb0 = __byte_perm(va, vb, 0x5410);
-    const uint32_t pb1 = __byte_perm(va, vb, 0x7632);
-#pragma unroll
-    for (int mb = 0; mb < 8; ++mb)
-      mma_bf16(acc[mb], vf[mb].x, vf[mb].y, vf[mb].z, vf[mb].w, pb0, pb1);
+    bf16_page_update(s, vf, v0, v1, kappa, g, t, acc, m_run, l_run);
   }
   if (i < count) {
     for (int j = i + 1; j < count && j < i + kStagesBf16; ++j)
@@ -783,47 +811,178 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodeAr
 // in shared memory by a bulk copy issued before the kernel waits for the decode
 // kernel, so the copy overlaps the decode tail.  Warp h reduces the split
 // maxima and weights of head h; thread (h, d) then forms element d of head h.
+//
+// With a BF16 window (kWindow) the kernel first attends, with the plain query,
+// over the window tokens of the BF16 cache (the first win_sink and the last
+// win_recent positions), before it waits for the decode kernel: those reads
+// need nothing from it, and every kernel before it has finished by the time
+// the decode kernel lets it launch.  The merge then adds q.mu back to the INT2
+// partials (their logits were taken against centred keys) and sums both parts
+// in one softmax, in the plain basis (INT2 part rotated back) or, for
+// KVQ_OUT_ROTATED, in the rotated one (window part rotated forward by R_V).
 // ---------------------------------------------------------------------------
+constexpr int kCombineThreads = kMaxG * kDim;   // 512
+constexpr int kCombineWarps = kCombineThreads / 32;
+
 struct CombineSmem {
-  float Rt[kDim * kDim];
+  float Rt[kDim * kDim];      // R_V^T, or R_V for a rotated-basis output with a window
   float w[kMaxG][kMaxSplits];
   float o[kMaxG][kDim];
   float linv[kMaxG];
+  float ww[kMaxG];            // weight of the window part
   uint64_t bar;
 };
-constexpr int kCombineThreads = kMaxG * kDim;   // 512
 
+struct WindowSmem {
+  float o[kCombineWarps][kMaxG][kDim];
+  float m[kCombineWarps][kMaxG];
+  float l[kCombineWarps][kMaxG];
+  float M[kMaxG], L[kMaxG];
+};
+
+struct CombineWindowSmem {    // dynamic shared memory of combine_kernel<true>
+  CombineSmem c;
+  WindowSmem win;
+};
+
+// BF16 window part of (b, kv): tokens p < win_sink or p >= len - win_recent.
+// Warp w takes window pages w, w + 16, ...; each lane loads its fragments of a
+// page straight from global memory (the record is in fragment order).  Leaves
+// the window maximum / sum per head in ws.M / ws.L and returns, for thread
+// (h, d), element d of head h's window output relative to ws.M[h].
+__device__ float window_partial(const DecodeArgs& a, WindowSmem& ws, int b, int kv) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  int len = a.seq_lens[b];
+  if (len < 0 || len > a.max_pages * kPage) len = 0;   // flagged by the decode kernel
+  const int sink = min(a.win_sink, len);
+  const int rstart = max(len - a.win_recent, 0);       // first recent position
+  const int n_pages = (len + kPage - 1) / kPage;
+  const int A = (sink + kPage - 1) / kPage;             // pages holding sink tokens
+  const int Bp = max(A, rstart / kPage);                // first further page holding recent ones
+  const int nwin = A + (n_pages - Bp);
+  const int32_t* ptab = a.bf16_page_table + static_cast<size_t>(b) * a.max_pages;
+
+  uint32_t qf[16];
+  bf16_q_frags(a, b, kv, g, t, qf);
+  float acc[8][4];
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[mb][k] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f;
+  for (int i = warp; i < nwin; i += kCombineWarps) {
+    const int pg = i < A ? i : Bp + (i - A);
+    const int id = ptab[pg];
+    if (id < 0 || id >= a.bf16_num_pool_pages) {
+      if (lane == 0) atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+      continue;
+    }
+    const uint8_t* rec = a.bf16_pool + (static_cast<size_t>(id) * a.Hkv + kv) * kBf16Rec;
+    uint4 vf[8];
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+      vf[mb] = __ldg(reinterpret_cast<const uint4*>(rec + 4096 + 512 * mb + 16 * lane));
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const uint4 kf = __ldg(reinterpret_cast<const uint4*>(rec + 512 * w + 16 * lane));
+      mma_bf16(s, kf.x, kf.y, kf.z, kf.w, qf[2 * w], qf[2 * w + 1]);
+    }
+    const int pos0 = pg * kPage + g, pos1 = pos0 + 8;
+    const bool v0 = pos0 < len && (pos0 < sink || pos0 >= rstart);
+    const bool v1 = pos1 < len && (pos1 < sink || pos1 >= rstart);
+    bf16_page_update(s, vf, v0, v1, a.log2_scale, g, t, acc, m_run, l_run);
+  }
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
+  if (t < a.G) {
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      ws.o[warp][t][16 * mb + g] = acc[mb][0] + acc[mb][1];
+      ws.o[warp][t][16 * mb + g + 8] = acc[mb][2] + acc[mb][3];
+    }
+    if (g == 0) {
+      ws.m[warp][t] = m_run;
+      ws.l[warp][t] = l_run;
+    }
+  }
+  __syncthreads();
+  const int h = tid / kDim, d = tid % kDim;
+  float o = 0.0f;
+  if (h < a.G) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) M = fmaxf(M, ws.m[w][h]);
+    float L = 0.0f;
+    if (M > -INFINITY) {
+#pragma unroll 4
+      for (int w = 0; w < kCombineWarps; ++w) {
+        if (ws.m[w][h] == -INFINITY) continue;
+        const float f = fast_exp2(ws.m[w][h] - M);
+        L = fmaf(f, ws.l[w][h], L);
+        o = fmaf(f, ws.o[w][h][d], o);
+      }
+    }
+    if (d == 0) {
+      ws.M[h] = M;
+      ws.L[h] = L;
+    }
+  }
+  return o;
+}
+
+template <bool kWindow>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   CombineSmem& sm = *reinterpret_cast<CombineSmem*>(smem_raw);
+  WindowSmem& ws = *reinterpret_cast<WindowSmem*>(smem_raw + sizeof(CombineSmem));
   const int b = blockIdx.x, kv = blockIdx.y, tid = threadIdx.x;
   const int h = tid / kDim, d = tid % kDim;       // thread (h, d)
   const int warp = tid >> 5, lane = tid & 31;
   const int S = a.splits, G = a.G;
   const uint32_t bar = smem_u32(&sm.bar);
-  if (a.rotate_out && tid == 0) {
+  // the matrix of the one basis change: R_V^T (INT2 part back to the plain
+  // basis) or, for a rotated-basis output, R_V (window part forward)
+  const bool stage = kWindow || a.rotate_out;
+  if (stage && tid == 0) {
+    const float* R = a.rotate_out ? a.RVt : a.RV;
     mbar_init(bar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(bar, kDim * kDim * 4);
-    bulk_g2s(smem_u32(sm.Rt), a.RVt + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
+    bulk_g2s(smem_u32(sm.Rt), R + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
   }
+  float owin = 0.0f;
+  if constexpr (kWindow) owin = window_partial(a, ws, b, kv);
   griddep_wait();       // the partials come from the decode kernel
+  if (kWindow) __syncthreads();   // ws.M / ws.L
   if (warp < G) {
     const float* parts = a.part + (static_cast<size_t>(b) * a.H + kv * G + warp) * S * kPartStride;
+    // INT2 logits were taken against centred keys: with a window, add q.mu back
+    const float qmu =
+        kWindow ? a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * kQMeta + 8 + warp] : 0.0f;
     float M = -INFINITY;
     for (int j = lane; j < S; j += 32) M = fmaxf(M, parts[j * kPartStride]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (kWindow) M = fmaxf(M + qmu, ws.M[warp]);
     float L = 0.0f;
     for (int j = lane; j < S; j += 32) {
       const float mj = parts[j * kPartStride];
-      const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj - M);
+      const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj + qmu - M);
       sm.w[warp][j] = w;
       L = fmaf(w, parts[j * kPartStride + 1], L);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (lane == 0) sm.linv[warp] = (L > 0.0f) ? 1.0f / L : 0.0f;
+    if (lane == 0) {
+      if (kWindow) {
+        const float ww = (ws.M[warp] == -INFINITY) ? 0.0f : fast_exp2(ws.M[warp] - M);
+        sm.ww[warp] = ww;
+        L = fmaf(ww, ws.L[warp], L);
+      }
+      sm.linv[warp] = (L > 0.0f) ? 1.0f / L : 0.0f;
+    }
   }
   __syncthreads();
   float o = 0.0f;
@@ -831,10 +990,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(DecodeArgs a) 
     const float* parts = a.part + (static_cast<size_t>(b) * a.H + kv * G + h) * S * kPartStride;
 #pragma unroll 8
     for (int j = 0; j < S; ++j) o = fmaf(sm.w[h][j], parts[j * kPartStride + 4 + d], o);
-    o *= sm.linv[h];
+    if (!kWindow) o *= sm.linv[h];
   }
-  if (a.rotate_out) {
-    sm.o[h][d] = o;
+  if (stage) {
+    // y R for the part that changes basis
+    sm.o[h][d] = (kWindow && !a.rotate_out) ? owin : o;
     const bool ok = mbar_wait_bounded(bar, 0);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
@@ -843,7 +1003,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(DecodeArgs a) 
     float r = 0.0f;
 #pragma unroll 8
     for (int j = 0; j < kDim; ++j) r = fmaf(sm.o[h][j], sm.Rt[j * kDim + d], r);
-    o = r;
+    if (!kWindow) o = r;
+    else if (h < G) o = (a.rotate_out ? fmaf(sm.ww[h], owin, r) : fmaf(sm.ww[h], r, o)) * sm.linv[h];
   }
   if (h < G) a.out[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + d] = o;
 }
@@ -933,11 +1094,12 @@ cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_
 
 }  // namespace
 
-cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, float sm_scale, cudaStream_t st) {
+cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, const float* mu, float sm_scale,
+                         cudaStream_t st) {
   cudaError_t e = set_smem_attr<QprepSmem>(qprep_kernel);
   if (e != cudaSuccess) return e;
   dim3 grid(a.batch, a.Hkv);
-  e = launch_dependent(qprep_kernel, grid, dim3(128), sizeof(QprepSmem), st, a, RK,
+  e = launch_dependent(qprep_kernel, grid, dim3(128), sizeof(QprepSmem), st, a, RK, mu,
                        sm_scale * kLog2e);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -959,10 +1121,18 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st) {
-  cudaError_t e = set_smem_attr<CombineSmem>(combine_kernel);
-  if (e != cudaSuccess) return e;
-  e = launch_dependent(combine_kernel, dim3(a.batch, a.Hkv), dim3(kCombineThreads),
-                       sizeof(CombineSmem), st, a);
+  cudaError_t e;
+  if (a.window) {
+    e = set_smem_attr<CombineWindowSmem>(combine_kernel<true>);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(combine_kernel<true>, dim3(a.batch, a.Hkv), dim3(kCombineThreads),
+                         sizeof(CombineWindowSmem), st, a);
+  } else {
+    e = set_smem_attr<CombineSmem>(combine_kernel<false>);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(combine_kernel<false>, dim3(a.batch, a.Hkv), dim3(kCombineThreads),
+                         sizeof(CombineSmem), st, a);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -141,13 +141,27 @@ int check_decode_args(kvq_handle* h, const void* pool, int num_pool_pages, const
   return KVQ_OK;
 }
 
+// The BF16 window of kvq_decode_window (absent for the plain decodes).
+struct Window {
+  const void* bf16_pool = nullptr;
+  int bf16_num_pool_pages = 0;
+  const int32_t* bf16_page_table = nullptr;
+  int sink = 0, recent = 0;
+  bool on = false;
+};
+
 int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages,
                   const uint16_t* q, const int32_t* page_table, int max_pages,
                   const int32_t* seq_lens, int batch, float* out, void* workspace,
-                  size_t ws_bytes, int num_splits, void* stream) {
+                  size_t ws_bytes, int num_splits, void* stream, const Window& win = Window()) {
   int rc = check_decode_args(h, pool, num_pool_pages, q, page_table, max_pages, seq_lens, batch,
                              out, workspace, num_splits);
   if (rc != KVQ_OK) return rc;
+  if (win.on) {
+    if (!win.bf16_pool || !win.bf16_page_table || win.bf16_num_pool_pages < 1) return KVQ_EINVAL;
+    if (win.sink < 0 || win.recent < 0) return KVQ_EINVAL;
+    if (reinterpret_cast<uintptr_t>(win.bf16_pool) % 16 != 0) return KVQ_EINVAL;
+  }
   if (int2 && !h->ready) return KVQ_ENOTREADY;
   const int splits = num_splits ? num_splits : choose_splits(h, batch, max_pages, int2);
   const kvq::DecodeWs w =
@@ -174,13 +188,21 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
   a.hpc = heads_per_cta(a.Hkv);
   a.out = out;
   a.RVt = h->bank ? h->bank + static_cast<size_t>(2) * a.Hkv * kDim * kDim : nullptr;
+  a.RV = h->bank ? h->bank + static_cast<size_t>(a.Hkv) * kDim * kDim : nullptr;
   a.rotate_out = (int2 && !(h->L.flags & KVQ_OUT_ROTATED)) ? 1 : 0;
   a.status = h->status;
   a.log2_scale = h->sm_scale * 1.4426950408889634f;
+  a.window = win.on ? 1 : 0;
+  a.win_sink = win.on ? win.sink : 0;
+  a.win_recent = win.on ? win.recent : 0;
+  a.bf16_pool = static_cast<const uint8_t*>(win.bf16_pool);
+  a.bf16_num_pool_pages = win.bf16_num_pool_pages;
+  a.bf16_page_table = win.bf16_page_table;
   cudaStream_t st = S(stream);
   cudaError_t e;
   if (int2) {
-    e = kvq::launch_qprep(a, h->bank, h->sm_scale, st);
+    const float* mu = h->bank + static_cast<size_t>(3) * a.Hkv * kDim * kDim;
+    e = kvq::launch_qprep(a, h->bank, mu, h->sm_scale, st);
     if (e != cudaSuccess) return KVQ_ECUDA;
   }
   int slot;
@@ -334,6 +356,23 @@ int kvq_decode(kvq_handle* h, const void* pool, int num_pool_pages, const uint16
                float* out, void* workspace, size_t ws_bytes, int num_splits, void* stream) {
   return decode_common(h, true, pool, num_pool_pages, q, page_table, max_pages, seq_lens, batch,
                        out, workspace, ws_bytes, num_splits, stream);
+}
+
+int kvq_decode_window(kvq_handle* h, const void* pool, int num_pool_pages,
+                      const void* bf16_pool, int bf16_num_pool_pages,
+                      const int32_t* bf16_page_table, const uint16_t* q,
+                      const int32_t* page_table, int max_pages, const int32_t* seq_lens, int batch,
+                      int sink, int recent, float* out, void* workspace, size_t ws_bytes,
+                      int num_splits, void* stream) {
+  Window win;
+  win.bf16_pool = bf16_pool;
+  win.bf16_num_pool_pages = bf16_num_pool_pages;
+  win.bf16_page_table = bf16_page_table;
+  win.sink = sink;
+  win.recent = recent;
+  win.on = true;
+  return decode_common(h, true, pool, num_pool_pages, q, page_table, max_pages, seq_lens, batch,
+                       out, workspace, ws_bytes, num_splits, stream, win);
 }
 
 int kvq_bf16_decode(kvq_handle* h, const void* pool, int num_pool_pages, const uint16_t* q,

@@ -19,6 +19,7 @@ constexpr int kBf16Rec = KVQ_BF16_RECORD_BYTES;
 constexpr int kMaxG = 4;           // query heads per KV head handled per CTA
 constexpr int kPartStride = 132;   // floats per split partial: m, l, 2 pad, o[128]
 constexpr int kQFragWords = 32 * 16;   // uint32 per (b, kv): 32 lanes x 16 B-fragment regs
+constexpr int kQMeta = 12;         // floats per (b, kv): {kappa, zeta} x 4 heads, q.mu x 4 heads
 constexpr int kMaxSplits = 1024;
 constexpr int kDecodeWarps = 4;    // BF16 decode CTA
 constexpr int kInt2Warps = 8;      // INT2 decode CTA
@@ -42,13 +43,20 @@ struct DecodeArgs {
   int splits, chunk_pages;
   int hpc;                   // KV heads per INT2 decode CTA (1, 2, 4 or 8; divides Hkv)
   const uint32_t* qfrag;     // [B][Hkv][32][16]
-  const float* qmeta;        // [B][Hkv][4][2]: kappa, zeta per head
+  const float* qmeta;        // [B][Hkv][kQMeta]: kappa, zeta per head, then q.mu per head
   float* part;               // [B][H][splits][kPartStride]
   float* out;                // [B][H][D]
   const float* RVt;          // [Hkv][D][D] transposed value rotations
+  const float* RV;           // [Hkv][D][D] value rotations
   int rotate_out;            // 1: out = o_rot R_V^T, 0: out = o_rot
   uint32_t* status;
   float log2_scale;          // sm_scale * log2(e)
+  // BF16 window (sink + recent tokens); window = 0 for a plain decode
+  int window;
+  int win_sink, win_recent;
+  const uint8_t* bf16_pool;
+  int bf16_num_pool_pages;
+  const int32_t* bf16_page_table;   // [B][max_pages]
 };
 
 struct AppendArgs {
@@ -70,7 +78,8 @@ struct AppendArgs {
 // ---- launchers (defined in the .cu files) --------------------------------
 cudaError_t launch_append_int2(const AppendArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_append_bf16(const AppendArgs& a, cudaStream_t st);
-cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, float sm_scale, cudaStream_t st);
+cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, const float* mu, float sm_scale,
+                         cudaStream_t st);
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st);

@@ -41,6 +41,8 @@ SIGNATURES = {
     "kvq_bf16_workspace_bytes": ([_P, _I, _I], _SZ),
     "kvq_bf16_decode": ([_P, _P, _I, _P, _P, _I, _P, _I, _P, _P, _SZ, _I, _P], _I),
     "kvq_decode_static": ([_P, _P, _I, _P, _P, _I, _P, _I, _P, _I, _P], _I),
+    "kvq_decode_window": ([_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _SZ, _I,
+                           _P], _I),
     "kvq_get_status": ([_P, _P, _P], _I),
     "kvq_auto_splits": ([_P, _I, _I], _I),
     "kvq_profile_enable": ([_P, _I], _I),
@@ -231,6 +233,24 @@ def kvq_decode_static(h, pool, num_pool_pages, q, page_table, seq_lens, out, num
         h.ptr, _ptr(pool, _U8, "pool"), int(num_pool_pages), _ptr(q, _BF16, "q"),
         _ptr(page_table, _I32, "page_table"), max_pages, _ptr(seq_lens, _I32, "seq_lens"),
         batch, _ptr(out, _F32, "out"), int(num_splits), _stream(stream)))
+
+
+def kvq_decode_window(h, pool, num_pool_pages, bf16_pool, bf16_num_pool_pages, bf16_page_table,
+                      q, page_table, seq_lens, sink, recent, out, workspace, num_splits=0,
+                      stream=None):
+    """Decode with a BF16 window: positions < sink and >= len - recent from the
+    BF16 cache (bf16_page_table: int32 [B, P], same shape as page_table), the
+    others from the INT2 cache, in one softmax.  Workspace as for kvq_decode."""
+    batch, max_pages = int(page_table.shape[0]), int(page_table.shape[1])
+    if tuple(bf16_page_table.shape) != (batch, max_pages):
+        raise ValueError("bf16_page_table must have the shape of page_table")
+    _check("kvq_decode_window", load_library().kvq_decode_window(
+        h.ptr, _ptr(pool, _U8, "pool"), int(num_pool_pages), _ptr(bf16_pool, _U8, "bf16_pool"),
+        int(bf16_num_pool_pages), _ptr(bf16_page_table, _I32, "bf16_page_table"),
+        _ptr(q, _BF16, "q"), _ptr(page_table, _I32, "page_table"), max_pages,
+        _ptr(seq_lens, _I32, "seq_lens"), batch, int(sink), int(recent), _ptr(out, _F32, "out"),
+        _ptr(workspace, _U8, "workspace"), int(workspace.numel()), int(num_splits),
+        _stream(stream)))
 
 
 def kvq_dequant(h, pool, num_pool_pages, page_table, seq, start, length, K_out=None, V_out=None,

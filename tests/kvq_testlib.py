@@ -142,3 +142,42 @@ def compare_codes(cache: Cache, pool_np: np.ndarray, samples, Ktok, Vtok):
                 assert frac <= np.spacing(np.float32(t[i])), (s, p, kv, which, i, t[i], c[i], c2[i])
                 near += 1
     return near
+
+
+# ---- BF16 sink + recent window ---------------------------------------------------
+
+def window_page_table(lens, max_pages, sink, recent):
+    """A BF16 page table that maps only the pages holding a window position
+    (p < sink or p >= len - recent) of each sequence; other entries are -1.
+    Returns (table int32 [B, max_pages], num_pool_pages)."""
+    pt = np.full((len(lens), max_pages), -1, np.int32)
+    n = 0
+    for b, L in enumerate(lens):
+        for pg in range((int(L) + 15) // 16):
+            first, last = 16 * pg, min(16 * pg + 16, int(L)) - 1
+            if first < sink or last >= int(L) - recent:
+                pt[b, pg] = n
+                n += 1
+    return pt, max(n, 1)
+
+
+def window_positions(L, sink, recent):
+    return [p for p in range(int(L)) if p < sink or p >= int(L) - recent]
+
+
+def window_decode(ci: Cache, cb: Cache, q_np, seq_lens, sink, recent, num_splits=0):
+    """kvq_decode_window over INT2 cache `ci` and BF16 cache `cb`."""
+    B = ci.pt_np.shape[0]
+    out = torch.empty((B, ci.H, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.kvq_workspace_bytes(ci.h, B, num_splits), dtype=torch.uint8, device="cuda")
+    K.kvq_decode_window(ci.h, ci.pool, ci.npool, cb.pool, cb.npool, cb.pt, u16(q_np), ci.pt,
+                        i32(seq_lens), int(sink), int(recent), out, ws, num_splits)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64)
+
+
+def oracle_window(ci: Cache, cb: Cache, q_np, seq_lens, pairs, sink, recent):
+    return oracle.decode_window_pairs(
+        ci.pool_host(), ci.npool, cb.pool_host(), cb.npool, cb.pt_np, ci.H, ci.Hkv, q_np,
+        ci.pt_np, seq_lens, pairs, sink, recent, ci.R, ci.mu,
+        out_rotated=bool(ci.layout.flags & K.KVQ_OUT_ROTATED))

@@ -14,7 +14,8 @@ import pytest
 import torch
 
 import oracle
-from kvq_testlib import Cache, assert_close_attention, compare_codes, i32, u16
+from kvq_testlib import (Cache, assert_close_attention, compare_codes, i32, oracle_window, u16,
+                         window_decode, window_page_table, window_positions)
 from rotated_int2_kv_kvq_gb300 import kvq as K
 from rotated_int2_kv_kvq_gb300 import workloads as W
 
@@ -187,6 +188,33 @@ def test_qwen32k_decode_sampled(qwen32k):
     pairs += [[0, 0], [15, 31]]
     want = c.oracle_decode(c.pool_host(), q, lens, pairs)
     assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want, "qwen32k")
+
+
+def test_qwen32k_window_decode_sampled(qwen32k):
+    """The OptR setting at full size: 64 sink + 256 recent tokens from a BF16
+    cache that holds the window pages only, the rest from the INT2 cache, the
+    automatic split choice."""
+    c = qwen32k
+    sink, recent = 64, 256
+    lens = [c.wl.ctx] * c.wl.batch
+    pt, npool = window_page_table(lens, c.pt_np.shape[1], sink, recent)
+    cb = Cache(c.wl, kind="bf16", page_table=pt, num_pool_pages=npool)
+    pos = np.array(window_positions(c.wl.ctx, sink, recent), np.int32)
+    assert len(pos) == sink + recent
+    for b in range(c.wl.batch):
+        Kw = np.concatenate([W.tokens(c.wl, 0, b, 0, 0, sink),
+                             W.tokens(c.wl, 0, b, 0, c.wl.ctx - recent, recent)])
+        Vw = np.concatenate([W.tokens(c.wl, 0, b, 1, 0, sink),
+                             W.tokens(c.wl, 0, b, 1, c.wl.ctx - recent, recent)])
+        cb.append(Kw, Vw, np.full(len(pos), b), pos)
+    q = W.queries(c.wl, 0, 2)
+    got = window_decode(c, cb, q, lens, sink, recent, 0)
+    rng = np.random.default_rng(25)
+    pairs = [[int(rng.integers(0, 16)), int(rng.integers(0, 32))] for _ in range(8)]
+    pairs += [[0, 0], [15, 31]]
+    want = oracle_window(c, cb, q, lens, pairs, sink, recent)
+    assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want, "window 32k")
+    assert c.status() == 0 and cb.status() == 0
 
 
 @pytest.mark.parametrize("splits", [64, 128, 256])
