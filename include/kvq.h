@@ -77,6 +77,11 @@ extern "C" {
  * o_rot * R_V^T.  This is the deployment form in which R_V is folded into
  * W_V / W_O ("If this is right", third item). */
 #define KVQ_OUT_ROTATED 1u
+/* The query passed to kvq_decode is already in the rotated key basis,
+ * q_rot = q * R_K (the caller folded R_K into its query projection, after any
+ * position encoding), so decode skips the query rotation.  Rejected by
+ * kvq_decode_window (KVQ_EINVAL), whose BF16 tokens need the plain query. */
+#define KVQ_Q_ROTATED 2u
 
 typedef struct kvq_layout {
   int32_t num_heads;     /* H, query heads                                      */
@@ -87,7 +92,7 @@ typedef struct kvq_layout {
   float clip_k;          /* key clip ratio c_K, in (0, 1]; the pages use 0.96   */
   float clip_v;          /* value clip ratio c_V, in (0, 1]; the pages use 0.92 */
   float sm_scale;        /* softmax scale; <= 0 selects 1/sqrt(head_dim)        */
-  uint32_t flags;        /* KVQ_OUT_ROTATED or 0                                */
+  uint32_t flags;        /* 0 or an OR of KVQ_OUT_ROTATED, KVQ_Q_ROTATED         */
 } kvq_layout;
 
 typedef struct kvq_handle kvq_handle;
@@ -204,7 +209,8 @@ int kvq_append(kvq_handle* h, void* pool, int num_pool_pages,
 size_t kvq_workspace_bytes(const kvq_handle* h, int batch, int num_splits);
 
 /* One decode step for every sequence b in [0, batch):
- *     q_rot   = q[b][h] * R_K(kv)             (kv = h / (H / Hkv))
+ *     q_rot   = q[b][h] * R_K(kv)             (kv = h / (H / Hkv); q itself
+ *                                               with KVQ_Q_ROTATED)
  *     logit_t = sm_scale * q_rot . k~_t        for positions t in [0, seq_lens[b])
  *     o_rot   = softmax(logit) . v~
  *     out     = o_rot * R_V(kv)^T              (o_rot if KVQ_OUT_ROTATED)

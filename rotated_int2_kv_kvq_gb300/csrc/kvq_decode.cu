@@ -79,6 +79,7 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // qmu = sm_scale*log2e * (q . mu), the logit shift that centring the keys took
 // out ("What carries the argument", mechanism 2); only a decode that mixes INT2
 // and BF16 tokens in one softmax needs it back.
+// RK == nullptr: q is already rotated (KVQ_Q_ROTATED) and is used as it is.
 // Launched as a programmatic dependent of the preceding kernel: the bulk copy
 // of R_K (set by kvq_set_rotation, complete before any decode call starts) is
 // issued before the kernel waits for its predecessor; q, which a preceding
@@ -102,16 +103,15 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
   const int b = blockIdx.x, kv = blockIdx.y, i = threadIdx.x;
   const int G = a.G;
   griddep_launch_dependents();
+  const bool rotate = RK != nullptr;
   const uint32_t bar = smem_u32(&sm.bar);
-  if (i == 0) {
+  if (rotate && i == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-  }
-  __syncthreads();
-  if (i == 0) {
     mbar_arrive_expect_tx(bar, kDim * kDim * 4);
     bulk_g2s(smem_u32(sm.R), RK + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
   }
+  __syncthreads();     // the barrier is initialised before any thread waits on it
   griddep_wait();      // q may come from the preceding kernel
 #pragma unroll
   for (int h = 0; h < kMaxG; ++h) {
@@ -122,20 +122,25 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
     }
     sm.qs[h][i] = x;
   }
-  const bool ok = mbar_wait_bounded(bar, 0);
-  if (__syncthreads_or(!ok)) {
-    if (i == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
-    return;
-  }
-  float acc[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (rotate) {
+    const bool ok = mbar_wait_bounded(bar, 0);
+    if (__syncthreads_or(!ok)) {
+      if (i == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+      return;
+    }
+    float acc[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 8
-  for (int j = 0; j < kDim; ++j) {
-    const float r = sm.R[j * kDim + i];
+    for (int j = 0; j < kDim; ++j) {
+      const float r = sm.R[j * kDim + i];
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h) acc[h] = fmaf(sm.qs[h][j], r, acc[h]);
+      for (int h = 0; h < kMaxG; ++h) acc[h] = fmaf(sm.qs[h][j], r, acc[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) sm.qr[h][i] = acc[h];
+  } else {
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) sm.qr[h][i] = sm.qs[h][i];
   }
-#pragma unroll
-  for (int h = 0; h < kMaxG; ++h) sm.qr[h][i] = acc[h];
   __syncthreads();
   // per-vector sum and max|.|: warp w handles vector w
   {

@@ -44,7 +44,7 @@ bool layout_ok(const kvq_layout* L) {
   if (!(L->clip_k > 0.f && L->clip_k <= 1.f) || !(L->clip_v > 0.f && L->clip_v <= 1.f))
     return false;
   if (!(L->sm_scale == L->sm_scale)) return false;        // NaN
-  if (L->flags & ~KVQ_OUT_ROTATED) return false;
+  if (L->flags & ~(KVQ_OUT_ROTATED | KVQ_Q_ROTATED)) return false;
   return true;
 }
 
@@ -158,6 +158,7 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
                              out, workspace, num_splits);
   if (rc != KVQ_OK) return rc;
   if (win.on) {
+    if (h->L.flags & KVQ_Q_ROTATED) return KVQ_EINVAL;
     if (!win.bf16_pool || !win.bf16_page_table || win.bf16_num_pool_pages < 1) return KVQ_EINVAL;
     if (win.sink < 0 || win.recent < 0) return KVQ_EINVAL;
     if (reinterpret_cast<uintptr_t>(win.bf16_pool) % 16 != 0) return KVQ_EINVAL;
@@ -202,7 +203,8 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
   cudaError_t e;
   if (int2) {
     const float* mu = h->bank + static_cast<size_t>(3) * a.Hkv * kDim * kDim;
-    e = kvq::launch_qprep(a, h->bank, mu, h->sm_scale, st);
+    const bool q_rotated = (h->L.flags & KVQ_Q_ROTATED) != 0;
+    e = kvq::launch_qprep(a, q_rotated ? nullptr : h->bank, mu, h->sm_scale, st);
     if (e != cudaSuccess) return KVQ_ECUDA;
   }
   int slot;

@@ -22,6 +22,7 @@ KVQ_STATUS_BAD_SEQLEN = 4
 KVQ_STATUS_BAD_SEQ = 8
 KVQ_STATUS_TIMEOUT = 16
 KVQ_OUT_ROTATED = 1
+KVQ_Q_ROTATED = 2
 INT2_RECORD_BYTES = 1152
 BF16_RECORD_BYTES = 8192
 
@@ -139,9 +140,11 @@ class Handle:
 
 
 def make_layout(num_heads, num_kv_heads, clip_k=0.96, clip_v=0.92, sm_scale=0.0,
-                out_rotated=False, head_dim=128, group=128, page_size=16) -> KvqLayout:
+                out_rotated=False, head_dim=128, group=128, page_size=16,
+                q_rotated=False) -> KvqLayout:
+    flags = (KVQ_OUT_ROTATED if out_rotated else 0) | (KVQ_Q_ROTATED if q_rotated else 0)
     return KvqLayout(num_heads, num_kv_heads, head_dim, group, page_size, clip_k, clip_v,
-                     sm_scale, KVQ_OUT_ROTATED if out_rotated else 0)
+                     sm_scale, flags)
 
 
 # ---- entry points (same names as the C ABI) ------------------------------------

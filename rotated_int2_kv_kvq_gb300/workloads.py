@@ -249,3 +249,12 @@ def cache_bytes_per_token_head(kind: str = "int2") -> int:
 def effective_bits(group: int = 128) -> float:
     """Bits per cached element: 2-bit code plus two fp16 per group."""
     return 2.0 + 32.0 / group
+
+
+def effective_bits_window(ctx: int, sink: int = 64, recent: int = 256, group: int = 128) -> float:
+    """Bits per cached element of a context of `ctx` tokens whose first `sink`
+    and last `recent` tokens stay in BF16 (16 bits) and the rest in INT2 with
+    fp16 scale/zero per group (the OptR accounting, "Assumptions & free
+    parameters" of the OptR page)."""
+    n16 = min(ctx, sink + recent)
+    return ((ctx - n16) * effective_bits(group) + n16 * 16.0) / ctx

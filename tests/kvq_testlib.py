@@ -27,11 +27,13 @@ class Cache:
     """One layer of one workload on the device: handle, pool, page table."""
 
     def __init__(self, wl: W.Workload, layer: int = 0, kind: str = "int2", out_rotated=False,
-                 page_table=None, num_pool_pages=None, num_heads=None, num_kv_heads=None):
+                 page_table=None, num_pool_pages=None, num_heads=None, num_kv_heads=None,
+                 q_rotated=False):
         self.wl, self.layer, self.kind = wl, layer, kind
         self.H = num_heads or wl.num_heads
         self.Hkv = num_kv_heads or wl.num_kv_heads
-        self.layout = K.make_layout(self.H, self.Hkv, wl.clip_k, wl.clip_v, 0.0, out_rotated)
+        self.layout = K.make_layout(self.H, self.Hkv, wl.clip_k, wl.clip_v, 0.0, out_rotated,
+                                    q_rotated=q_rotated)
         self.h = K.kvq_create(self.layout)
         if page_table is None:
             page_table, num_pool_pages = W.page_table(wl, layer)

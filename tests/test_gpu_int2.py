@@ -106,6 +106,39 @@ def test_out_rotated_flag(tiny):
     assert_close_attention(rot, want, "rotated output")
 
 
+def _rotate_queries(q_bits, RK, G):
+    """bf16(q R_K) per query head, the query a caller with R_K folded into its
+    projection passes under KVQ_Q_ROTATED."""
+    q = W.bf16_bits_to_float(q_bits).astype(np.float64)
+    out = np.empty_like(q)
+    for h in range(q.shape[1]):
+        out[:, h] = q[:, h] @ RK[h // G].astype(np.float64)
+    return W.to_bf16_bits(out.astype(np.float32))
+
+
+@pytest.mark.parametrize("out_rotated", [False, True])
+def test_q_rotated_flag(tiny, out_rotated):
+    """KVQ_Q_ROTATED: the caller passes q R_K; decode skips the query rotation.
+    Oracle: the same pool with R_K replaced by the identity for the query."""
+    c, Kt, Vt = tiny
+    c2 = Cache(c.wl, q_rotated=True, out_rotated=out_rotated)
+    c2.append(Kt, Vt, np.zeros(Kt.shape[0]), np.arange(Kt.shape[0]))
+    assert np.array_equal(c2.pool_host(), c.pool_host())    # append ignores the flags
+    q = W.queries(c.wl, 0, 10)
+    qr = _rotate_queries(q, c.R[0], 4)
+    got = c2.decode(qr, [777], 3)
+    R_id = c.R.copy()
+    R_id[0] = np.eye(128, dtype=np.float32)
+    want = oracle.decode_pairs("int2", c2.pool_host(), c2.npool, 4, 1, qr, c2.pt_np, [777],
+                               [[0, h] for h in range(4)], R=R_id, out_rotated=out_rotated)
+    assert_close_attention(got[0], want, f"q rotated, out_rotated={out_rotated}")
+    # against the unfolded path: only the bf16 rounding of q R_K differs
+    plain = c.decode(q, [777], 3)[0]
+    if out_rotated:
+        plain = plain @ c.R[1, 0].astype(np.float64)
+    assert np.abs(got[0] - plain).max() <= 2e-2 * np.abs(plain).max()
+
+
 @pytest.mark.parametrize("G", [1, 2])
 def test_gqa_group_sizes(G):
     wl = W.WORKLOADS["tiny_1k"]

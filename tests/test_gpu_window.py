@@ -11,6 +11,7 @@ Tolerance: 1e-3 relative L2 and 5e-3 max-abs per output vector.
 """
 import numpy as np
 import pytest
+import torch
 
 from kvq_testlib import (Cache, assert_close_attention, oracle_window, window_decode,
                          window_page_table, window_positions)
@@ -142,3 +143,18 @@ def test_ragged_batch_window():
     want = oracle_window(ci, cb, q, lens, pairs, sink, recent)
     assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want, "ragged")
     assert ci.status() == 0 and cb.status() == 0
+
+
+def test_window_rejects_rotated_query(tiny):
+    """The window's BF16 tokens need the plain query: KVQ_Q_ROTATED is refused."""
+    from rotated_int2_kv_kvq_gb300 import kvq as K
+    ci, cb = tiny
+    cq = Cache(ci.wl, q_rotated=True)
+    out = torch.empty((1, 4, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.kvq_workspace_bytes(cq.h, 1, 2), dtype=torch.uint8, device="cuda")
+    q = torch.zeros((1, 4, 128), dtype=torch.int16, device="cuda")
+    sl = torch.tensor([100], dtype=torch.int32, device="cuda")
+    with pytest.raises(K.KvqError) as e:
+        K.kvq_decode_window(cq.h, cq.pool, cq.npool, cb.pool, cb.npool, cb.pt, q, cq.pt, sl, 64,
+                            256, out, ws, 2)
+    assert e.value.code == K.KVQ_EINVAL

@@ -52,3 +52,14 @@ def test_rotations_deterministic():
     wl = W.WORKLOADS["tiny_1k"]
     assert np.array_equal(W.rotations(wl), W.rotations(wl))
     assert not np.array_equal(W.rotations(wl, 0), W.rotations(wl, 1))
+
+
+def test_effective_bits_match_the_pages_accounting():
+    """INT2 with fp16 scale/zero per 128-element group is 2 + 32/128 = 2.25
+    bits; keeping 64 sink and 256 recent tokens in BF16 brings a 64K context to
+    the 2.32 bits the OptR page prints ("Assumptions & free parameters")."""
+    assert W.effective_bits(128) == 2.25
+    assert round(W.effective_bits_window(65536, 64, 256), 2) == 2.32
+    assert W.effective_bits_window(320, 64, 256) == 16.0        # all of it in the window
+    assert W.effective_bits_window(100, 0, 0) == 2.25
+    assert abs(W.effective_bits_window(32768, 64, 256) - (32448 * 2.25 + 320 * 16) / 32768) < 1e-12
