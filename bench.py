@@ -502,10 +502,152 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# The 36-layer stack: one decode step = every layer appends one token per
+# sequence and decodes, captured as one CUDA graph
+# ---------------------------------------------------------------------------
+
+FULL_STACK_METRIC = "decode steps/s of a 36-layer stack (append + INT2 decode per layer)"
+
+
+def run_full_stack(args):
+    import torch
+
+    from rotated_int2_kv_kvq_gb300 import kvq as K
+    from rotated_int2_kv_kvq_gb300.pipeline import DecodeStepGraph, LayerCache
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    K.load_library()
+    wl = W.WORKLOADS["full_stack_36l"]
+    B, H, Hkv, L, P, S = (wl.batch, wl.num_heads, wl.num_kv_heads, wl.layers, wl.prefill,
+                          wl.decode_steps)
+    dev16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+    t_build = time.perf_counter()
+    layers = []
+    K_tab = torch.empty((S, L, B, Hkv, 128), dtype=torch.int16, device="cuda")
+    V_tab = torch.empty_like(K_tab)
+    q_tab = torch.empty((S, L, B, H, 128), dtype=torch.int16, device="cuda")
+    for l in range(L):
+        h = K.kvq_create(K.make_layout(H, Hkv, wl.clip_k, wl.clip_v))
+        K.kvq_set_rotation(h, torch.from_numpy(W.rotations(wl, l)).cuda(),
+                           torch.from_numpy(W.key_mean(wl, l)).cuda())
+        pt_np, npool = W.page_table(wl, l)
+        pool = torch.zeros(npool * K.kvq_page_bytes(h), dtype=torch.uint8, device="cuda")
+        pt = i32(pt_np)
+        Ks = W.tokens_many(wl, l, range(B), 0, 0, P + S)
+        Vs = W.tokens_many(wl, l, range(B), 1, 0, P + S)
+        for b in range(B):
+            K.kvq_append(h, pool, npool, dev16(Ks[b][:P]), dev16(Vs[b][:P]), i32(np.full(P, b)),
+                         i32(np.arange(P)), pt)
+        K_tab[:, l] = dev16(np.stack([Ks[b][P:] for b in range(B)], axis=1))
+        V_tab[:, l] = dev16(np.stack([Vs[b][P:] for b in range(B)], axis=1))
+        q_tab[:, l] = dev16(np.stack([W.queries(wl, l, st) for st in range(S)]))
+        layers.append(LayerCache(h, pool, npool, pt))
+    lens_tab = i32(np.stack([np.full(B, P + st + 1) for st in range(S)]))
+    pos_tab = i32(np.stack([np.full(B, P + st) for st in range(S)]))
+    torch.cuda.synchronize()
+    t_build = time.perf_counter() - t_build
+
+    def make(fused):
+        g = DecodeStepGraph(layers, B, H, Hkv, fused=fused)
+        g.load(K_tab[0], V_tab[0], q_tab[0], lens_tab[0], pos_tab[0])
+        return g
+
+    stream = torch.cuda.current_stream()
+
+    def timed(g, steps, warmup, graph=True):
+        """Step i uses the inputs of decode step i mod S (positions P + i mod S)."""
+        def one(i):
+            s = i % S
+            g.load(K_tab[s], V_tab[s], q_tab[s], lens_tab[s], pos_tab[s])
+            if graph:
+                g.replay()
+            else:
+                g.run()
+
+        for i in range(warmup):
+            one(i)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            one(warmup + i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1), dist)
+
+    steps = min(args.steps, 1000)
+    fused_g = make(True)
+    fused_g.capture()
+    clocks = Clocks(local)
+    clocks.start()
+    ms = timed(fused_g, steps, args.warmup)
+    extra, t_extra = 0, time.time()
+    while clocks.proc is not None and clocks.samples() < 3 and time.time() - t_extra < 10.0:
+        for _ in range(20):
+            fused_g.replay()
+        torch.cuda.synchronize()
+        extra += 20
+    clk = clocks.stop()
+    if clk is not None:
+        clk["window"] = "warm-up + timed steps" + (f" + {extra} untimed steps" if extra else "")
+    n_eager = max(3, steps // 4)
+    eager_ms = timed(fused_g, n_eager, 3, graph=False) / n_eager
+    unfused_g = make(False)
+    unfused_g.capture()
+    unfused_ms = timed(unfused_g, steps, args.warmup) / steps
+    status = [K.kvq_get_status(c.h) for c in layers]
+    assert not any(status), f"device status bits set: {status}"
+
+    ms_step = ms / steps
+    # algorithmic INT2 cache bytes per step at the mean context of the S steps
+    mean_ctx = P + (S + 1) / 2.0
+    cache_bytes = L * B * Hkv * mean_ctx * W.cache_bytes_per_token_head("int2")
+    peak, peak_kind = measured_peaks()
+    line = {
+        "metric": FULL_STACK_METRIC, "value": world * steps / (ms * 1e-3), "unit": "steps/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int2 codes, fp16 mma, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": wl.name, "layers": L, "batch": B, "heads": H, "kv_heads": Hkv,
+                   "prefill": P, "ctx": f"{P + 1}..{P + S}", "splits": fused_g.splits,
+                   "l2": f"inputs larger than L2: {cache_bytes / 1e9:.2f} GB of INT2 cache "
+                         f"per step over {L} pools, no flush",
+                   "cache_build_s": round(t_build, 1)},
+        "per_layer_us": ms_step * 1e3 / L,
+        "cache_gbs": cache_bytes / (ms_step * 1e-3) / 1e9,
+        "pct_of_hbm_peak": 100.0 * cache_bytes / (ms_step * 1e-3) / 1e9 / peak,
+        "peak_kind": peak_kind,
+        "launches_per_step": 3 * L,
+        "graph": True,
+        "eager_ms_per_step": eager_ms,
+        "unfused_graph_ms_per_step": unfused_ms,
+        "clocks": clk,
+        "gpu_launches": 3 * L * steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "full_stack_36l":
+        run_full_stack(args)
     else:
         run_ours(args)
 

@@ -232,6 +232,25 @@ int kvq_decode(kvq_handle* h, const void* pool, int num_pool_pages,
                const int32_t* seq_lens, int batch, float* out,
                void* workspace, size_t ws_bytes, int num_splits, void* stream);
 
+/* ---- append and decode in one call ---------------------------------------------
+ * The usual decode step: every sequence b with seq_lens[b] >= 1 gets one new
+ * token, at position seq_lens[b] - 1, then attends over [0, seq_lens[b]).
+ * Equal, byte for byte in the pool and bit for bit in out, to
+ *     kvq_append(K_new[b], V_new[b] at (b, seq_lens[b] - 1) for each such b)
+ *     kvq_decode(...same arguments...)
+ * but the append and the query rotation run in one kernel, so a step is three
+ * kernel launches instead of four.
+ *   K_new, V_new : device bf16 [batch][Hkv][D], 4-byte aligned.
+ *   pool         : written (the new tokens' slots) and read.
+ *   other arguments, errors and status bits as for kvq_append / kvq_decode
+ *   (a sequence whose new position has no valid page sets
+ *   KVQ_STATUS_BAD_PAGE; its token is not stored). */
+int kvq_append_decode(kvq_handle* h, void* pool, int num_pool_pages,
+                      const uint16_t* K_new, const uint16_t* V_new, const uint16_t* q,
+                      const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                      int batch, float* out, void* workspace, size_t ws_bytes,
+                      int num_splits, void* stream);
+
 /* ---- decode with a BF16 sink + recent window ----------------------------------
  * The OptR setting ("Assumptions & free parameters" of the OptR page: a BF16
  * window of 64 sink and 256 recent tokens beside the INT2 cache).  For every

@@ -93,6 +93,75 @@ struct QprepSmem {
   uint64_t bar;
 };
 
+// Second half of the query preparation, shared by qprep_kernel and
+// step_prep_kernel (128 threads, called by all of them once qr is complete):
+// per-head sum, max|.| and q.mu, the logit constants, and the B fragments.
+__device__ __forceinline__ void qprep_tail(const DecodeArgs& a, float (&qs)[kMaxG][kDim],
+                                           float (&qr)[kMaxG][kDim], int (&e_sm)[kMaxG],
+                                           const float* __restrict__ mu, float log2_scale, int b,
+                                           int kv) {
+  const int i = threadIdx.x, G = a.G;
+  // per-vector sum and max|.|: warp w handles vector w
+  {
+    const int w = i >> 5, lane = i & 31;
+    float s = 0.0f, m = 0.0f, qm = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float x = qr[w][lane + 32 * k];
+      s += x;
+      m = fmaxf(m, fabsf(x));
+      qm = fmaf(qs[w][lane + 32 * k], mu[static_cast<size_t>(kv) * kDim + lane + 32 * k], qm);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      s += __shfl_xor_sync(0xffffffffu, s, off);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      qm += __shfl_xor_sync(0xffffffffu, qm, off);
+    }
+    if (lane == 0) {
+      int e = 0;
+      if (m > 0.0f && m < INFINITY) {
+        int E;
+        frexpf(m, &E);           // m = f * 2^E, f in [0.5, 1)
+        e = 14 - E;              // m * 2^e in [2^13, 2^14)
+      }
+      e_sm[w] = e;
+      float* meta = const_cast<float*>(a.qmeta) + (static_cast<size_t>(b) * a.Hkv + kv) * kQMeta;
+      meta[2 * w] = (w < G) ? log2_scale * ldexpf(1.0f, 16 - e) : 0.0f;
+      meta[2 * w + 1] = (w < G) ? log2_scale * s : 0.0f;
+      meta[8 + w] = (w < G) ? log2_scale * qm : 0.0f;
+    }
+  }
+  __syncthreads();
+  // B fragments: 32 lanes x 16 registers; thread i writes 4 registers of lane i/4
+  {
+    const int L = i >> 2, quad = i & 3;
+    const int g = L >> 2, t = L & 3, head = g >> 1, part = g & 1;
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = 4 * quad + k;
+      const int w = r >> 1, which = r & 1;
+      const int row = 16 * w + 2 * t + 8 * which;
+      float x2[2] = {0.0f, 0.0f};
+      if (head < G) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          // x * 2 for even k-blocks (codes enter as c * 2^-17), x / 2 for odd
+          // ones (c * 2^-15): every product is c * q * 2^(e - 16)
+          const float x = ldexpf(qr[head][row + u], e_sm[head] + ((w & 1) ? -1 : 1));
+          const __half hi = __float2half_rn(x);
+          x2[u] = part ? (x - __half2float(hi)) * 2048.0f : __half2float(hi);
+        }
+      }
+      out[k] = pack_half2(x2[0], x2[1]);
+    }
+    uint32_t* dst = const_cast<uint32_t*>(a.qfrag) +
+                    ((static_cast<size_t>(b) * a.Hkv + kv) * 32 + L) * 16 + 4 * quad;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
 // One CTA per (sequence, KV head); thread i computes element i of the G
 // rotated query vectors.
 __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* __restrict__ RK,
@@ -142,65 +211,169 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
     for (int h = 0; h < kMaxG; ++h) sm.qr[h][i] = sm.qs[h][i];
   }
   __syncthreads();
-  // per-vector sum and max|.|: warp w handles vector w
+  qprep_tail(a, sm.qs, sm.qr, sm.e, mu, log2_scale, b, kv);
+}
+
+// ---------------------------------------------------------------------------
+// Append + query preparation in one kernel (kvq_append_decode): CTA (b, kv)
+// quantises sequence b's new token (position seq_lens[b] - 1) for KV head kv
+// into its page record, with exactly the fp32 operation sequence of the append
+// kernel (centre, fmaf chain over j = 0..127 in order, max/min, clip, fp16
+// scale/zero, rint codes), and then prepares the rotated query like
+// qprep_kernel.  One pass over j serves all chains: the key and value
+// rotations and the G query rotations.  R_K and R_V are bulk-copied before
+// the kernel waits for its predecessor; the token, q and the tables are read,
+// and the pool written, only after that wait.
+// ---------------------------------------------------------------------------
+struct StepSmem {
+  float RK[kDim * kDim];
+  float RV[kDim * kDim];
+  float qs[kMaxG][kDim];
+  float qr[kMaxG][kDim];
+  float x[2][kDim];          // centred key, value
+  float red[2][2][4];        // [K|V][max|min][warp]
+  uint8_t codes[2][kDim];
+  int e[kMaxG];
+  uint64_t bar;
+};
+
+__global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs st) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  StepSmem& sm = *reinterpret_cast<StepSmem*>(smem_raw);
+  const int b = blockIdx.x, kv = blockIdx.y, i = threadIdx.x;
+  const int warp = i >> 5, lane = i & 31;
+  const int G = a.G;
+  griddep_launch_dependents();
+  const uint32_t bar = smem_u32(&sm.bar);
+  if (i == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, 2 * kDim * kDim * 4);
+    bulk_g2s(smem_u32(sm.RK), st.RK + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
+    bulk_g2s(smem_u32(sm.RV), st.RV + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
+  }
+  __syncthreads();
+  griddep_wait();      // token, q and tables may come from preceding kernels
+
+  // the record slot of the new token, or none
+  const int seq_len = a.seq_lens[b];
+  const int p = seq_len - 1;
+  uint8_t* rec = nullptr;
+  if (seq_len > a.max_pages * kPage) {
+    if (i == 0 && kv == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
+  } else if (p >= 0) {
+    const int page = a.page_table[static_cast<size_t>(b) * a.max_pages + p / kPage];
+    if (page >= 0 && page < a.num_pool_pages)
+      rec = st.pool + (static_cast<size_t>(page) * a.Hkv + kv) * kInt2Rec;
+    else if (i == 0)
+      atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+  }
   {
-    const int w = i >> 5, lane = i & 31;
-    float s = 0.0f, m = 0.0f, qm = 0.0f;
+    const size_t src = (static_cast<size_t>(b) * a.Hkv + kv) * kDim + i;
+    const float k = __uint_as_float(static_cast<uint32_t>(st.K[src]) << 16);
+    sm.x[0][i] = __fsub_rn(k, st.mu[static_cast<size_t>(kv) * kDim + i]);
+    sm.x[1][i] = __uint_as_float(static_cast<uint32_t>(st.V[src]) << 16);
+  }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float x = sm.qr[w][lane + 32 * k];
-      s += x;
-      m = fmaxf(m, fabsf(x));
-      qm = fmaf(sm.qs[w][lane + 32 * k], mu[static_cast<size_t>(kv) * kDim + lane + 32 * k], qm);
+  for (int h = 0; h < kMaxG; ++h) {
+    float x = 0.0f;
+    if (h < G) {
+      const uint16_t bits = a.q[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + i];
+      x = __uint_as_float(static_cast<uint32_t>(bits) << 16);
     }
+    sm.qs[h][i] = x;
+  }
+  const bool ok = mbar_wait_bounded(bar, 0);
+  if (__syncthreads_or(!ok)) {
+    if (i == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+    return;
+  }
+  // r_i = fmaf chains over j = 0..127 (keys, values, G queries)
+  float rk = 0.0f, rv = 0.0f;
+  float acc[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+  for (int j = 0; j < kDim; ++j) {
+    const float ak = sm.RK[j * kDim + i];
+    rk = fmaf(sm.x[0][j], ak, rk);
+    rv = fmaf(sm.x[1][j], sm.RV[j * kDim + i], rv);
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) acc[h] = fmaf(sm.qs[h][j], ak, acc[h]);
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) sm.qr[h][i] = st.q_rotated ? sm.qs[h][i] : acc[h];
+
+  // max / min of the rotated key and value over the whole vector
+  {
+    float mk = rk, nk = rk, mv = rv, nv = rv;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      s += __shfl_xor_sync(0xffffffffu, s, off);
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      qm += __shfl_xor_sync(0xffffffffu, qm, off);
+      mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
+      nk = fminf(nk, __shfl_xor_sync(0xffffffffu, nk, off));
+      mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+      nv = fminf(nv, __shfl_xor_sync(0xffffffffu, nv, off));
     }
     if (lane == 0) {
-      int e = 0;
-      if (m > 0.0f && m < INFINITY) {
-        int E;
-        frexpf(m, &E);           // m = f * 2^E, f in [0.5, 1)
-        e = 14 - E;              // m * 2^e in [2^13, 2^14)
-      }
-      sm.e[w] = e;
-      float* meta = const_cast<float*>(a.qmeta) + (static_cast<size_t>(b) * a.Hkv + kv) * kQMeta;
-      meta[2 * w] = (w < G) ? log2_scale * ldexpf(1.0f, 16 - e) : 0.0f;
-      meta[2 * w + 1] = (w < G) ? log2_scale * s : 0.0f;
-      meta[8 + w] = (w < G) ? log2_scale * qm : 0.0f;
+      sm.red[0][0][warp] = mk;
+      sm.red[0][1][warp] = nk;
+      sm.red[1][0][warp] = mv;
+      sm.red[1][1][warp] = nv;
     }
   }
   __syncthreads();
-  // B fragments: 32 lanes x 16 registers; thread i writes 4 registers of lane i/4
-  {
-    const int L = i >> 2, quad = i & 3;
-    const int g = L >> 2, t = L & 3, head = g >> 1, part = g & 1;
-    uint32_t out[4];
+  uint32_t szw[2];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int r = 4 * quad + k;
-      const int w = r >> 1, which = r & 1;
-      const int row = 16 * w + 2 * t + 8 * which;
-      float x2[2] = {0.0f, 0.0f};
-      if (head < G) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          // x * 2 for even k-blocks (codes enter as c * 2^-17), x / 2 for odd
-          // ones (c * 2^-15): every product is c * q * 2^(e - 16)
-          const float x = ldexpf(sm.qr[head][row + u], sm.e[head] + ((w & 1) ? -1 : 1));
-          const __half hi = __float2half_rn(x);
-          x2[u] = part ? (x - __half2float(hi)) * 2048.0f : __half2float(hi);
-        }
-      }
-      out[k] = pack_half2(x2[0], x2[1]);
+  for (int which = 0; which < 2; ++which) {
+    const float mx = fmaxf(fmaxf(sm.red[which][0][0], sm.red[which][0][1]),
+                           fmaxf(sm.red[which][0][2], sm.red[which][0][3]));
+    const float mn = fminf(fminf(sm.red[which][1][0], sm.red[which][1][1]),
+                           fminf(sm.red[which][1][2], sm.red[which][1][3]));
+    const float clip = which ? st.clip_v : st.clip_k;
+    const float mxc = __fmul_rn(clip, mx);
+    const float mnc = __fmul_rn(clip, mn);
+    const float s32 = __fdiv_rn(__fsub_rn(mxc, mnc), 3.0f);
+    const __half sh = __float2half_rn(s32);
+    const __half zh = __float2half_rn(mnc);
+    const float sc = __half2float(sh), z = __half2float(zh);
+    uint32_t code = 0;
+    if (sc != 0.0f) {
+      const float t = __fdiv_rn(__fsub_rn(which ? rv : rk, z), sc);
+      code = static_cast<uint32_t>(fminf(fmaxf(rintf(t), 0.0f), 3.0f));
     }
-    uint32_t* dst = const_cast<uint32_t*>(a.qfrag) +
-                    ((static_cast<size_t>(b) * a.Hkv + kv) * 32 + L) * 16 + 4 * quad;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+    sm.codes[which][i] = static_cast<uint8_t>(code);
+    szw[which] = static_cast<uint32_t>(__half_as_ushort(sh)) |
+                 (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
   }
+  __syncthreads();
+  // scatter into the page record (layout in include/kvq.h)
+  if (rec != nullptr) {
+    const int tau = p % kPage;
+    if (i < 8) {
+      // keys: word h of lane group t of row tau & 7
+      const int t = i & 3, h = i >> 2;
+      uint32_t wv = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const int d = 16 * w + 2 * t + 8 * h;
+        wv |= static_cast<uint32_t>(sm.codes[0][d]) << (2 * w);
+        wv |= static_cast<uint32_t>(sm.codes[0][d + 1]) << (16 + 2 * w);
+      }
+      *reinterpret_cast<uint32_t*>(rec + 16 * (4 * (tau & 7) + t) + 8 * (tau >> 3) + 4 * h) = wv;
+    } else if (i < 24) {
+      // values: the token's 16-bit half of word (2 th + dh) of lane 4 g + t
+      const int k = i - 8, g = k >> 1, dh = k & 1;
+      uint32_t hv = 0;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) hv |= static_cast<uint32_t>(sm.codes[1][16 * m + g + 8 * dh]) << (2 * m);
+      const int t = (tau & 7) >> 1, e = tau & 1, th = tau >> 3;
+      *reinterpret_cast<uint16_t*>(rec + 512 + 16 * (4 * g + t) + 4 * (2 * th + dh) + 2 * e) =
+          static_cast<uint16_t>(hv);
+    } else if (i < 26) {
+      const int which = i - 24;
+      *reinterpret_cast<uint32_t*>(rec + 1024 + 16 * (tau & 7) + 8 * which + 4 * (tau >> 3)) =
+          which ? szw[1] : szw[0];
+    }
+  }
+  qprep_tail(a, sm.qs, sm.qr, sm.e, st.mu, a.log2_scale, b, kv);
 }
 
 // ---------------------------------------------------------------------------
@@ -1106,6 +1279,14 @@ cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, const float* mu, 
   dim3 grid(a.batch, a.Hkv);
   e = launch_dependent(qprep_kernel, grid, dim3(128), sizeof(QprepSmem), st, a, RK, mu,
                        sm_scale * kLog2e);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_step_prep(const DecodeArgs& a, const StepArgs& sa, cudaStream_t st) {
+  cudaError_t e = set_smem_attr<StepSmem>(step_prep_kernel);
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(step_prep_kernel, dim3(a.batch, a.Hkv), dim3(128), sizeof(StepSmem), st,
+                       a, sa);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

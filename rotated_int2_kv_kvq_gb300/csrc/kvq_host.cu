@@ -153,7 +153,8 @@ struct Window {
 int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages,
                   const uint16_t* q, const int32_t* page_table, int max_pages,
                   const int32_t* seq_lens, int batch, float* out, void* workspace,
-                  size_t ws_bytes, int num_splits, void* stream, const Window& win = Window()) {
+                  size_t ws_bytes, int num_splits, void* stream, const Window& win = Window(),
+                  kvq::StepArgs* step = nullptr) {
   int rc = check_decode_args(h, pool, num_pool_pages, q, page_table, max_pages, seq_lens, batch,
                              out, workspace, num_splits);
   if (rc != KVQ_OK) return rc;
@@ -204,7 +205,17 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
   if (int2) {
     const float* mu = h->bank + static_cast<size_t>(3) * a.Hkv * kDim * kDim;
     const bool q_rotated = (h->L.flags & KVQ_Q_ROTATED) != 0;
-    e = kvq::launch_qprep(a, q_rotated ? nullptr : h->bank, mu, h->sm_scale, st);
+    if (step) {
+      step->RK = h->bank;
+      step->RV = h->bank + static_cast<size_t>(a.Hkv) * kDim * kDim;
+      step->mu = mu;
+      step->clip_k = h->L.clip_k;
+      step->clip_v = h->L.clip_v;
+      step->q_rotated = q_rotated ? 1 : 0;
+      e = kvq::launch_step_prep(a, *step, st);
+    } else {
+      e = kvq::launch_qprep(a, q_rotated ? nullptr : h->bank, mu, h->sm_scale, st);
+    }
     if (e != cudaSuccess) return KVQ_ECUDA;
   }
   int slot;
@@ -375,6 +386,21 @@ int kvq_decode_window(kvq_handle* h, const void* pool, int num_pool_pages,
   win.on = true;
   return decode_common(h, true, pool, num_pool_pages, q, page_table, max_pages, seq_lens, batch,
                        out, workspace, ws_bytes, num_splits, stream, win);
+}
+
+int kvq_append_decode(kvq_handle* h, void* pool, int num_pool_pages, const uint16_t* K_new,
+                      const uint16_t* V_new, const uint16_t* q, const int32_t* page_table,
+                      int max_pages, const int32_t* seq_lens, int batch, float* out,
+                      void* workspace, size_t ws_bytes, int num_splits, void* stream) {
+  if (!K_new || !V_new) return KVQ_EINVAL;
+  if (reinterpret_cast<uintptr_t>(K_new) % 4 || reinterpret_cast<uintptr_t>(V_new) % 4)
+    return KVQ_EINVAL;
+  kvq::StepArgs step;
+  step.pool = static_cast<uint8_t*>(pool);
+  step.K = K_new;
+  step.V = V_new;
+  return decode_common(h, true, pool, num_pool_pages, q, page_table, max_pages, seq_lens, batch,
+                       out, workspace, ws_bytes, num_splits, stream, Window(), &step);
 }
 
 int kvq_bf16_decode(kvq_handle* h, const void* pool, int num_pool_pages, const uint16_t* q,

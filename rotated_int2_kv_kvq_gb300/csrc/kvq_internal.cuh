@@ -75,11 +75,24 @@ struct AppendArgs {
   uint32_t* status;
 };
 
+// The append half of kvq_append_decode: one new token per sequence.
+struct StepArgs {
+  uint8_t* pool;
+  const uint16_t* K;         // [B][Hkv][D] bf16, the token at position seq_lens[b] - 1
+  const uint16_t* V;
+  const float* RK;           // [Hkv][D][D]
+  const float* RV;           // [Hkv][D][D]
+  const float* mu;           // [Hkv][D]
+  float clip_k, clip_v;
+  int q_rotated;             // 1: q is already q R_K
+};
+
 // ---- launchers (defined in the .cu files) --------------------------------
 cudaError_t launch_append_int2(const AppendArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_append_bf16(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, const float* mu, float sm_scale,
                          cudaStream_t st);
+cudaError_t launch_step_prep(const DecodeArgs& a, const StepArgs& sa, cudaStream_t st);
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st);

@@ -42,6 +42,7 @@ SIGNATURES = {
     "kvq_bf16_workspace_bytes": ([_P, _I, _I], _SZ),
     "kvq_bf16_decode": ([_P, _P, _I, _P, _P, _I, _P, _I, _P, _P, _SZ, _I, _P], _I),
     "kvq_decode_static": ([_P, _P, _I, _P, _P, _I, _P, _I, _P, _I, _P], _I),
+    "kvq_append_decode": ([_P, _P, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _SZ, _I, _P], _I),
     "kvq_decode_window": ([_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _SZ, _I,
                            _P], _I),
     "kvq_get_status": ([_P, _P, _P], _I),
@@ -236,6 +237,19 @@ def kvq_decode_static(h, pool, num_pool_pages, q, page_table, seq_lens, out, num
         h.ptr, _ptr(pool, _U8, "pool"), int(num_pool_pages), _ptr(q, _BF16, "q"),
         _ptr(page_table, _I32, "page_table"), max_pages, _ptr(seq_lens, _I32, "seq_lens"),
         batch, _ptr(out, _F32, "out"), int(num_splits), _stream(stream)))
+
+
+def kvq_append_decode(h, pool, num_pool_pages, K_new, V_new, q, page_table, seq_lens, out,
+                      workspace, num_splits=0, stream=None):
+    """One decode step: append K_new[b], V_new[b] ([B, Hkv, 128] bf16) at
+    position seq_lens[b] - 1 of every sequence, then decode (as kvq_decode)."""
+    batch, max_pages = int(page_table.shape[0]), int(page_table.shape[1])
+    _check("kvq_append_decode", load_library().kvq_append_decode(
+        h.ptr, _ptr(pool, _U8, "pool"), int(num_pool_pages), _ptr(K_new, _BF16, "K_new"),
+        _ptr(V_new, _BF16, "V_new"), _ptr(q, _BF16, "q"), _ptr(page_table, _I32, "page_table"),
+        max_pages, _ptr(seq_lens, _I32, "seq_lens"), batch, _ptr(out, _F32, "out"),
+        _ptr(workspace, _U8, "workspace"), int(workspace.numel()), int(num_splits),
+        _stream(stream)))
 
 
 def kvq_decode_window(h, pool, num_pool_pages, bf16_pool, bf16_num_pool_pages, bf16_page_table,
