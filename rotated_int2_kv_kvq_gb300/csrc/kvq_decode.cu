@@ -14,15 +14,16 @@
 // How the INT2 kernel maps onto sm_103a
 // -------------------------------------
 // One CTA = 8 warps = one (split, group of HPC KV heads, sequence); warp w
-// serves KV head w / (8/HPC) of the group.  The pool stores the records of all
-// KV heads of a page next to each other, so one 1-D TMA bulk copy
-// (cp.async.bulk, mbarrier completion) brings a page for all the CTA's heads.
-// A stage holds 2 * (8/HPC) pages; every warp takes two pages from each stage
-// (two independent tensor-core chains in flight).  The last warp to finish a
-// stage (a shared-memory arrival counter) refills it, so no warp waits for a
-// free slot.  A page record (1152 B per head) holds the 16 tokens' codes in
-// tensor-core fragment order, so each lane takes its share of a page with one
-// 16-byte shared load and hands it to mma.sync.m16n8k16 without shuffling:
+// serves KV head w / (8/HPC) of the group and takes every (8/HPC)-th page of
+// the split.  Each warp streams its own pages through its own ring of stages:
+// lane 0 issues 1-D TMA bulk copies (cp.async.bulk, mbarrier completion) of the
+// head's 1152-byte records, two pages per stage (two independent tensor-core
+// chains in flight), and refills a stage as soon as the warp has read it.  No
+// stage is shared between warps, so a warp that runs ahead never waits for a
+// slower one (sharing one copy of a page between the CTA's heads made every
+// warp keep the pace of the slowest and cost 6 %).  A page record holds the 16
+// tokens' codes in tensor-core fragment order, so each lane takes its share of
+// a page with one 16-byte shared load and hands it to mma.sync.m16n8k16 without shuffling:
 //   scores  S[token][col] = Kcode[token][dim] . B[dim][col]     (M = 16 tokens)
 //   values  O^T[dim][col] += Vcode^T[dim][token] . P[token][col] (M = 16 dims)
 // with col = 2*head + {hi, lo}: each operand that is not a code is split into an
@@ -529,44 +530,40 @@ __device__ __forceinline__ void process_pair(WarpState& st, const uint32_t (&qf)
 
 constexpr int kW = kInt2Warps;                 // warps per CTA
 constexpr int kNS = 4;                         // pipeline stages
-constexpr int kStageBytes = 2 * kW * kInt2Rec; // 2 pages x (8/HPC) x HPC heads
 constexpr int kMaxIds = 1024;                  // page ids staged per sub-chunk
 
+// Every warp streams its own KV head's records through its own ring: no stage
+// is shared between warps, so no warp waits for another to release a slot.
 struct Int2Smem {
-  uint8_t ring[kNS][kStageBytes];
-  uint64_t full[kNS];
-  int cnt[kNS];
+  uint8_t ring[kW][kNS][2 * kInt2Rec];
+  uint64_t full[kW][kNS];
   int ids[kMaxIds];
   float o[kW][kMaxG][kDim];
   float m[kW][kMaxG];
   float l[kW][kMaxG];
 };
 
-
-// Fill stage `k` of the current sub-chunk (single thread).
-__device__ __forceinline__ void issue_stage(Int2Smem& sm, const DecodeArgs& a, int k, int slot,
-                                            int nsub, int PPS, int HPC, int hg) {
-  const uint32_t rec_bytes = static_cast<uint32_t>(HPC) * kInt2Rec;
-  uint32_t bytes = 0;
-  for (int u = 0; u < PPS; ++u) {
-    const int li = k * PPS + u;
-    if (li < nsub && sm.ids[li] >= 0) bytes += rec_bytes;
-  }
-  const uint32_t bar = smem_u32(&sm.full[slot]);
+// Fill stage k of warp `warp` (pages 2k and 2k+1 of the warp's share of the
+// sub-chunk: local page index gi + GPH * j).  Lane 0 only.
+__device__ __forceinline__ void issue_warp_stage(Int2Smem& sm, const DecodeArgs& a, int warp, int k,
+                                                 int slot, int npw, int gi, int GPH, int kv) {
+  const int j0 = 2 * k, j1 = j0 + 1;
+  const int li0 = gi + GPH * j0, li1 = gi + GPH * j1;
+  const int id0 = j0 < npw ? sm.ids[li0] : -1;
+  const int id1 = j1 < npw ? sm.ids[li1] : -1;
+  const uint32_t bytes = (id0 >= 0 ? kInt2Rec : 0) + (id1 >= 0 ? kInt2Rec : 0);
+  const uint32_t bar = smem_u32(&sm.full[warp][slot]);
   if (bytes == 0) {
     mbar_arrive(bar);
     return;
   }
   mbar_arrive_expect_tx(bar, bytes);
-  for (int u = 0; u < PPS; ++u) {
-    const int li = k * PPS + u;
-    if (li >= nsub) break;
-    const int id = sm.ids[li];
-    if (id < 0) continue;
-    bulk_g2s(smem_u32(&sm.ring[slot][u * rec_bytes]),
-             a.pool + (static_cast<size_t>(id) * a.Hkv + static_cast<size_t>(hg) * HPC) * kInt2Rec,
-             rec_bytes, bar);
-  }
+  if (id0 >= 0)
+    bulk_g2s(smem_u32(&sm.ring[warp][slot][0]),
+             a.pool + (static_cast<size_t>(id0) * a.Hkv + kv) * kInt2Rec, kInt2Rec, bar);
+  if (id1 >= 0)
+    bulk_g2s(smem_u32(&sm.ring[warp][slot][kInt2Rec]),
+             a.pool + (static_cast<size_t>(id1) * a.Hkv + kv) * kInt2Rec, kInt2Rec, bar);
 }
 
 __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
@@ -579,11 +576,8 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   const int hl = warp / GPH, gi = warp % GPH;
   const int kv = hg * HPC + hl;
 
-  if (tid == 0) {
-    for (int s = 0; s < kNS; ++s) {
-      mbar_init(smem_u32(&sm.full[s]), 1);
-      sm.cnt[s] = 0;
-    }
+  if (lane == 0) {
+    for (int s = 0; s < kNS; ++s) mbar_init(smem_u32(&sm.full[warp][s]), 1);
     fence_mbar_init();
   }
   griddep_wait();      // inputs (pool, tables, rotated queries) come from predecessors
@@ -625,7 +619,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   ws.l_run = 0.0f;
   ws.z_run = 0.0f;
 
-  int gs = 0;            // stages consumed so far (ring phase)
+  int gs = 0;            // this warp's stages consumed so far (ring phase)
   bool timed_out = false;
   for (int sub = 0; sub < npg && !timed_out; sub += kMaxIds) {
     const int nsub = min(kMaxIds, npg - sub);
@@ -638,24 +632,25 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
       ids_ok = ids_ok && ok;
     }
     const bool all_ids_ok = __syncthreads_and(ids_ok);
-    const int nst = (nsub + PPS - 1) / PPS;
-    if (tid == 0)
-      for (int k = 0; k < kNS && k < nst; ++k) issue_stage(sm, a, k, (gs + k) % kNS, nsub, PPS, HPC, hg);
+    const int npw = nsub > gi ? (nsub - gi + GPH - 1) / GPH : 0;   // this warp's pages
+    const int nst = (npw + 1) >> 1;
+    if (lane == 0)
+      for (int k = 0; k < kNS && k < nst; ++k)
+        issue_warp_stage(sm, a, warp, k, (gs + k) % kNS, npw, gi, GPH, kv);
 
     for (int k = 0; k < nst; ++k) {
       const int slot = (gs + k) % kNS;
-      if (!mbar_wait_bounded(smem_u32(&sm.full[slot]), ((gs + k) / kNS) & 1)) {
+      if (!mbar_wait_bounded(smem_u32(&sm.full[warp][slot]), ((gs + k) / kNS) & 1)) {
         if (lane == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
         timed_out = true;
         break;
       }
-      const int ua = k * PPS + gi, ub = ua + GPH;
-      // both pages of every warp present, valid and all their tokens in [lo, hi)
-      const bool full = all_ids_ok && (k + 1) * PPS <= nsub &&
-                        (p0 + sub + (k + 1) * PPS) * kPage <= hi &&
-                        (p0 + sub + k * PPS) * kPage >= lo;
-      const uint8_t* sta = &sm.ring[slot][(gi * HPC + hl) * kInt2Rec];
-      const uint8_t* stb = &sm.ring[slot][((GPH + gi) * HPC + hl) * kInt2Rec];
+      const int ua = gi + GPH * (2 * k), ub = ua + GPH;
+      // both pages present, valid and all their tokens in [lo, hi)
+      const bool full = all_ids_ok && 2 * k + 1 < npw && (p0 + sub + ub + 1) * kPage <= hi &&
+                        (p0 + sub + ua) * kPage >= lo;
+      const uint8_t* sta = &sm.ring[warp][slot][0];
+      const uint8_t* stb = &sm.ring[warp][slot][kInt2Rec];
       const uint4 kwa = *reinterpret_cast<const uint4*>(sta + 16 * lane);
       const uint4 vwa = *reinterpret_cast<const uint4*>(sta + 512 + 16 * lane);
       const uint4 mta = *reinterpret_cast<const uint4*>(sta + 1024 + 16 * g);
@@ -663,24 +658,16 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
       const uint4 vwb = *reinterpret_cast<const uint4*>(stb + 512 + 16 * lane);
       const uint4 mtb = *reinterpret_cast<const uint4*>(stb + 1024 + 16 * g);
       __syncwarp();
-      if (lane == 0) {
-        // release the stage; the last of the kW warps refills it
-        __threadfence_block();
-        const int prev = atomicAdd(&sm.cnt[slot], 1);
-        if (prev == kW - 1) {
-          sm.cnt[slot] = 0;
-          if (k + kNS < nst) {
-            fence_proxy_async();
-            issue_stage(sm, a, k + kNS, slot, nsub, PPS, HPC, hg);
-          }
-        }
+      if (lane == 0 && k + kNS < nst) {
+        fence_proxy_async();
+        issue_warp_stage(sm, a, warp, k + kNS, slot, npw, gi, GPH, kv);
       }
       if (full) {
         process_pair<false>(ws, qf, kappa, zeta, g, t, kwa, vwa, mta, kwb, vwb, mtb, true, true,
                             true, true);
       } else {
-        const bool oka = ua < nsub && sm.ids[ua] >= 0;
-        const bool okb = ub < nsub && sm.ids[ub] >= 0;
+        const bool oka = 2 * k < npw && sm.ids[ua] >= 0;
+        const bool okb = 2 * k + 1 < npw && sm.ids[ub] >= 0;
         const int posa = (p0 + sub + ua) * kPage, posb = (p0 + sub + ub) * kPage;
         const bool va0 = oka && posa + g >= lo && posa + g < hi;
         const bool va1 = oka && posa + g + 8 >= lo && posa + g + 8 < hi;
@@ -691,12 +678,13 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
       }
     }
     gs += nst;
-    __syncthreads();     // sm.ids is reloaded for the next sub-chunk
+    // sm.ids is reloaded for the next sub-chunk; every warp leaves together
+    timed_out = __syncthreads_or(timed_out);
   }
   if (timed_out) {
     // A wait gave up: let the copies already issued land (bounded) before the
     // CTA can exit, so no bulk copy targets freed shared memory.
-    for (int s = 0; s < kNS; ++s) mbar_wait_bounded(smem_u32(&sm.full[s]), 0);
+    for (int s = 0; s < kNS; ++s) mbar_wait_bounded(smem_u32(&sm.full[warp][s]), 0);
   }
   griddep_launch_dependents();
 
