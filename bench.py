@@ -1,9 +1,10 @@
 """Benchmark of the rotated INT2 KV-cache decode step on GB300.
 
-One step = the whole hot path for one batch: quantise-and-append one new K/V
-token per sequence (centre, rotate, clip, INT2 pack into its page) and one
-split-K INT2 decode-attention call over the paged cache (query rotation, scores,
-online softmax, P.V, log-sum-exp combine, inverse value rotation).
+One step = the whole hot path for one batch, one kvq_append_decode call:
+quantise-and-append one new K/V token per sequence (centre, rotate, clip, INT2
+pack into its page) and split-K INT2 decode attention over the paged cache
+(query rotation, scores, online softmax, P.V, log-sum-exp combine, inverse value
+rotation).  The same step as two calls (kvq_append, kvq_decode) is reported too.
 
 Workload (default): Qwen3-8B-shaped layer, batch 16, 32 query / 8 KV heads,
 head_dim 128, context 32768 per sequence in 16-token pages over a shuffled pool.
@@ -313,7 +314,13 @@ def run_ours(args):
     out = torch.empty((B, H, 128), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
+    # One decode step through the library's one-call form: append each
+    # sequence's token at position len-1, then decode (3 kernel launches).
     def step():
+        K.kvq_append_decode(h, pool, npool, kd_new, vd_new, qd, pt, seq_lens, out, ws, splits)
+
+    # The same step as two calls (append, then decode: 4 launches).
+    def step_two_calls():
         K.kvq_append(h, pool, npool, kd_new, vd_new, sid, pos, pt)
         K.kvq_decode(h, pool, npool, qd, pt, seq_lens, out, ws, splits)
 
@@ -379,8 +386,7 @@ def run_ours(args):
         qd2.copy_(q_h, non_blocking=True)
         kd2.copy_(k_h, non_blocking=True)
         vd2.copy_(v_h, non_blocking=True)
-        K.kvq_append(h, pool, npool, kd2, vd2, sid, pos, pt)
-        K.kvq_decode(h, pool, npool, qd2, pt, seq_lens, out, ws, splits)
+        K.kvq_append_decode(h, pool, npool, kd2, vd2, qd2, pt, seq_lens, out, ws, splits)
         out_h.copy_(out, non_blocking=True)
 
     e2e_ms, _ = timed(e2e_step, args.steps, max(3, args.warmup // 2))
@@ -421,14 +427,16 @@ def run_ours(args):
     qrd = dev(W.to_bf16_bits(qrot_np.astype(np.float32)))
 
     def folded_step():
-        K.kvq_append(hf, pool, npool, kd_new, vd_new, sid, pos, pt)
-        K.kvq_decode(hf, pool, npool, qrd, pt, seq_lens, out, ws, splits)
+        K.kvq_append_decode(hf, pool, npool, kd_new, vd_new, qrd, pt, seq_lens, out, ws, splits)
 
     fms, _ = timed(folded_step, args.steps, args.warmup)
+    tms, _ = timed(step_two_calls, args.steps, args.warmup)
     ums, _ = timed(step, args.steps, args.warmup)      # the default step again, back to back
     folded = {"ms_per_step": fms / args.steps, "default_ms_per_step": ums / args.steps,
               "rotation_overhead_pct": 100.0 * (ums - fms) / fms,
               "flags": "KVQ_Q_ROTATED | KVQ_OUT_ROTATED"}
+    two_calls = {"ms_per_step": tms / args.steps, "launches_per_step": 4,
+                 "calls": "kvq_append + kvq_decode"}
     assert K.kvq_get_status(hf) == 0, "device status bits set during the folded benchmark"
 
     # The OptR setting: 64 sink + 256 recent tokens kept in BF16 beside the INT2
@@ -467,7 +475,7 @@ def run_ours(args):
                          f"decode {H // Hkv} query heads over {ctx} tokens per step, "
                          f"{n_cpu} steps in {el_cpu:.1f} s"}
 
-    launches = 4 * args.steps       # append, q-rotation, split-K attention, split merge
+    launches = 3 * args.steps       # append + q-rotation, split-K attention, split merge
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -493,6 +501,7 @@ def run_ours(args):
         "bf16_comparison": bf16,
         "bf16_window": window,
         "folded_rotations": folded,
+        "two_call_step": two_calls,
         "clocks": clk,
         "gpu_launches": launches,
     }

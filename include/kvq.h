@@ -34,6 +34,14 @@
  *     caller.  The library never frees or retains it beyond the call.
  *   - `stream` is a cudaStream_t passed as void*.  NULL means the legacy default
  *     stream.  Every compute call is asynchronous on that stream.
+ *   - The decode kernels are launched as programmatic dependents of the
+ *     preceding work on the stream (CUDA programmatic dependent launch), so each
+ *     can become resident before its predecessor ends; each reads its inputs only
+ *     after waiting for that predecessor, so stream order holds for the caller's
+ *     data.  A caller kernel that follows on the stream and is itself launched
+ *     with the programmatic-serialisation attribute must execute
+ *     griddepcontrol.wait (cudaGridDependencySynchronize) before reading `out`;
+ *     ordinary launches, copies and host synchronisation need nothing.
  *   - bf16 tensors are passed as uint16_t bit patterns.
  *   - Return codes: KVQ_OK, or a KVQ_E* code below.  Argument errors are found on
  *     the host before anything is launched.  Data errors that only the device can

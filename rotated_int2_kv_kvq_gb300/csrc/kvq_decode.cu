@@ -1108,6 +1108,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(DecodeArgs a) 
   const int warp = tid >> 5, lane = tid & 31;
   const int S = a.splits, G = a.G;
   const uint32_t bar = smem_u32(&sm.bar);
+  // Let the next kernel in the stream launch now: the kernels of this library
+  // read nothing this one writes before their own griddepcontrol.wait, so the
+  // next decode step can stage its rotation matrices while this merge runs.
+  griddep_launch_dependents();
   // the matrix of the one basis change: R_V^T (INT2 part back to the plain
   // basis) or, for a rotated-basis output, R_V (window part forward)
   const bool stage = kWindow || a.rotate_out;
