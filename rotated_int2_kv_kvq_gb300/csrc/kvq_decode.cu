@@ -33,9 +33,10 @@
 // half is the fp16 number code * 2^-15 (or code * 2^-17), exactly; the powers of
 // two are folded into the query operands and removed in the value epilogue.
 //
-// Kernel chain of one decode call: qprep -> decode -> combine, each launched as
-// a programmatic dependent of the previous kernel (griddepcontrol), so each one
-// is resident and waiting when its predecessor finishes.
+// Kernel chain of one decode call: qprep (or step_prep, which also appends the
+// new token) -> decode -> combine, each launched as a programmatic dependent of
+// the previous kernel (griddepcontrol), so each one is resident and waiting when
+// its predecessor finishes.
 #include "kvq_internal.cuh"
 
 #include <math.h>

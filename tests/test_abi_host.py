@@ -54,7 +54,8 @@ def test_layout_struct_matches_header(lib):
     text = open(HEADER).read()
     for name, value in [("KVQ_OK", 0), ("KVQ_EINVAL", 1), ("KVQ_ENOSPACE", 2), ("KVQ_ECUDA", 3),
                         ("KVQ_ENOTREADY", 4), ("KVQ_INT2_RECORD_BYTES", 1152),
-                        ("KVQ_BF16_RECORD_BYTES", 8192), ("KVQ_OUT_ROTATED", 1)]:
+                        ("KVQ_BF16_RECORD_BYTES", 8192), ("KVQ_OUT_ROTATED", 1),
+                        ("KVQ_Q_ROTATED", 2)]:
         m = re.search(r"#define\s+%s\s+(\d+)" % name, text)
         assert m and int(m.group(1)) == value
 
@@ -83,3 +84,13 @@ def test_host_only_paths(lib):
     assert lib.kvq_append(None, None, 0, None, None, None, None, 1, None, 1, 1, None) == 1
     assert lib.kvq_decode(None, None, 0, None, None, 0, None, 0, None, None, 0, 0, None) == 1
     assert lib.kvq_get_status(None, None, None) == 1
+    assert lib.kvq_append_decode(None, None, 0, None, None, None, None, 0, None, 0, None, None, 0,
+                                 0, None) == 1
+    assert lib.kvq_decode_window(None, None, 0, None, 0, None, None, None, 0, None, 0, 64, 256,
+                                 None, None, 0, 0, None) == 1
+    # a layout with both folding flags is valid; an unknown flag is not
+    both = kvq.make_layout(32, 8, out_rotated=True, q_rotated=True)
+    assert both.flags == kvq.KVQ_OUT_ROTATED | kvq.KVQ_Q_ROTATED
+    bad = kvq.make_layout(32, 8)
+    bad.flags = 4
+    assert lib.kvq_create(ctypes.byref(bad), ctypes.byref(out)) == kvq.KVQ_EINVAL
