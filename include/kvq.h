@@ -337,6 +337,61 @@ int kvq_decode_static(kvq_handle* h, const void* pool, int num_pool_pages,
                       const int32_t* seq_lens, int batch, float* out, int num_splits,
                       void* stream);
 
+/* ---- OptR rotation calibration (off the decode path) ------------------------
+ * Learns, per KV head, the rotations the cache uses: R = R0 exp(A - A^T), the
+ * orthogonal correction of a base rotation R0 ("What carries the argument",
+ * mechanism (1)), with Adam ("Assumptions & free parameters": 80 steps,
+ * lambda_K = 1) through the whole quantised path with a straight-through
+ * estimator for the rounding (mechanism (3)); keys first, then values:
+ *   keys:   L_K = [ sum_h KL(p_h || p~_h) + lambda_K |sum_h (dp_h V) W_h^T|^2 ] / Nq
+ *   values: L_V = [ |sum_h (p~_h dV) W_h^T|^2 ] / Nq,   p~ fixed at the calibrated keys,
+ * summed over the last Nq query positions of a causal calibration chunk
+ * (the referee report's Eqs. (14), (16); "Gradients computed on the final 64
+ * query positions").  p is the attention with the exact keys, p~ with the keys
+ * centred by mu, rotated, quantised by this library's INT2 quantiser (fp16
+ * scale and zero), dequantised and rotated back; dV likewise for values.  The
+ * straight-through backward replaces the rounding by the identity and
+ * differentiates the clipping exactly.  A starts at 0; Adam beta1 0.9,
+ * beta2 0.999, eps 1e-8 (readings: the pages give none of these).
+ *   K, V       : device bf16 [Hkv][T][D] calibration keys / values (positions 0..T-1).
+ *   Q          : device bf16 [Hkv][Nq][G][D] queries at positions T-Nq .. T-1.
+ *   W_O        : device fp32 [Hkv][Dm][G*D], the KV head's slice of the output
+ *                projection (head h's output o_h contributes o_h W_O[:, hD:(h+1)D]^T).
+ *   R0         : device fp32 [2][Hkv][D][D] base rotations (keys, values).
+ *   mu         : device fp32 [Hkv][D] key means.
+ *   lr         : Adam step size (1e-3 is this library's default reading).
+ *   sm_scale   : <= 0 selects 1/sqrt(D).
+ *   R_out      : device fp32 [2][Hkv][D][D], the calibrated rotations, ready for
+ *                kvq_set_rotation.
+ *   history    : device fp32 [2][steps + 1][Hkv]: the loss before each Adam step
+ *                and after the last one (keys, then values).
+ *   workspace  : device, >= kvq_optr_workspace_bytes(...) bytes, 256-byte aligned.
+ * The call returns when the calibration has finished (it synchronises `stream`
+ * once per matrix exponential).  Shapes: 1 <= Hkv <= 64, 1 <= Nq <= T,
+ * 1 <= G <= 8, Dm >= 1; D is 128. */
+size_t kvq_optr_workspace_bytes(int num_kv_heads, int T, int Nq, int G, int Dm);
+int kvq_optr_calibrate(int num_kv_heads, int T, int Nq, int G, int Dm,
+                       const uint16_t* K, const uint16_t* V, const uint16_t* Q,
+                       const float* W_O, const float* R0, const float* mu,
+                       float clip_k, float clip_v, float lambda_k, float lr, int steps,
+                       float sm_scale, float* R_out, float* history,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* One evaluation of a calibration objective and its gradient, for callers that
+ * drive their own optimiser (and for testing): which = 0, the key objective L_K
+ * at R_K = R0_K exp(A_key - A_key^T); which = 1, the value objective L_V at
+ * R_V = R0_V exp(A_value - A_value^T) with p~ taken at A_key.  A_key, A_value:
+ * device fp32 [Hkv][D][D] (A_value may be NULL when which = 0).  loss: device
+ * fp32 [Hkv]; grad: device fp32 [Hkv][D][D], d loss / dA (straight-through).
+ * Other arguments as for kvq_optr_calibrate.  Returns when done. */
+int kvq_optr_loss_grad(int num_kv_heads, int T, int Nq, int G, int Dm,
+                       const uint16_t* K, const uint16_t* V, const uint16_t* Q,
+                       const float* W_O, const float* R0, const float* mu,
+                       float clip_k, float clip_v, float lambda_k, float sm_scale,
+                       const float* A_key, const float* A_value, int which,
+                       float* loss, float* grad, void* workspace, size_t ws_bytes,
+                       void* stream);
+
 /* ---- status and diagnostics ---------------------------------------------- */
 
 /* Read and clear the handle's device status word (KVQ_STATUS_* bits).

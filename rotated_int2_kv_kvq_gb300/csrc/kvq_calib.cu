@@ -1,0 +1,738 @@
+// kvq_calib.cu — OptR rotation calibration on the GPU (off the decode path).
+//
+// Method: "Output-Aware Rotation for INT2 KV-Cache Quantization" (pith.science
+// review of arXiv 2608.02691).  Per KV head a correction of a base rotation,
+// R = R0 exp(S) with S = A - A^T ("What carries the argument", mechanism (1)),
+// is learned with Adam ("Assumptions & free parameters": 80 steps, lambda_K = 1)
+// through the whole quantised path with a straight-through estimator for the
+// rounding (mechanism (3)): first for keys, minimising KL(p || p~) plus lambda_K
+// times the key-induced post-W_O error with values unquantised; then for values,
+// minimising the value-induced post-W_O error with the quantised-key attention
+// fixed (the error decomposition of "What carries the argument" and the referee
+// report's Eqs. (14), (16)).  The objective is taken over the last Nq query
+// positions of a causal calibration chunk.
+//
+// Structure: every contraction is one launch of a batched fp32 GEMM (batch =
+// KV head); the quantiser, its straight-through backward, the causal softmax
+// with its KL and backward, the post-W_O error and Adam are row or element
+// kernels; exp(S) is scaling and squaring of a Taylor polynomial (carrying
+// exp - I through the squarings), and the
+// gradient with respect to S is the adjoint of the Frechet derivative of exp,
+// L_exp(S^T, G), read from the upper-right block of exp([[S^T, G], [0, S^T]]).
+// The host needs each step's largest |S| to pick the number of squarings, so a
+// calibration call synchronises its stream once per matrix exponential.
+#include <math.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kD = kDim;
+
+// ---------------------------------------------------------------------------
+// Batched fp32 GEMM: C[b] = alpha * op(A[b]) * op(B[b]) + beta * C[b], row-major.
+// op(A) is M x K: A[m * lda + k], or, transposed, A stored K x M: A[k * lda + m].
+// op(B) is K x N: B[k * ldb + n], or, transposed, B stored N x K: B[n * ldb + k].
+// 64 x 64 tile per CTA, k-slices of 16 staged in shared memory, 4 x 4 outputs
+// per thread.  beta == 0 does not read C.
+// ---------------------------------------------------------------------------
+struct Gemm {
+  const float* A;
+  const float* B;
+  float* C;
+  int M, N, K, lda, ldb, ldc;
+  long long sA, sB, sC;
+  float alpha, beta;
+  int ta, tb;
+};
+
+__global__ void __launch_bounds__(256) gemm_kernel(Gemm g) {
+  __shared__ float As[16][68];
+  __shared__ float Bs[16][68];
+  const int bz = blockIdx.z;
+  const float* A = g.A + bz * g.sA;
+  const float* B = g.B + bz * g.sB;
+  float* C = g.C + bz * g.sC;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  for (int k0 = 0; k0 < g.K; k0 += 16) {
+    for (int i = tid; i < 1024; i += 256) {
+      int mm, kk;
+      if (g.ta) { kk = i >> 6; mm = i & 63; } else { mm = i >> 4; kk = i & 15; }
+      const int gm = m0 + mm, gk = k0 + kk;
+      float v = 0.0f;
+      if (gm < g.M && gk < g.K)
+        v = g.ta ? A[static_cast<long long>(gk) * g.lda + gm] : A[static_cast<long long>(gm) * g.lda + gk];
+      As[kk][mm] = v;
+    }
+    for (int i = tid; i < 1024; i += 256) {
+      int nn, kk;
+      if (g.tb) { nn = i >> 4; kk = i & 15; } else { kk = i >> 6; nn = i & 63; }
+      const int gn = n0 + nn, gk = k0 + kk;
+      float v = 0.0f;
+      if (gn < g.N && gk < g.K)
+        v = g.tb ? B[static_cast<long long>(gn) * g.ldb + gk] : B[static_cast<long long>(gk) * g.ldb + gn];
+      Bs[kk][nn] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty + 16 * i;
+    if (m >= g.M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx + 16 * j;
+      if (n >= g.N) continue;
+      float* c = C + static_cast<long long>(m) * g.ldc + n;
+      *c = g.beta == 0.0f ? g.alpha * acc[i][j] : fmaf(g.alpha, acc[i][j], g.beta * *c);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Row kernels (one warp per row of kD = 128 elements; lane l owns 4l .. 4l+3)
+// ---------------------------------------------------------------------------
+
+// INT2 quantiser of the library (fp32 arithmetic, fp16 scale and zero, round
+// half to even), row by row, keeping what the straight-through backward needs:
+// flag 0 = code not at a clamp, 1 = clamped high (value follows c * max),
+// 2 = clamped low (follows c * min); argmax / argmin (first index on ties).
+__global__ void quantise_rows_kernel(const float* __restrict__ r, float* __restrict__ rt,
+                                     uint8_t* __restrict__ flag, int* __restrict__ amax,
+                                     int* __restrict__ amin, long long rows, float clip) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float4 x4 = *reinterpret_cast<const float4*>(r + row * kD + 4 * lane);
+  const float x[4] = {x4.x, x4.y, x4.z, x4.w};
+  float mx = x[0], mn = x[0];
+  int imx = 4 * lane, imn = 4 * lane;
+#pragma unroll
+  for (int j = 1; j < 4; ++j) {
+    if (x[j] > mx) { mx = x[j]; imx = 4 * lane + j; }
+    if (x[j] < mn) { mn = x[j]; imn = 4 * lane + j; }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float omx = __shfl_xor_sync(0xffffffffu, mx, off);
+    const int oimx = __shfl_xor_sync(0xffffffffu, imx, off);
+    const float omn = __shfl_xor_sync(0xffffffffu, mn, off);
+    const int oimn = __shfl_xor_sync(0xffffffffu, imn, off);
+    if (omx > mx || (omx == mx && oimx < imx)) { mx = omx; imx = oimx; }
+    if (omn < mn || (omn == mn && oimn < imn)) { mn = omn; imn = oimn; }
+  }
+  const float mxc = __fmul_rn(clip, mx);
+  const float mnc = __fmul_rn(clip, mn);
+  const float s = __half2float(__float2half_rn(__fdiv_rn(__fsub_rn(mxc, mnc), 3.0f)));
+  const float z = __half2float(__float2half_rn(mnc));
+  float o[4];
+  uint32_t fl = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float code = 0.0f;
+    uint32_t f = 2;
+    if (s != 0.0f) {
+      const float t = __fdiv_rn(__fsub_rn(x[j], z), s);
+      code = fminf(fmaxf(rintf(t), 0.0f), 3.0f);
+      f = t > 3.0f ? 1u : (t < 0.0f ? 2u : 0u);
+    }
+    o[j] = fmaf(code, s, z);      // code * s is exact: one rounding, as the oracle's
+    fl |= f << (8 * j);
+  }
+  *reinterpret_cast<float4*>(rt + row * kD + 4 * lane) = make_float4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint32_t*>(flag + row * kD + 4 * lane) = fl;
+  if (lane == 0) {
+    amax[row] = imx;
+    amin[row] = imn;
+  }
+}
+
+// d loss / d r from d loss / d r~: identity where the code is not clamped; the
+// clamped elements' gradients, times c, go to the row's argmax / argmin.
+__global__ void ste_backward_kernel(const float* __restrict__ grt, const uint8_t* __restrict__ flag,
+                                    const int* __restrict__ amax, const int* __restrict__ amin,
+                                    float* __restrict__ gr, long long rows, float clip) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float4 g4 = *reinterpret_cast<const float4*>(grt + row * kD + 4 * lane);
+  const float g[4] = {g4.x, g4.y, g4.z, g4.w};
+  const uint32_t fl = *reinterpret_cast<const uint32_t*>(flag + row * kD + 4 * lane);
+  float o[4], sh = 0.0f, sl = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t f = (fl >> (8 * j)) & 0xffu;
+    o[j] = f == 0 ? g[j] : 0.0f;
+    if (f == 1) sh += g[j];
+    if (f == 2) sl += g[j];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sh += __shfl_xor_sync(0xffffffffu, sh, off);
+    sl += __shfl_xor_sync(0xffffffffu, sl, off);
+  }
+  const int im = amax[row], in = amin[row];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (4 * lane + j == im) o[j] = fmaf(clip, sh, o[j]);
+    if (4 * lane + j == in) o[j] = fmaf(clip, sl, o[j]);
+  }
+  *reinterpret_cast<float4*>(gr + row * kD + 4 * lane) = make_float4(o[0], o[1], o[2], o[3]);
+}
+
+// ---------------------------------------------------------------------------
+// Causal softmax over a row of T logits (one CTA per row).  Row q * G + h of a
+// head belongs to the query at position T - Nq + q.  mode 0: write p (the
+// reference attention).  mode 1: write p~, dp = p~ - p and add the row's
+// KL(p || p~) to kl[head].
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = is_max ? fmaxf(v, o) : v + o;
+  }
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  v = red[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) v = is_max ? fmaxf(v, red[i]) : v + red[i];
+  return v;
+}
+
+__global__ void softmax_rows_kernel(const float* __restrict__ logits, const float* __restrict__ p,
+                                    float* __restrict__ out, float* __restrict__ dp,
+                                    float* __restrict__ kl, int T, int Nq, int G, int mode) {
+  __shared__ float red[32];
+  const int row = blockIdx.x, head = blockIdx.y;
+  const long long base = (static_cast<long long>(head) * Nq * G + row) * T;
+  const int pos = T - Nq + row / G;
+  float mx = -INFINITY;
+  for (int t = threadIdx.x; t <= pos; t += blockDim.x) mx = fmaxf(mx, logits[base + t]);
+  mx = block_reduce(mx, red, true);
+  float sum = 0.0f;
+  for (int t = threadIdx.x; t <= pos; t += blockDim.x) sum += __expf(logits[base + t] - mx);
+  sum = block_reduce(sum, red, false);
+  const float inv = 1.0f / sum, lsum = logf(sum);
+  float klp = 0.0f;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    float v = 0.0f;
+    if (t <= pos) v = __expf(logits[base + t] - mx) * inv;
+    out[base + t] = v;
+    if (mode == 1) {
+      const float pr = p[base + t];
+      dp[base + t] = v - pr;
+      if (pr > 0.0f) klp += pr * (logf(pr) - (logits[base + t] - mx - lsum));
+    }
+  }
+  if (mode == 1) {
+    klp = block_reduce(klp, red, false);
+    if (threadIdx.x == 0) atomicAdd(kl + head, klp);
+  }
+}
+
+// d loss / d logit = p~ (g - <p~, g>) + (p~ - p) / Nq  (the KL part only with
+// with_kl).  In place over g.
+__global__ void softmax_backward_kernel(const float* __restrict__ pt, const float* __restrict__ p,
+                                        float* __restrict__ g, int T, int Nq, int G, float inv_nq,
+                                        int with_kl) {
+  __shared__ float red[32];
+  const int row = blockIdx.x, head = blockIdx.y;
+  const long long base = (static_cast<long long>(head) * Nq * G + row) * T;
+  float dot = 0.0f;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) dot = fmaf(pt[base + t], g[base + t], dot);
+  dot = block_reduce(dot, red, false);
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    const float a = pt[base + t];
+    float v = a * (g[base + t] - dot);
+    if (with_kl) v = fmaf(a - p[base + t], inv_nq, v);
+    g[base + t] = v;
+  }
+}
+
+// err[head] += sum e^2 over the head's Nq x Dm block; ge = coef * e.
+__global__ void sq_err_kernel(const float* __restrict__ e, float* __restrict__ ge,
+                              float* __restrict__ err, long long n, float coef) {
+  __shared__ float red[32];
+  const int head = blockIdx.y;
+  const float* eh = e + head * n;
+  float* gh = ge + head * n;
+  float s = 0.0f;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float v = eh[i];
+    s = fmaf(v, v, s);
+    gh[i] = coef * v;
+  }
+  s = block_reduce(s, red, false);
+  if (threadIdx.x == 0) atomicAdd(err + head, s);
+}
+
+// ---------------------------------------------------------------------------
+// Element kernels
+// ---------------------------------------------------------------------------
+
+// out = bf16 x (- mu per column when mu != null), fp32.
+__global__ void bf16_to_f32_kernel(const uint16_t* __restrict__ x, const float* __restrict__ mu,
+                                   float* __restrict__ out, long long rows_per_head, long long n) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float v = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
+    if (mu) v = __fsub_rn(v, mu[(i / (rows_per_head * kD)) * kD + (i % kD)]);
+    out[i] = v;
+  }
+}
+
+// y = x + mu per column (per head)
+__global__ void add_mu_kernel(float* __restrict__ x, const float* __restrict__ mu,
+                              long long rows_per_head, long long n) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    x[i] += mu[(i / (rows_per_head * kD)) * kD + (i % kD)];
+}
+
+// Per head (n x n, batch stride n*n): out = a * X + b * I
+__global__ void axpi_kernel(const float* __restrict__ X, float* __restrict__ out, int n, float a,
+                            float b, int heads) {
+  const long long total = static_cast<long long>(heads) * n * n;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long k = i % (static_cast<long long>(n) * n);
+    const int r = static_cast<int>(k / n), c = static_cast<int>(k % n);
+    out[i] = (X ? a * X[i] : 0.0f) + (r == c ? b : 0.0f);
+  }
+}
+
+// S = A - A^T (kD x kD per head)
+__global__ void skew_kernel(const float* __restrict__ A, float* __restrict__ S, int heads) {
+  const long long total = static_cast<long long>(heads) * kD * kD;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long h = i / (kD * kD), k = i % (kD * kD);
+    const int r = static_cast<int>(k / kD), c = static_cast<int>(k % kD);
+    S[i] = A[h * kD * kD + r * kD + c] - A[h * kD * kD + c * kD + r];
+  }
+}
+
+// M = [[S^T, Gb], [0, S^T]] (2kD x 2kD per head)
+__global__ void block_kernel(const float* __restrict__ S, const float* __restrict__ Gb,
+                             float* __restrict__ M, int heads) {
+  const int n = 2 * kD;
+  const long long total = static_cast<long long>(heads) * n * n;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long h = i / (n * n), k = i % (n * n);
+    const int r = static_cast<int>(k / n), c = static_cast<int>(k % n);
+    const float* Sh = S + h * kD * kD;
+    float v = 0.0f;
+    if (r < kD && c < kD) v = Sh[c * kD + r];
+    else if (r < kD) v = Gb[h * kD * kD + r * kD + (c - kD)];
+    else if (c >= kD) v = Sh[(c - kD) * kD + (r - kD)];
+    M[i] = v;
+  }
+}
+
+// gA = X - X^T where X is the upper-right kD x kD block of M (2kD x 2kD per head)
+__global__ void grad_from_block_kernel(const float* __restrict__ M, float* __restrict__ gA,
+                                       int heads) {
+  const int n = 2 * kD;
+  const long long total = static_cast<long long>(heads) * kD * kD;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long h = i / (kD * kD), k = i % (kD * kD);
+    const int r = static_cast<int>(k / kD), c = static_cast<int>(k % kD);
+    const float* Mh = M + h * n * n;
+    gA[i] = Mh[r * n + kD + c] - Mh[c * n + kD + r];
+  }
+}
+
+// max over columns of sum |X| (the 1-norm), per head, into norm[head] (as int
+// bits: non-negative floats order like their bit patterns)
+__global__ void norm1_kernel(const float* __restrict__ X, int n, unsigned int* __restrict__ norm) {
+  const int h = blockIdx.y, c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= n) return;
+  const float* Xh = X + static_cast<long long>(h) * n * n;
+  float s = 0.0f;
+  for (int r = 0; r < n; ++r) s += fabsf(Xh[static_cast<long long>(r) * n + c]);
+  atomicMax(norm + h, __float_as_uint(s));
+}
+
+__global__ void adam_kernel(float* __restrict__ A, const float* __restrict__ g,
+                            float* __restrict__ m, float* __restrict__ v, long long n, float lr,
+                            float bc1, float bc2) {
+  const float b1 = 0.9f, b2 = 0.999f, eps = 1e-8f;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float gi = g[i];
+    const float mi = b1 * m[i] + (1.0f - b1) * gi;
+    const float vi = b2 * v[i] + (1.0f - b2) * gi * gi;
+    m[i] = mi;
+    v[i] = vi;
+    A[i] -= lr * (mi / bc1) / (sqrtf(vi / bc2) + eps);
+  }
+}
+
+// hist[head] = (kl[head] + lam * err[head]) / Nq; then clear kl, err
+__global__ void loss_kernel(float* __restrict__ kl, float* __restrict__ err, float* __restrict__ hist,
+                            int heads, float lam, float inv_nq) {
+  const int h = threadIdx.x;
+  if (h >= heads) return;
+  hist[h] = (kl[h] + lam * err[h]) * inv_nq;
+  kl[h] = 0.0f;
+  err[h] = 0.0f;
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+int grid_for(long long n) { return static_cast<int>(std::min<long long>((n + 255) / 256, 4096)); }
+
+struct Ctx {
+  cudaStream_t st;
+  int H, T, Nq, G, Dm;
+  cudaError_t err = cudaSuccess;
+  void check() { if (err == cudaSuccess) err = cudaGetLastError(); }
+};
+
+// C = alpha op(A) op(B) + beta C for every head (strides sA, sB, sC per head)
+void gemm(Ctx& c, const float* A, int ta, long long sA, int lda, const float* B, int tb,
+          long long sB, int ldb, float* C, long long sC, int ldc, int M, int N, int K, float alpha,
+          float beta) {
+  Gemm g{A, B, C, M, N, K, lda, ldb, ldc, sA, sB, sC, alpha, beta, ta, tb};
+  dim3 grid((N + 63) / 64, (M + 63) / 64, c.H);
+  gemm_kernel<<<grid, 256, 0, c.st>>>(g);
+  c.check();
+}
+
+// Workspace carve-up (floats unless noted), all per-head arrays [H][...]
+struct Ws {
+  float *x32, *r, *rt, *kt, *gkt, *grt, *gr;        // [T][D]
+  float *V32;                                       // [T][D]
+  float *Q32;                                       // [Nq*G][D]
+  float *logit, *pt, *p, *dp;                       // [Nq*G][T]
+  float *att, *gatt;                                // [Nq*G][D]
+  float *e, *ge;                                    // [Nq][Dm]
+  float *A, *m, *v, *S, *E, *R, *gR, *Gb, *gA;      // [D][D]
+  float *X2, *P2, *Q2;                              // [2D][2D] (expm scratch)
+  float *kl, *errsum;                               // [H]
+  unsigned int* norm;                               // [H]
+  uint8_t* flag;                                    // [T][D]
+  int *amax, *amin;                                 // [T]
+  size_t total;
+};
+
+Ws carve(uint8_t* base, int H, int T, int Nq, int G, int Dm) {
+  Ws w;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? base + o : nullptr;
+    o += (bytes + 255) & ~static_cast<size_t>(255);
+    return p;
+  };
+  const size_t hd = static_cast<size_t>(H);
+  const size_t TD = hd * T * kD * 4, QD = hd * Nq * G * kD * 4, QT = hd * Nq * G * T * 4;
+  const size_t DD = hd * kD * kD * 4, D2 = hd * 4 * kD * kD * 4;
+  w.x32 = reinterpret_cast<float*>(take(TD));
+  w.r = reinterpret_cast<float*>(take(TD));
+  w.rt = reinterpret_cast<float*>(take(TD));
+  w.kt = reinterpret_cast<float*>(take(TD));
+  w.gkt = reinterpret_cast<float*>(take(TD));
+  w.grt = reinterpret_cast<float*>(take(TD));
+  w.gr = reinterpret_cast<float*>(take(TD));
+  w.V32 = reinterpret_cast<float*>(take(TD));
+  w.Q32 = reinterpret_cast<float*>(take(QD));
+  w.logit = reinterpret_cast<float*>(take(QT));
+  w.pt = reinterpret_cast<float*>(take(QT));
+  w.p = reinterpret_cast<float*>(take(QT));
+  w.dp = reinterpret_cast<float*>(take(QT));
+  w.att = reinterpret_cast<float*>(take(QD));
+  w.gatt = reinterpret_cast<float*>(take(QD));
+  w.e = reinterpret_cast<float*>(take(hd * Nq * Dm * 4));
+  w.ge = reinterpret_cast<float*>(take(hd * Nq * Dm * 4));
+  w.A = reinterpret_cast<float*>(take(DD));
+  w.m = reinterpret_cast<float*>(take(DD));
+  w.v = reinterpret_cast<float*>(take(DD));
+  w.S = reinterpret_cast<float*>(take(DD));
+  w.E = reinterpret_cast<float*>(take(DD));
+  w.R = reinterpret_cast<float*>(take(DD));
+  w.gR = reinterpret_cast<float*>(take(DD));
+  w.Gb = reinterpret_cast<float*>(take(DD));
+  w.gA = reinterpret_cast<float*>(take(DD));
+  w.X2 = reinterpret_cast<float*>(take(D2));
+  w.P2 = reinterpret_cast<float*>(take(D2));
+  w.Q2 = reinterpret_cast<float*>(take(D2));
+  w.kl = reinterpret_cast<float*>(take(hd * 4));
+  w.errsum = reinterpret_cast<float*>(take(hd * 4));
+  w.norm = reinterpret_cast<unsigned int*>(take(hd * 4));
+  w.flag = take(hd * T * kD);
+  w.amax = reinterpret_cast<int*>(take(hd * T * 4));
+  w.amin = reinterpret_cast<int*>(take(hd * T * 4));
+  w.total = o;
+  return w;
+}
+
+// exp(M) for every head (n x n, n = kD or 2 kD): scaling by 2^j with |M / 2^j|_1
+// <= 1/2, a degree-12 Taylor polynomial, then j squarings.  The squarings carry
+// F = exp(X) - I (F <- 2F + F F), so rounding errors stay relative to F rather
+// than to I: the rotation stays orthogonal to fp32 accuracy.  Result in `out`
+// (which may be X); X, P, Q are scratch (n x n per head); M is read only to
+// form X, so it may be Q.  Reads the 1-norms (syncs the stream).
+void expm(Ctx& c, Ws& w, const float* M, int n, float* out, float* X, float* P, float* Q) {
+  if (c.err != cudaSuccess) return;
+  const long long nn = static_cast<long long>(n) * n;
+  c.err = cudaMemsetAsync(w.norm, 0, c.H * sizeof(unsigned int), c.st);
+  norm1_kernel<<<dim3((n + 127) / 128, c.H), 128, 0, c.st>>>(M, n, w.norm);
+  c.check();
+  std::vector<unsigned int> nb(c.H);
+  if (c.err == cudaSuccess)
+    c.err = cudaMemcpyAsync(nb.data(), w.norm, c.H * sizeof(unsigned int), cudaMemcpyDeviceToHost, c.st);
+  if (c.err == cudaSuccess) c.err = cudaStreamSynchronize(c.st);
+  if (c.err != cudaSuccess) return;
+  float nmax = 0.0f;
+  for (unsigned int b : nb) {
+    float f;
+    memcpy(&f, &b, 4);
+    nmax = std::max(nmax, f);
+  }
+  int j = 0;
+  while (nmax / ldexpf(1.0f, j) > 0.5f && j < 60) ++j;
+  const float sc = ldexpf(1.0f, -j);
+  const int g = grid_for(c.H * nn);
+  axpi_kernel<<<g, 256, 0, c.st>>>(M, X, n, sc, 0.0f, c.H);             // X = M / 2^j
+  axpi_kernel<<<g, 256, 0, c.st>>>(nullptr, P, n, 0.0f, 1.0f, c.H);     // P = I
+  c.check();
+  // Horner down to P = I + X/2 (I + X/3 (...)); then F = exp(X) - I = X P
+  float* cur = P;
+  float* nxt = Q;
+  for (int k = 12; k >= 2; --k) {
+    axpi_kernel<<<g, 256, 0, c.st>>>(nullptr, nxt, n, 0.0f, 1.0f, c.H);
+    c.check();
+    gemm(c, X, 0, nn, n, cur, 0, nn, n, nxt, nn, n, n, n, n, 1.0f / k, 1.0f);
+    std::swap(cur, nxt);
+  }
+  gemm(c, X, 0, nn, n, cur, 0, nn, n, nxt, nn, n, n, n, n, 1.0f, 0.0f);
+  std::swap(cur, nxt);                                                   // cur = F
+  for (int s = 0; s < j && c.err == cudaSuccess; ++s) {
+    c.err = cudaMemcpyAsync(nxt, cur, c.H * nn * sizeof(float), cudaMemcpyDeviceToDevice, c.st);
+    gemm(c, cur, 0, nn, n, cur, 0, nn, n, nxt, nn, n, n, n, n, 1.0f, 2.0f);   // 2F + F F
+    std::swap(cur, nxt);
+  }
+  axpi_kernel<<<g, 256, 0, c.st>>>(cur, out, n, 1.0f, 1.0f, c.H);       // out = F + I
+  c.check();
+}
+
+// R = R0 exp(A - A^T) for every head; also leaves S and E.
+void rotation(Ctx& c, Ws& w, const float* R0) {
+  const long long DD = static_cast<long long>(kD) * kD;
+  skew_kernel<<<grid_for(c.H * DD), 256, 0, c.st>>>(w.A, w.S, c.H);
+  c.check();
+  expm(c, w, w.S, kD, w.E, w.X2, w.P2, w.Q2);
+  gemm(c, R0, 0, DD, kD, w.E, 0, DD, kD, w.R, DD, kD, kD, kD, kD, 1.0f, 0.0f);
+}
+
+// d loss / dA from d loss / dR (in w.gR): Gb = R0^T gR, then the Frechet adjoint.
+void rotation_backward(Ctx& c, Ws& w, const float* R0) {
+  const long long DD = static_cast<long long>(kD) * kD, D4 = 4 * DD;
+  gemm(c, R0, 1, DD, kD, w.gR, 0, DD, kD, w.Gb, DD, kD, kD, kD, kD, 1.0f, 0.0f);
+  // the block matrix in P2; expm reads it once (into X2, scaled) before P2 is reused
+  block_kernel<<<grid_for(c.H * D4), 256, 0, c.st>>>(w.S, w.Gb, w.P2, c.H);
+  c.check();
+  expm(c, w, w.P2, 2 * kD, w.X2, w.X2, w.Q2, w.P2);
+  grad_from_block_kernel<<<grid_for(c.H * DD), 256, 0, c.st>>>(w.X2, w.gA, c.H);
+  c.check();
+}
+
+// Problem description shared by the entry points.
+struct Prob {
+  int H, T, Nq, G, Dm;
+  const uint16_t *K, *V, *Q;
+  const float *W, *R0, *mu;
+  float clip_k, clip_v, lambda_k, sm_scale;
+};
+
+// Inputs to fp32 (centred keys, values, queries) and the reference attention p
+// of the exact keys.
+void prepare(Ctx& c, Ws& w, const Prob& pb) {
+  const long long TD = static_cast<long long>(pb.T) * kD, QG = static_cast<long long>(pb.Nq) * pb.G;
+  const long long QT = QG * pb.T, QD = QG * kD;
+  bf16_to_f32_kernel<<<grid_for(pb.H * TD), 256, 0, c.st>>>(pb.K, pb.mu, w.x32, pb.T, pb.H * TD);
+  bf16_to_f32_kernel<<<grid_for(pb.H * TD), 256, 0, c.st>>>(pb.V, nullptr, w.V32, pb.T, pb.H * TD);
+  bf16_to_f32_kernel<<<grid_for(pb.H * QD), 256, 0, c.st>>>(pb.Q, nullptr, w.Q32, QG, pb.H * QD);
+  bf16_to_f32_kernel<<<grid_for(pb.H * TD), 256, 0, c.st>>>(pb.K, nullptr, w.kt, pb.T, pb.H * TD);
+  c.check();
+  if (c.err == cudaSuccess) c.err = cudaMemsetAsync(w.kl, 0, pb.H * 4, c.st);
+  if (c.err == cudaSuccess) c.err = cudaMemsetAsync(w.errsum, 0, pb.H * 4, c.st);
+  gemm(c, w.Q32, 0, QD, kD, w.kt, 1, TD, kD, w.logit, QT, pb.T, static_cast<int>(QG), pb.T, kD,
+       pb.sm_scale, 0.0f);
+  softmax_rows_kernel<<<dim3(static_cast<unsigned>(QG), pb.H), 256, 0, c.st>>>(
+      w.logit, nullptr, w.p, nullptr, nullptr, pb.T, pb.Nq, pb.G, 0);
+  c.check();
+}
+
+// One evaluation of objective `which` (0 keys, 1 values) at the generator in
+// w.A: the loss per head into loss[H], and with `grad` d loss / dA into w.gA.
+// Keys leave their quantised-key attention p~ in w.pt, which the value
+// objective reads.
+void objective(Ctx& c, Ws& w, const Prob& pb, int which, bool grad, float* loss) {
+  const int H = pb.H, T = pb.T, Nq = pb.Nq, Dm = pb.Dm;
+  const long long TD = static_cast<long long>(T) * kD, DD = static_cast<long long>(kD) * kD;
+  const long long QG = static_cast<long long>(Nq) * pb.G, QT = QG * T, QD = QG * kD;
+  const long long ED = static_cast<long long>(Nq) * Dm, GD = static_cast<long long>(pb.G) * kD;
+  const float inv_nq = 1.0f / Nq;
+  const float* R0w = pb.R0 + (which ? H * DD : 0);
+  const float clip = which ? pb.clip_v : pb.clip_k;
+  const float* X = which ? w.V32 : w.x32;          // the rows that are rotated
+  const long long rows = static_cast<long long>(H) * T;
+  const int row_blocks = static_cast<int>((rows + 7) / 8);
+  const float lam = which ? 1.0f : pb.lambda_k;
+  // ---- forward
+  rotation(c, w, R0w);
+  gemm(c, X, 0, TD, kD, w.R, 0, DD, kD, w.r, TD, kD, T, kD, kD, 1.0f, 0.0f);     // r = X R
+  quantise_rows_kernel<<<row_blocks, 256, 0, c.st>>>(w.r, w.rt, w.flag, w.amax, w.amin, rows, clip);
+  c.check();
+  gemm(c, w.rt, 0, TD, kD, w.R, 1, DD, kD, w.kt, TD, kD, T, kD, kD, 1.0f, 0.0f);  // rt R^T
+  if (which == 0) {
+    add_mu_kernel<<<grid_for(H * TD), 256, 0, c.st>>>(w.kt, pb.mu, T, H * TD);
+    c.check();
+    gemm(c, w.Q32, 0, QD, kD, w.kt, 1, TD, kD, w.logit, QT, T, static_cast<int>(QG), T, kD,
+         pb.sm_scale, 0.0f);
+    softmax_rows_kernel<<<dim3(static_cast<unsigned>(QG), H), 256, 0, c.st>>>(
+        w.logit, w.p, w.pt, w.dp, w.kl, T, Nq, pb.G, 1);
+    c.check();
+    gemm(c, w.dp, 0, QT, T, w.V32, 0, TD, kD, w.att, QD, kD, static_cast<int>(QG), kD, T, 1.0f,
+         0.0f);                                                                    // dp V
+  } else {
+    // att = p~ (v~ - v)
+    gemm(c, w.pt, 0, QT, T, w.kt, 0, TD, kD, w.att, QD, kD, static_cast<int>(QG), kD, T, 1.0f, 0.0f);
+    gemm(c, w.pt, 0, QT, T, w.V32, 0, TD, kD, w.att, QD, kD, static_cast<int>(QG), kD, T, -1.0f,
+         1.0f);
+  }
+  // e = att (Nq x G D) W^T (G D x Dm)
+  gemm(c, w.att, 0, QD, static_cast<int>(GD), pb.W, 1, static_cast<long long>(Dm) * GD,
+       static_cast<int>(GD), w.e, ED, Dm, Nq, Dm, static_cast<int>(GD), 1.0f, 0.0f);
+  sq_err_kernel<<<dim3(std::max(1, std::min(64, static_cast<int>((ED + 255) / 256))), H), 256, 0,
+                  c.st>>>(w.e, w.ge, w.errsum, ED, 2.0f * lam * inv_nq);
+  c.check();
+  loss_kernel<<<1, 64, 0, c.st>>>(w.kl, w.errsum, loss, H, lam, inv_nq);
+  c.check();
+  if (!grad) return;
+  // ---- backward
+  // gatt = ge W  (Nq x Dm)(Dm x G D)
+  gemm(c, w.ge, 0, ED, Dm, pb.W, 0, static_cast<long long>(Dm) * GD, static_cast<int>(GD), w.gatt,
+       QD, static_cast<int>(GD), Nq, static_cast<int>(GD), Dm, 1.0f, 0.0f);
+  if (which == 0) {
+    // g_pt = gatt V^T (QG x T) in logit's buffer, then the softmax backward
+    gemm(c, w.gatt, 0, QD, kD, w.V32, 1, TD, kD, w.logit, QT, T, static_cast<int>(QG), T, kD, 1.0f,
+         0.0f);
+    softmax_backward_kernel<<<dim3(static_cast<unsigned>(QG), H), 256, 0, c.st>>>(
+        w.pt, w.p, w.logit, T, Nq, pb.G, inv_nq, 1);
+    c.check();
+    // g_kt = scale g_logit^T Q  (T x D)
+    gemm(c, w.logit, 1, QT, T, w.Q32, 0, QD, kD, w.gkt, TD, kD, T, kD, static_cast<int>(QG),
+         pb.sm_scale, 0.0f);
+  } else {
+    // g_vt = p~^T gatt  (T x D)
+    gemm(c, w.pt, 1, QT, T, w.gatt, 0, QD, kD, w.gkt, TD, kD, T, kD, static_cast<int>(QG), 1.0f,
+         0.0f);
+  }
+  gemm(c, w.gkt, 0, TD, kD, w.R, 0, DD, kD, w.grt, TD, kD, T, kD, kD, 1.0f, 0.0f);   // g_rt
+  gemm(c, w.gkt, 1, TD, kD, w.rt, 0, TD, kD, w.gR, DD, kD, kD, kD, T, 1.0f, 0.0f);    // gkt^T rt
+  ste_backward_kernel<<<row_blocks, 256, 0, c.st>>>(w.grt, w.flag, w.amax, w.amin, w.gr, rows, clip);
+  c.check();
+  gemm(c, X, 1, TD, kD, w.gr, 0, TD, kD, w.gR, DD, kD, kD, kD, T, 1.0f, 1.0f);        // + X^T gr
+  rotation_backward(c, w, R0w);
+}
+
+}  // namespace
+
+size_t optr_workspace_bytes(int H, int T, int Nq, int G, int Dm) {
+  return carve(nullptr, H, T, Nq, G, Dm).total;
+}
+
+int optr_calibrate(int H, int T, int Nq, int G, int Dm, const uint16_t* K, const uint16_t* V,
+                   const uint16_t* Qb, const float* W, const float* R0, const float* mu,
+                   float clip_k, float clip_v, float lambda_k, float lr, int steps, float sm_scale,
+                   float* R_out, float* hist, void* workspace, cudaStream_t st) {
+  Ctx c;
+  c.st = st;
+  c.H = H; c.T = T; c.Nq = Nq; c.G = G; c.Dm = Dm;
+  Ws w = carve(static_cast<uint8_t*>(workspace), H, T, Nq, G, Dm);
+  const Prob pb{H, T, Nq, G, Dm, K, V, Qb, W, R0, mu, clip_k, clip_v, lambda_k, sm_scale};
+  const long long DD = static_cast<long long>(kD) * kD;
+  prepare(c, w, pb);
+  for (int which = 0; which < 2 && c.err == cudaSuccess; ++which) {
+    float* hw = hist + static_cast<long long>(which) * (steps + 1) * H;
+    if (c.err == cudaSuccess) c.err = cudaMemsetAsync(w.A, 0, H * DD * 4, st);
+    if (c.err == cudaSuccess) c.err = cudaMemsetAsync(w.m, 0, H * DD * 4, st);
+    if (c.err == cudaSuccess) c.err = cudaMemsetAsync(w.v, 0, H * DD * 4, st);
+    for (int step = 0; step <= steps && c.err == cudaSuccess; ++step) {
+      // the loss before each update, and after the last one (no gradient then)
+      objective(c, w, pb, which, step < steps, hw + static_cast<long long>(step) * H);
+      if (step == steps) break;
+      adam_kernel<<<grid_for(H * DD), 256, 0, st>>>(w.A, w.gA, w.m, w.v, H * DD, lr,
+                                                    1.0f - powf(0.9f, step + 1.0f),
+                                                    1.0f - powf(0.999f, step + 1.0f));
+      c.check();
+    }
+    // the calibrated rotation (the last forward ran at the final generator);
+    // after the keys, the attention p~ they give stays in w.pt for the values
+    if (c.err == cudaSuccess)
+      c.err = cudaMemcpyAsync(R_out + static_cast<long long>(which) * H * DD, w.R, H * DD * 4,
+                              cudaMemcpyDeviceToDevice, st);
+  }
+  if (c.err == cudaSuccess) c.err = cudaStreamSynchronize(st);
+  return c.err == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+int optr_loss_grad(int H, int T, int Nq, int G, int Dm, const uint16_t* K, const uint16_t* V,
+                   const uint16_t* Qb, const float* W, const float* R0, const float* mu,
+                   float clip_k, float clip_v, float lambda_k, float sm_scale, const float* A_key,
+                   const float* A_value, int which, float* loss, float* grad, void* workspace,
+                   cudaStream_t st) {
+  Ctx c;
+  c.st = st;
+  c.H = H; c.T = T; c.Nq = Nq; c.G = G; c.Dm = Dm;
+  Ws w = carve(static_cast<uint8_t*>(workspace), H, T, Nq, G, Dm);
+  const Prob pb{H, T, Nq, G, Dm, K, V, Qb, W, R0, mu, clip_k, clip_v, lambda_k, sm_scale};
+  const long long DD = static_cast<long long>(kD) * kD;
+  prepare(c, w, pb);
+  if (c.err == cudaSuccess)
+    c.err = cudaMemcpyAsync(w.A, A_key, H * DD * 4, cudaMemcpyDeviceToDevice, st);
+  // the key objective at A_key (its gradient only when it is the one asked for)
+  objective(c, w, pb, 0, which == 0, loss);
+  if (which == 1) {
+    if (c.err == cudaSuccess)
+      c.err = cudaMemcpyAsync(w.A, A_value, H * DD * 4, cudaMemcpyDeviceToDevice, st);
+    objective(c, w, pb, 1, true, loss);
+  }
+  if (c.err == cudaSuccess)
+    c.err = cudaMemcpyAsync(grad, w.gA, H * DD * 4, cudaMemcpyDeviceToDevice, st);
+  if (c.err == cudaSuccess) c.err = cudaStreamSynchronize(st);
+  return c.err == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+}  // namespace kvq

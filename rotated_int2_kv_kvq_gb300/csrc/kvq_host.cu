@@ -465,6 +465,54 @@ int kvq_profile_read(kvq_handle* h, double* total_ms, int* launches) {
   return KVQ_OK;
 }
 
+namespace {
+bool optr_shape_ok(int Hkv, int T, int Nq, int G, int Dm) {
+  return Hkv >= 1 && Hkv <= 64 && Nq >= 1 && T >= Nq && T <= (1 << 20) && G >= 1 && G <= 8 &&
+         Dm >= 1 && Dm <= 65536 && static_cast<long long>(Nq) * G <= 65535;
+}
+}  // namespace
+
+size_t kvq_optr_workspace_bytes(int num_kv_heads, int T, int Nq, int G, int Dm) {
+  if (!optr_shape_ok(num_kv_heads, T, Nq, G, Dm)) return 0;
+  return kvq::optr_workspace_bytes(num_kv_heads, T, Nq, G, Dm);
+}
+
+int kvq_optr_calibrate(int num_kv_heads, int T, int Nq, int G, int Dm, const uint16_t* K,
+                       const uint16_t* V, const uint16_t* Q, const float* W_O, const float* R0,
+                       const float* mu, float clip_k, float clip_v, float lambda_k, float lr,
+                       int steps, float sm_scale, float* R_out, float* history, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  if (!optr_shape_ok(num_kv_heads, T, Nq, G, Dm)) return KVQ_EINVAL;
+  if (!K || !V || !Q || !W_O || !R0 || !mu || !R_out || !history || !workspace) return KVQ_EINVAL;
+  if (!(clip_k > 0.f && clip_k <= 1.f) || !(clip_v > 0.f && clip_v <= 1.f)) return KVQ_EINVAL;
+  if (!(lr > 0.f) || !(lambda_k >= 0.f) || steps < 0 || steps > 100000) return KVQ_EINVAL;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return KVQ_EINVAL;
+  if (ws_bytes < kvq::optr_workspace_bytes(num_kv_heads, T, Nq, G, Dm)) return KVQ_ENOSPACE;
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(kDim));
+  return kvq::optr_calibrate(num_kv_heads, T, Nq, G, Dm, K, V, Q, W_O, R0, mu, clip_k, clip_v,
+                             lambda_k, lr, steps, scale, R_out, history, workspace, S(stream));
+}
+
+int kvq_optr_loss_grad(int num_kv_heads, int T, int Nq, int G, int Dm, const uint16_t* K,
+                       const uint16_t* V, const uint16_t* Q, const float* W_O, const float* R0,
+                       const float* mu, float clip_k, float clip_v, float lambda_k,
+                       float sm_scale, const float* A_key, const float* A_value, int which,
+                       float* loss, float* grad, void* workspace, size_t ws_bytes, void* stream) {
+  if (!optr_shape_ok(num_kv_heads, T, Nq, G, Dm)) return KVQ_EINVAL;
+  if (!K || !V || !Q || !W_O || !R0 || !mu || !A_key || !loss || !grad || !workspace)
+    return KVQ_EINVAL;
+  if (which != 0 && which != 1) return KVQ_EINVAL;
+  if (which == 1 && !A_value) return KVQ_EINVAL;
+  if (!(clip_k > 0.f && clip_k <= 1.f) || !(clip_v > 0.f && clip_v <= 1.f)) return KVQ_EINVAL;
+  if (!(lambda_k >= 0.f)) return KVQ_EINVAL;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return KVQ_EINVAL;
+  if (ws_bytes < kvq::optr_workspace_bytes(num_kv_heads, T, Nq, G, Dm)) return KVQ_ENOSPACE;
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(static_cast<float>(kDim));
+  return kvq::optr_loss_grad(num_kv_heads, T, Nq, G, Dm, K, V, Q, W_O, R0, mu, clip_k, clip_v,
+                             lambda_k, scale, A_key, A_value, which, loss, grad, workspace,
+                             S(stream));
+}
+
 const char* kvq_strerror(int code) {
   switch (code) {
     case KVQ_OK: return "ok";

@@ -100,6 +100,16 @@ cudaError_t launch_dequant(const uint8_t* pool, int num_pool_pages, const int32_
                            int max_pages, int Hkv, int seq, int start, int len, float* K_out,
                            float* V_out, uint32_t* status, cudaStream_t st);
 cudaError_t launch_transpose(const float* in, float* out, int count, cudaStream_t st);
+size_t optr_workspace_bytes(int H, int T, int Nq, int G, int Dm);
+int optr_calibrate(int H, int T, int Nq, int G, int Dm, const uint16_t* K, const uint16_t* V,
+                   const uint16_t* Q, const float* W, const float* R0, const float* mu,
+                   float clip_k, float clip_v, float lambda_k, float lr, int steps, float sm_scale,
+                   float* R_out, float* hist, void* workspace, cudaStream_t st);
+int optr_loss_grad(int H, int T, int Nq, int G, int Dm, const uint16_t* K, const uint16_t* V,
+                   const uint16_t* Q, const float* W, const float* R0, const float* mu,
+                   float clip_k, float clip_v, float lambda_k, float sm_scale, const float* A_key,
+                   const float* A_value, int which, float* loss, float* grad, void* workspace,
+                   cudaStream_t st);
 int decode_int2_ctas_per_sm();
 int decode_bf16_ctas_per_sm();
 int handle_device(const kvq_handle* h);   // CUDA device the handle was created on

@@ -42,6 +42,11 @@ SIGNATURES = {
     "kvq_bf16_workspace_bytes": ([_P, _I, _I], _SZ),
     "kvq_bf16_decode": ([_P, _P, _I, _P, _P, _I, _P, _I, _P, _P, _SZ, _I, _P], _I),
     "kvq_decode_static": ([_P, _P, _I, _P, _P, _I, _P, _I, _P, _I, _P], _I),
+    "kvq_optr_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
+    "kvq_optr_calibrate": ([_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, _I, _F, _P,
+                            _P, _P, _SZ, _P], _I),
+    "kvq_optr_loss_grad": ([_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, _P, _P, _I,
+                            _P, _P, _P, _SZ, _P], _I),
     "kvq_append_decode": ([_P, _P, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _SZ, _I, _P], _I),
     "kvq_decode_window": ([_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _SZ, _I,
                            _P], _I),
@@ -296,6 +301,54 @@ def kvq_profile_read(h: Handle):
     _check("kvq_profile_read", load_library().kvq_profile_read(h.ptr, ctypes.byref(ms),
                                                                ctypes.byref(n)))
     return float(ms.value), int(n.value)
+
+
+def kvq_optr_workspace_bytes(num_kv_heads, T, Nq, G, Dm) -> int:
+    return int(load_library().kvq_optr_workspace_bytes(int(num_kv_heads), int(T), int(Nq), int(G),
+                                                       int(Dm)))
+
+
+def kvq_optr_calibrate(K, V, Q, W_O, R0, mu, clip_k, clip_v, lambda_k=1.0, lr=1e-3, steps=80,
+                       sm_scale=0.0, workspace=None, stream=None):
+    """OptR calibration of the key and value rotations of every KV head.
+    K, V: bf16 [Hkv, T, 128]; Q: bf16 [Hkv, Nq, G, 128]; W_O: fp32 [Hkv, Dm, G*128];
+    R0: fp32 [2, Hkv, 128, 128]; mu: fp32 [Hkv, 128].  Returns (R fp32
+    [2, Hkv, 128, 128], history fp32 [2, steps + 1, Hkv]) as CUDA tensors."""
+    Hkv, T = int(K.shape[0]), int(K.shape[1])
+    Nq, G, Dm = int(Q.shape[1]), int(Q.shape[2]), int(W_O.shape[1])
+    R = torch.empty((2, Hkv, 128, 128), dtype=torch.float32, device=K.device)
+    hist = torch.empty((2, int(steps) + 1, Hkv), dtype=torch.float32, device=K.device)
+    if workspace is None:
+        workspace = torch.empty(kvq_optr_workspace_bytes(Hkv, T, Nq, G, Dm), dtype=torch.uint8,
+                                device=K.device)
+    _check("kvq_optr_calibrate", load_library().kvq_optr_calibrate(
+        Hkv, T, Nq, G, Dm, _ptr(K, _BF16, "K"), _ptr(V, _BF16, "V"), _ptr(Q, _BF16, "Q"),
+        _ptr(W_O, _F32, "W_O"), _ptr(R0, _F32, "R0"), _ptr(mu, _F32, "mu"), float(clip_k),
+        float(clip_v), float(lambda_k), float(lr), int(steps), float(sm_scale), _ptr(R, _F32, "R"),
+        _ptr(hist, _F32, "history"), _ptr(workspace, _U8, "workspace"), int(workspace.numel()),
+        _stream(stream)))
+    return R, hist
+
+
+def kvq_optr_loss_grad(K, V, Q, W_O, R0, mu, clip_k, clip_v, A_key, A_value=None, which=0,
+                       lambda_k=1.0, sm_scale=0.0, workspace=None, stream=None):
+    """Loss [Hkv] and d loss / dA [Hkv, 128, 128] of the key (which = 0) or value
+    (which = 1) calibration objective, as CUDA tensors."""
+    Hkv, T = int(K.shape[0]), int(K.shape[1])
+    Nq, G, Dm = int(Q.shape[1]), int(Q.shape[2]), int(W_O.shape[1])
+    loss = torch.empty(Hkv, dtype=torch.float32, device=K.device)
+    grad = torch.empty((Hkv, 128, 128), dtype=torch.float32, device=K.device)
+    if workspace is None:
+        workspace = torch.empty(kvq_optr_workspace_bytes(Hkv, T, Nq, G, Dm), dtype=torch.uint8,
+                                device=K.device)
+    _check("kvq_optr_loss_grad", load_library().kvq_optr_loss_grad(
+        Hkv, T, Nq, G, Dm, _ptr(K, _BF16, "K"), _ptr(V, _BF16, "V"), _ptr(Q, _BF16, "Q"),
+        _ptr(W_O, _F32, "W_O"), _ptr(R0, _F32, "R0"), _ptr(mu, _F32, "mu"), float(clip_k),
+        float(clip_v), float(lambda_k), float(sm_scale), _ptr(A_key, _F32, "A_key"),
+        _ptr(A_value, _F32, "A_value"), int(which), _ptr(loss, _F32, "loss"),
+        _ptr(grad, _F32, "grad"), _ptr(workspace, _U8, "workspace"), int(workspace.numel()),
+        _stream(stream)))
+    return loss, grad
 
 
 def kvq_strerror(code: int) -> str:

@@ -258,3 +258,27 @@ def effective_bits_window(ctx: int, sink: int = 64, recent: int = 256, group: in
     parameters" of the OptR page)."""
     n16 = min(ctx, sink + recent)
     return ((ctx - n16) * effective_bits(group) + n16 * 16.0) / ctx
+
+
+# ---- calibration traces (rotation calibration) -----------------------------------
+
+def calibration_traces(wl: Workload, layer: int = 0, T: int = 4096, Nq: int = 64,
+                       Dm: int = 4096, heads=None, seq: int = 0):
+    """Synthetic calibration chunk of one sequence for the KV heads `heads`
+    (default all): keys and values at positions [0, T) (the token recipe above),
+    the queries of the last Nq positions (N(0, 1), bf16) and a Gaussian stand-in
+    for the KV head's slice of the output projection, N(0, 1/(H*D)).
+    Returns (K bits [Hs, T, D], V bits [Hs, T, D], Q bits [Hs, Nq, G, D],
+    W_O fp32 [Hs, Dm, G*D])."""
+    heads = list(range(wl.num_kv_heads)) if heads is None else list(heads)
+    G = wl.num_heads // wl.num_kv_heads
+    Kt = tokens(wl, layer, seq, 0, 0, T)
+    Vt = tokens(wl, layer, seq, 1, 0, T)
+    g = _rng(wl.seed, 23, layer, seq)
+    q = to_bf16_bits(g.standard_normal((Nq, wl.num_heads, D), dtype=np.float32))
+    w = g.standard_normal((wl.num_kv_heads, Dm, G * D), dtype=np.float32) / np.float32(
+        np.sqrt(wl.num_heads * D))
+    K = np.ascontiguousarray(Kt[:, heads].transpose(1, 0, 2))
+    V = np.ascontiguousarray(Vt[:, heads].transpose(1, 0, 2))
+    Q = np.ascontiguousarray(np.stack([q[:, h * G:(h + 1) * G] for h in heads]))
+    return K, V, Q, np.ascontiguousarray(w[heads])
