@@ -654,12 +654,96 @@ def run_full_stack(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# OptR rotation calibration of one layer (off the decode path)
+# ---------------------------------------------------------------------------
+
+OPTR_METRIC = "OptR calibration of one layer (8 KV heads, 80 + 80 Adam steps): seconds"
+
+
+def optr_flops_per_step(T, Nq, G, Dm, D=128):
+    """Algorithmic fp32 flops of one key step plus one value step of one KV
+    head with gradient: the objective's contractions (rotations, logits,
+    attention products, post-W_O error and their transposes), not counting the
+    matrix exponentials."""
+    QG = Nq * G
+    key = (2 * T * D * D) * 5 + (2 * QG * T * D) * 4 + (2 * Nq * G * D * Dm) * 2
+    value = (2 * T * D * D) * 5 + (2 * QG * T * D) * 3 + (2 * Nq * G * D * Dm) * 2
+    return key + value
+
+
+def run_optr(args):
+    import torch
+
+    from rotated_int2_kv_kvq_gb300 import kvq as K
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    K.load_library()
+    wl = W.WORKLOADS["qwen3_8b_32k"]
+    T, Nq, Dm, steps = 4096, 64, 4096, 80
+    H, G = wl.num_kv_heads, wl.num_heads // wl.num_kv_heads
+    Kb, Vb, Qb, Wo = W.calibration_traces(wl, 0, T, Nq, Dm)
+    d16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    inputs = (d16(Kb), d16(Vb), d16(Qb), torch.from_numpy(Wo).cuda(),
+              torch.from_numpy(W.rotations(wl)).cuda(), torch.from_numpy(W.key_mean(wl)).cuda(),
+              wl.clip_k, wl.clip_v)
+    ws = torch.empty(K.kvq_optr_workspace_bytes(H, T, Nq, G, Dm), dtype=torch.uint8, device="cuda")
+    for _ in range(max(1, args.warmup)):
+        K.kvq_optr_calibrate(*inputs, steps=2, workspace=ws)
+    torch.cuda.synchronize()
+    reps = max(1, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        R, hist = K.kvq_optr_calibrate(*inputs, steps=steps, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / reps
+    h = hist.cpu().numpy()
+    flops = optr_flops_per_step(T, Nq, G, Dm) * steps * H
+    nominal = 152 * 128 * 2 * 2.07e9 / 1e12       # fp32 FMA, TFLOP/s
+    cpu = None
+    if not args.no_cpu:
+        from oracle import optr
+
+        f = lambda b: W.bf16_bits_to_float(b).astype(np.float64)
+        Wh = Wo.reshape(H, Dm, G, 128).transpose(0, 2, 1, 3)
+        R0 = W.rotations(wl).astype(np.float64)
+        mu = W.key_mean(wl).astype(np.float64)
+        n_cpu = 2
+        t0 = time.perf_counter()
+        optr.calibrate(R0[0, 0], R0[1, 0], f(Kb[0]), f(Vb[0]), f(Qb[0]), Wh[0], mu[0], wl.clip_k,
+                       wl.clip_v, steps=n_cpu)
+        el = time.perf_counter() - t0
+        cpu_layer_s = el / n_cpu * steps * H
+        cpu = {"value": cpu_layer_s, "unit": "s per layer (extrapolated)", "cores": 1,
+               "kind": "oracle",
+               "sample": f"float64 oracle, KV head 0: {n_cpu} key + {n_cpu} value steps in "
+                         f"{el:.1f} s, scaled to {steps} + {steps} steps x {H} heads"}
+    line = {
+        "metric": OPTR_METRIC, "value": sec, "unit": "s", "n_gpus": 1, "steps": reps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3 / (2 * steps), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "optr_calib", "kv_heads": H, "group": G, "calib_tokens": T,
+                   "query_positions": Nq, "d_model": Dm, "adam_steps": steps, "lr": 1e-3},
+        "roofline": {"bound": "alu", "achieved": flops / sec / 1e12, "peak": nominal,
+                     "unit": "TFLOP/s", "frac": flops / sec / 1e12 / nominal, "traffic": None,
+                     "peak_kind": "fp32 FMA nominal: 152 SMs x 128 lanes x 2 x 2.07 GHz"},
+        "losses": {"key": [float(h[0, 0].mean()), float(h[0, -1].mean())],
+                   "value": [float(h[1, 0].mean()), float(h[1, -1].mean())]},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "full_stack_36l":
         run_full_stack(args)
+    elif args.workload == "optr_calib":
+        run_optr(args)
     else:
         run_ours(args)
 
