@@ -207,9 +207,10 @@ def oracle_step(wl, s):
                         [[0, h] for h in range(s["G"])], R=s["R"])
 
 
-def cpu_oracle_rate(wl, min_seconds=10.0, max_steps=None, warmup=0):
+def cpu_oracle_rate(wl, min_seconds=10.0, max_steps=None, warmup=0, max_seconds=None):
     """Cache GB/s of the oracle on (sequence 0, KV head 0): each step reads that
-    head's whole context once for its G query heads."""
+    head's whole context once for its G query heads.  Stops after max_steps
+    steps, or after max_seconds if that comes first."""
     s = oracle_sample_setup(wl)
     for _ in range(warmup):
         oracle_step(wl, s)
@@ -220,6 +221,8 @@ def cpu_oracle_rate(wl, min_seconds=10.0, max_steps=None, warmup=0):
         el = time.perf_counter() - t0
         if (max_steps is not None and n >= max_steps) or (max_steps is None and el >= min_seconds):
             break
+        if max_seconds is not None and el >= max_seconds:
+            break
     bytes_per_step = wl.ctx * W.cache_bytes_per_token_head("int2")
     return bytes_per_step * n / el / 1e9, n, el
 
@@ -229,7 +232,9 @@ def run_reference(args):
     if rank != 0:
         return
     wl = W.WORKLOADS[args.workload]
-    gbs, n, el = cpu_oracle_rate(wl, max_steps=max(1, args.steps), warmup=max(0, args.warmup))
+    # at most about four minutes of oracle work: the line reports the steps timed
+    gbs, n, el = cpu_oracle_rate(wl, max_steps=max(1, args.steps), warmup=min(max(0, args.warmup), 3),
+                                 max_seconds=240.0)
     sample = (f"float64 oracle, sequence 0 / KV head 0 of {wl.name}: per step re-quantise one "
               f"token and decode {wl.num_heads // wl.num_kv_heads} query heads over {wl.ctx} "
               f"tokens ({n} steps, {el:.1f} s)")
