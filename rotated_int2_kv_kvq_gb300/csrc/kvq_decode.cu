@@ -165,15 +165,13 @@ __device__ __forceinline__ void qprep_tail(const DecodeArgs& a, float (&qs)[kMax
 }
 
 // One CTA per (sequence, KV head); thread i computes element i of the G
-// rotated query vectors.
-__global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* __restrict__ RK,
-                                                    const float* __restrict__ mu,
-                                                    float log2_scale) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  QprepSmem& sm = *reinterpret_cast<QprepSmem*>(smem_raw);
-  const int b = blockIdx.x, kv = blockIdx.y, i = threadIdx.x;
+// rotated query vectors, one fmaf chain over j = 0..127 each, with the query
+// elements read four j at a time (one broadcast load per vector).
+__device__ __forceinline__ void qprep_cta(const DecodeArgs& a, const float* __restrict__ RK,
+                                          const float* __restrict__ mu, float log2_scale,
+                                          QprepSmem& sm, int b, int kv) {
+  const int i = threadIdx.x;
   const int G = a.G;
-  griddep_launch_dependents();
   const bool rotate = RK != nullptr;
   const uint32_t bar = smem_u32(&sm.bar);
   if (rotate && i == 0) {
@@ -200,11 +198,19 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
       return;
     }
     float acc[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 8
-    for (int j = 0; j < kDim; ++j) {
-      const float r = sm.R[j * kDim + i];
+#pragma unroll 2
+    for (int j0 = 0; j0 < kDim; j0 += 4) {
+      float r[4];
 #pragma unroll
-      for (int h = 0; h < kMaxG; ++h) acc[h] = fmaf(sm.qs[h][j], r, acc[h]);
+      for (int u = 0; u < 4; ++u) r[u] = sm.R[(j0 + u) * kDim + i];
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        const float4 x = *reinterpret_cast<const float4*>(&sm.qs[h][j0]);
+        acc[h] = fmaf(x.x, r[0], acc[h]);
+        acc[h] = fmaf(x.y, r[1], acc[h]);
+        acc[h] = fmaf(x.z, r[2], acc[h]);
+        acc[h] = fmaf(x.w, r[3], acc[h]);
+      }
     }
 #pragma unroll
     for (int h = 0; h < kMaxG; ++h) sm.qr[h][i] = acc[h];
@@ -216,36 +222,50 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
   qprep_tail(a, sm.qs, sm.qr, sm.e, mu, log2_scale, b, kv);
 }
 
+__global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* __restrict__ RK,
+                                                    const float* __restrict__ mu,
+                                                    float log2_scale) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  griddep_launch_dependents();
+  qprep_cta(a, RK, mu, log2_scale, *reinterpret_cast<QprepSmem*>(smem_raw), blockIdx.x, blockIdx.y);
+}
+
 // ---------------------------------------------------------------------------
-// Append + query preparation in one kernel (kvq_append_decode): CTA (b, kv)
-// quantises sequence b's new token (position seq_lens[b] - 1) for KV head kv
-// into its page record, with exactly the fp32 operation sequence of the append
-// kernel (centre, fmaf chain over j = 0..127 in order, max/min, clip, fp16
-// scale/zero, rint codes), and then prepares the rotated query like
-// qprep_kernel.  One pass over j serves all chains: the key and value
-// rotations and the G query rotations.  R_K and R_V are bulk-copied before
-// the kernel waits for its predecessor; the token, q and the tables are read,
-// and the pool written, only after that wait.
+// Append + query preparation in one launch (kvq_append_decode), CTA (b, kv,
+// role).  Role 0 quantises sequence b's new token (position seq_lens[b] - 1)
+// for KV head kv into its page record, with exactly the fp32 operation
+// sequence of the append kernel (centre, fmaf chain over j = 0..127 in order,
+// max/min, clip, fp16 scale/zero, rint codes); role 1 prepares the rotated
+// query exactly like qprep_kernel.  The two halves share nothing, so they run
+// side by side on separate SMs.  Rotation matrices are bulk-copied before the
+// CTA waits for its predecessor; the token, q and the tables are read, and the
+// pool written, only after that wait.
 // ---------------------------------------------------------------------------
 struct StepSmem {
   float RK[kDim * kDim];
   float RV[kDim * kDim];
-  float qs[kMaxG][kDim];
-  float qr[kMaxG][kDim];
-  float x[2][kDim];          // centred key, value
-  float red[2][2][4];        // [K|V][max|min][warp]
+  alignas(16) float x[2][kDim];   // centred key, value
+  float red[2][2][4];             // [K|V][max|min][warp]
   uint8_t codes[2][kDim];
-  int e[kMaxG];
   uint64_t bar;
+};
+
+union StepPrepSmem {
+  StepSmem append;
+  QprepSmem query;
 };
 
 __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs st) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  StepSmem& sm = *reinterpret_cast<StepSmem*>(smem_raw);
   const int b = blockIdx.x, kv = blockIdx.y, i = threadIdx.x;
-  const int warp = i >> 5, lane = i & 31;
-  const int G = a.G;
   griddep_launch_dependents();
+  if (blockIdx.z == 1) {
+    qprep_cta(a, st.q_rotated ? nullptr : st.RK, st.mu, a.log2_scale,
+              reinterpret_cast<StepPrepSmem*>(smem_raw)->query, b, kv);
+    return;
+  }
+  StepSmem& sm = reinterpret_cast<StepPrepSmem*>(smem_raw)->append;
+  const int warp = i >> 5, lane = i & 31;
   const uint32_t bar = smem_u32(&sm.bar);
   if (i == 0) {
     mbar_init(bar, 1);
@@ -255,8 +275,12 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
     bulk_g2s(smem_u32(sm.RV), st.RV + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
   }
   __syncthreads();
-  griddep_wait();      // token, q and tables may come from preceding kernels
+  griddep_wait();      // token and tables may come from preceding kernels
 
+  // the token first, so that its loads overlap the table lookups below
+  const size_t src = (static_cast<size_t>(b) * a.Hkv + kv) * kDim + i;
+  const uint16_t kbits = st.K[src], vbits = st.V[src];
+  const float mui = st.mu[static_cast<size_t>(kv) * kDim + i];
   // the record slot of the new token, or none
   const int seq_len = a.seq_lens[b];
   const int p = seq_len - 1;
@@ -270,39 +294,28 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
     else if (i == 0)
       atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
   }
-  {
-    const size_t src = (static_cast<size_t>(b) * a.Hkv + kv) * kDim + i;
-    const float k = __uint_as_float(static_cast<uint32_t>(st.K[src]) << 16);
-    sm.x[0][i] = __fsub_rn(k, st.mu[static_cast<size_t>(kv) * kDim + i]);
-    sm.x[1][i] = __uint_as_float(static_cast<uint32_t>(st.V[src]) << 16);
-  }
-#pragma unroll
-  for (int h = 0; h < kMaxG; ++h) {
-    float x = 0.0f;
-    if (h < G) {
-      const uint16_t bits = a.q[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + i];
-      x = __uint_as_float(static_cast<uint32_t>(bits) << 16);
-    }
-    sm.qs[h][i] = x;
-  }
+  sm.x[0][i] = __fsub_rn(__uint_as_float(static_cast<uint32_t>(kbits) << 16), mui);
+  sm.x[1][i] = __uint_as_float(static_cast<uint32_t>(vbits) << 16);
   const bool ok = mbar_wait_bounded(bar, 0);
   if (__syncthreads_or(!ok)) {
     if (i == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
     return;
   }
-  // r_i = fmaf chains over j = 0..127 (keys, values, G queries)
+  // r_i = fmaf chains over j = 0..127, the vector elements read four j at a time
   float rk = 0.0f, rv = 0.0f;
-  float acc[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-  for (int j = 0; j < kDim; ++j) {
-    const float ak = sm.RK[j * kDim + i];
-    rk = fmaf(sm.x[0][j], ak, rk);
-    rv = fmaf(sm.x[1][j], sm.RV[j * kDim + i], rv);
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h) acc[h] = fmaf(sm.qs[h][j], ak, acc[h]);
+#pragma unroll 2
+  for (int j0 = 0; j0 < kDim; j0 += 4) {
+    const float4 xk = *reinterpret_cast<const float4*>(&sm.x[0][j0]);
+    const float4 xv = *reinterpret_cast<const float4*>(&sm.x[1][j0]);
+    rk = fmaf(xk.x, sm.RK[(j0 + 0) * kDim + i], rk);
+    rv = fmaf(xv.x, sm.RV[(j0 + 0) * kDim + i], rv);
+    rk = fmaf(xk.y, sm.RK[(j0 + 1) * kDim + i], rk);
+    rv = fmaf(xv.y, sm.RV[(j0 + 1) * kDim + i], rv);
+    rk = fmaf(xk.z, sm.RK[(j0 + 2) * kDim + i], rk);
+    rv = fmaf(xv.z, sm.RV[(j0 + 2) * kDim + i], rv);
+    rk = fmaf(xk.w, sm.RK[(j0 + 3) * kDim + i], rk);
+    rv = fmaf(xv.w, sm.RV[(j0 + 3) * kDim + i], rv);
   }
-#pragma unroll
-  for (int h = 0; h < kMaxG; ++h) sm.qr[h][i] = st.q_rotated ? sm.qs[h][i] : acc[h];
 
   // max / min of the rotated key and value over the whole vector
   {
@@ -375,7 +388,6 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
           which ? szw[1] : szw[0];
     }
   }
-  qprep_tail(a, sm.qs, sm.qr, sm.e, st.mu, a.log2_scale, b, kv);
 }
 
 // ---------------------------------------------------------------------------
@@ -573,7 +585,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int split = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
-  const int HPC = a.hpc, GPH = kW / HPC, PPS = 2 * GPH;
+  const int HPC = a.hpc, GPH = kW / HPC;
   const int hl = warp / GPH, gi = warp % GPH;
   const int kv = hg * HPC + hl;
 
@@ -695,11 +707,36 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     ws.l_run += __shfl_xor_sync(0xffffffffu, ws.l_run, off);
     ws.z_run += __shfl_xor_sync(0xffffffffu, ws.z_run, off);
   }
+  // undo the code scale (2^-17 for even m-blocks, 2^-15 for odd ones) and the
+  // weight scale 2^(14 - kLazy) = 2^6; the residual column carries a further 2^11
+  constexpr float kInvEven = 2048.0f;   // 2^(17 - 6)
+  constexpr float kInvOdd = 512.0f;     // 2^(15 - 6)
+  if (GPH == 1) {
+    // One warp per KV head: its (m, l, o) is the split partial as it stands,
+    // stored straight from registers (a merge through shared memory would be a
+    // chain of dependent loads on one warp per scheduler).  Same values as the
+    // merge below with a single term: an empty head gives (-inf, 0, 0), and
+    // "+ 0" turns a -0 into the +0 that merge's fmaf(1, o, 0) gives.
+    if (t < a.G) {
+      float* p = a.part + ((static_cast<size_t>(b) * a.H + kv * a.G + t) * a.splits + split) *
+                              kPartStride;
+      const bool any = ws.m_run > -INFINITY;
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) {
+        const float inv = (mb & 1) ? kInvOdd : kInvEven;
+        const float o0 = fmaf(fmaf(ws.acc[mb][1], 1.0f / 2048.0f, ws.acc[mb][0]), inv, ws.z_run);
+        const float o1 = fmaf(fmaf(ws.acc[mb][3], 1.0f / 2048.0f, ws.acc[mb][2]), inv, ws.z_run);
+        p[4 + 16 * mb + g] = any ? o0 + 0.0f : 0.0f;
+        p[4 + 16 * mb + g + 8] = any ? o1 + 0.0f : 0.0f;
+      }
+      if (g == 0) {
+        p[0] = ws.m_run;
+        p[1] = any ? ws.l_run : 0.0f;
+      }
+    }
+    return;
+  }
   if (t < a.G) {
-    // undo the code scale (2^-17 for even m-blocks, 2^-15 for odd ones) and the
-    // weight scale 2^(14 - kLazy) = 2^6; the residual column carries a further 2^11
-    constexpr float kInvEven = 2048.0f;   // 2^(17 - 6)
-    constexpr float kInvOdd = 512.0f;     // 2^(15 - 6)
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
       const float inv = (mb & 1) ? kInvOdd : kInvEven;
@@ -990,11 +1027,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodeAr
 // ---------------------------------------------------------------------------
 constexpr int kCombineThreads = kMaxG * kDim;   // 512
 constexpr int kCombineWarps = kCombineThreads / 32;
+static_assert(kCombineThreads == 4 * kDim, "the basis change splits j into four quarters");
 
 struct CombineSmem {
   float Rt[kDim * kDim];      // R_V^T, or R_V for a rotated-basis output with a window
   float w[kMaxG][kMaxSplits];
-  float o[kMaxG][kDim];
+  alignas(16) float ot[kDim][kMaxG];   // the G outputs, element-major
+  float red[4][kMaxG][kDim];           // per-quarter sums of the basis change
   float linv[kMaxG];
   float ww[kMaxG];            // weight of the window part
   uint64_t bar;
@@ -1126,23 +1165,33 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(DecodeArgs a) 
   float owin = 0.0f;
   if constexpr (kWindow) owin = window_partial(a, ws, b, kv);
   griddep_wait();       // the partials come from the decode kernel
+  // Thread (h, d) loads element d of its head's first kPre split partials now,
+  // so that these loads and the (m, l) loads below share one round trip.
+  constexpr int kPre = 32;
+  const float* parts_h = a.part + (static_cast<size_t>(b) * a.H + kv * G + h) * S * kPartStride;
+  float v[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) v[u] = (h < G && u < S) ? parts_h[u * kPartStride + 4 + d] : 0.0f;
   if (kWindow) __syncthreads();   // ws.M / ws.L
   if (warp < G) {
     const float* parts = a.part + (static_cast<size_t>(b) * a.H + kv * G + warp) * S * kPartStride;
     // INT2 logits were taken against centred keys: with a window, add q.mu back
     const float qmu =
         kWindow ? a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * kQMeta + 8 + warp] : 0.0f;
-    float M = -INFINITY;
-    for (int j = lane; j < S; j += 32) M = fmaxf(M, parts[j * kPartStride]);
+    const float m0 = lane < S ? parts[lane * kPartStride] : -INFINITY;
+    const float l0 = lane < S ? parts[lane * kPartStride + 1] : 0.0f;
+    float M = m0;
+    for (int j = lane + 32; j < S; j += 32) M = fmaxf(M, parts[j * kPartStride]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     if (kWindow) M = fmaxf(M + qmu, ws.M[warp]);
     float L = 0.0f;
     for (int j = lane; j < S; j += 32) {
-      const float mj = parts[j * kPartStride];
+      const float mj = j == lane ? m0 : parts[j * kPartStride];
+      const float lj = j == lane ? l0 : parts[j * kPartStride + 1];
       const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj + qmu - M);
       sm.w[warp][j] = w;
-      L = fmaf(w, parts[j * kPartStride + 1], L);
+      L = fmaf(w, lj, L);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
@@ -1158,22 +1207,46 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(DecodeArgs a) 
   __syncthreads();
   float o = 0.0f;
   if (h < G) {
-    const float* parts = a.part + (static_cast<size_t>(b) * a.H + kv * G + h) * S * kPartStride;
-#pragma unroll 8
-    for (int j = 0; j < S; ++j) o = fmaf(sm.w[h][j], parts[j * kPartStride + 4 + d], o);
+    // splits in order: the preloaded ones, then the rest kPre at a time
+#pragma unroll
+    for (int u = 0; u < kPre; ++u)
+      if (u < S) o = fmaf(sm.w[h][u], v[u], o);
+    for (int j0 = kPre; j0 < S; j0 += kPre) {
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) v[u] = j0 + u < S ? parts_h[(j0 + u) * kPartStride + 4 + d] : 0.0f;
+#pragma unroll
+      for (int u = 0; u < kPre; ++u)
+        if (j0 + u < S) o = fmaf(sm.w[h][j0 + u], v[u], o);
+    }
     if (!kWindow) o *= sm.linv[h];
   }
   if (stage) {
-    // y R for the part that changes basis
-    sm.o[h][d] = (kWindow && !a.rotate_out) ? owin : o;
+    // y R for the part that changes basis; thread (q, d) sums j in quarter q
+    // for every head, so each element of the matrix is read once per CTA
+    sm.ot[d][h] = (kWindow && !a.rotate_out) ? owin : o;
     const bool ok = mbar_wait_bounded(bar, 0);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
       return;
     }
-    float r = 0.0f;
+    {
+      const int q = h;
+      float r4[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 8
-    for (int j = 0; j < kDim; ++j) r = fmaf(sm.o[h][j], sm.Rt[j * kDim + d], r);
+      for (int jj = 0; jj < kDim / 4; ++jj) {
+        const int j = q * (kDim / 4) + jj;
+        const float4 ov = *reinterpret_cast<const float4*>(sm.ot[j]);
+        const float rt = sm.Rt[j * kDim + d];
+        r4[0] = fmaf(ov.x, rt, r4[0]);
+        r4[1] = fmaf(ov.y, rt, r4[1]);
+        r4[2] = fmaf(ov.z, rt, r4[2]);
+        r4[3] = fmaf(ov.w, rt, r4[3]);
+      }
+#pragma unroll
+      for (int hh = 0; hh < kMaxG; ++hh) sm.red[q][hh][d] = r4[hh];
+    }
+    __syncthreads();
+    const float r = (sm.red[0][h][d] + sm.red[1][h][d]) + (sm.red[2][h][d] + sm.red[3][h][d]);
     if (!kWindow) o = r;
     else if (h < G) o = (a.rotate_out ? fmaf(sm.ww[h], owin, r) : fmaf(sm.ww[h], r, o)) * sm.linv[h];
   }
@@ -1276,10 +1349,10 @@ cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, const float* mu, 
 }
 
 cudaError_t launch_step_prep(const DecodeArgs& a, const StepArgs& sa, cudaStream_t st) {
-  cudaError_t e = set_smem_attr<StepSmem>(step_prep_kernel);
+  cudaError_t e = set_smem_attr<StepPrepSmem>(step_prep_kernel);
   if (e != cudaSuccess) return e;
-  e = launch_dependent(step_prep_kernel, dim3(a.batch, a.Hkv), dim3(128), sizeof(StepSmem), st,
-                       a, sa);
+  e = launch_dependent(step_prep_kernel, dim3(a.batch, a.Hkv, 2), dim3(128), sizeof(StepPrepSmem),
+                       st, a, sa);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
