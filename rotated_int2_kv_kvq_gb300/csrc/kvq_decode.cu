@@ -595,19 +595,30 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   }
   griddep_wait();      // inputs (pool, tables, rotated queries) come from predecessors
 
+  // INT2 tokens: positions [lo, hi); with a BF16 window the first win_sink and
+  // the last win_recent positions are left to the window pass.
+  const int lo = a.win_sink;
+  const int p0 = max(split * a.chunk_pages, lo / kPage);
+  const int32_t* ptab = a.page_table + static_cast<size_t>(b) * a.max_pages;
+  // The first sub-chunk's page ids are loaded together with seq_len (one round
+  // trip instead of two): every entry of the split's chunk inside the table,
+  // of which those below the sequence's end are used.
+  constexpr int kIdsPerThread = kMaxIds / (kW * 32);
+  const int nspec = min(kMaxIds, max(0, min(split * a.chunk_pages + a.chunk_pages, a.max_pages) - p0));
+  int spec[kIdsPerThread];
+#pragma unroll
+  for (int r = 0; r < kIdsPerThread; ++r) {
+    const int i = tid + r * kW * 32;
+    spec[r] = i < nspec ? ptab[p0 + i] : -1;
+  }
   int seq_len = a.seq_lens[b];
   if (seq_len < 0 || seq_len > a.max_pages * kPage) {
     if (tid == 0 && split == 0 && hg == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
     seq_len = 0;
   }
-  // INT2 tokens: positions [lo, hi); with a BF16 window the first win_sink and
-  // the last win_recent positions are left to the window pass.
-  const int lo = a.win_sink;
   const int hi = max(seq_len - a.win_recent, 0);
-  const int n_pages = (hi + kPage - 1) / kPage;
-  const int p0 = max(split * a.chunk_pages, lo / kPage);
+  const int n_pages = (hi + kPage - 1) / kPage;      // <= max_pages, so npg <= nspec
   const int npg = max(0, min(split * a.chunk_pages + a.chunk_pages, n_pages) - p0);
-  const int32_t* ptab = a.page_table + static_cast<size_t>(b) * a.max_pages;
 
   // B fragments of the rotated query and the head's logit constants
   uint32_t qf[16];
@@ -637,12 +648,16 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   for (int sub = 0; sub < npg && !timed_out; sub += kMaxIds) {
     const int nsub = min(kMaxIds, npg - sub);
     bool ids_ok = true;
-    for (int i = tid; i < nsub; i += kW * 32) {
-      const int id = ptab[p0 + sub + i];
-      const bool ok = id >= 0 && id < a.num_pool_pages;
-      if (!ok) atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
-      sm.ids[i] = ok ? id : -1;
-      ids_ok = ids_ok && ok;
+#pragma unroll
+    for (int r = 0; r < kIdsPerThread; ++r) {
+      const int i = tid + r * kW * 32;
+      if (i < nsub) {
+        const int id = sub == 0 ? spec[r] : ptab[p0 + sub + i];
+        const bool ok = id >= 0 && id < a.num_pool_pages;
+        if (!ok) atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+        sm.ids[i] = ok ? id : -1;
+        ids_ok = ids_ok && ok;
+      }
     }
     const bool all_ids_ok = __syncthreads_and(ids_ok);
     const int npw = nsub > gi ? (nsub - gi + GPH - 1) / GPH : 0;   // this warp's pages
