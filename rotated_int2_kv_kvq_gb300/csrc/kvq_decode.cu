@@ -27,8 +27,8 @@
 //   scores  S[token][col] = Kcode[token][dim] . B[dim][col]     (M = 16 tokens)
 //   values  O^T[dim][col] += Vcode^T[dim][token] . P[token][col] (M = 16 dims)
 // with col = 2*head + {hi, lo}: each operand that is not a code is split into an
-// fp16 high part and an fp16 residual (scaled by 2^11 so it stays a normal
-// number), which keeps products at fp32 accuracy.  Codes become fp16 operands
+// fp16 high part and an fp16 residual (the query's scaled by 2^11 so it stays a
+// normal number), which keeps products at fp32 accuracy.  Codes become fp16 operands
 // with shifts and ANDs: a 2-bit field moved to bits 9-10 (or 7-8) of a 16-bit
 // half is the fp16 number code * 2^-15 (or code * 2^-17), exactly; the powers of
 // two are folded into the query operands and removed in the value epilogue.
@@ -438,14 +438,31 @@ __device__ __forceinline__ void page_values(const uint4& vw, uint32_t pb0, uint3
 #undef KVQ_VSTEP
 }
 
+// P - float(h) for the two halves h of X, each in one mixed-precision fma
+// (f16 x f16 + f32: h * -1 + P, the f16 operands widened exactly).
+__device__ __forceinline__ void half2_residuals(uint32_t X, float P0, float P1, float& r0,
+                                                float& r1) {
+  asm("{\n\t.reg .f16 a, b, m;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "mov.b16 m, 0xBC00;\n\t"
+      "fma.rn.f32.f16 %0, a, m, %3;\n\t"
+      "fma.rn.f32.f16 %1, b, m, %4;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "r"(X), "f"(P0), "f"(P1));
+}
+
 // B fragments of the value product from this lane's weights of tokens g and
-// g+8 (head t): column 2*head holds the fp16 weight, column 2*head+1 the
-// residual scaled by 2^11.  Lane (g, t) needs head g>>1, tokens 2t, 2t+1,
-// 2t+8, 2t+9, held by lanes 4*(2t) + (g>>1) and 4*(2t+1) + (g>>1).
+// g+8 (head t): column 2*head holds the fp16 weight, column 2*head+1 the fp16
+// residual P - fp16(P) (at most 2^-11 P; for weights below 2^-3 it is an fp16
+// subnormal, a negligible loss next to the weight itself).  Lane (g, t) needs
+// head g>>1, tokens 2t, 2t+1, 2t+8, 2t+9, held by lanes 4*(2t) + (g>>1) and
+// 4*(2t+1) + (g>>1).
 __device__ __forceinline__ void weights_to_b(float P0, float P1, int g, int t, uint32_t& pb0,
                                              uint32_t& pb1) {
   const uint32_t X = pack_half2(P0, P1);
-  const uint32_t Y = pack_half2((P0 - half_lo(X)) * 2048.0f, (P1 - half_hi(X)) * 2048.0f);
+  float r0, r1;
+  half2_residuals(X, P0, P1, r0, r1);
+  const uint32_t Y = pack_half2(r0, r1);
   const int src0 = 4 * (2 * t) + (g >> 1);
   const uint32_t xa = __shfl_sync(0xffffffffu, X, src0);
   const uint32_t ya = __shfl_sync(0xffffffffu, Y, src0);
@@ -494,18 +511,29 @@ __device__ __forceinline__ void process_pair(WarpState& st, const uint32_t (&qf)
                                  zeta * half_hi(mtb.y)) : -INFINITY;
 
     // ---- online softmax.  The value weights P = p * s_v feed fp16 operands, so
-    // the running max m is kept over lv = logit + log2(s_v) and raised only when
-    // some lv exceeds m + kLazy: then p * s_v <= 2^kLazy for every token seen and
-    // P * 2^(14 - kLazy) stays below 2^14.  p = 2^(logit - m) itself may be large
-    // (at most 2^(kLazy + 24)); it is only summed in fp32.
+    // the running max m is kept over lv = logit + log2(max(s_v, 2^-24)) and
+    // raised only when some lv exceeds m + kLazy: then p * s_v <= 2^kLazy for
+    // every token seen and P * 2^(14 - kLazy) stays below 2^14.  p = 2^(logit - m)
+    // itself may be large (at most 2^(kLazy + 24)); it is only summed in fp32.
+    // The test lv > m + kLazy is taken as p * max(s_v, 2^-24) > 2^kLazy on the
+    // weights against the current m (true for p = inf when m is still -inf),
+    // so the logarithms are computed only on the rare stages that raise m.
     const float sva0 = half_lo(mta.z), sva1 = half_lo(mta.w);
     const float svb0 = half_lo(mtb.z), svb1 = half_lo(mtb.w);
-    const float lva0 = la0 + fmaxf(fast_log2(sva0), -24.0f);
-    const float lva1 = la1 + fmaxf(fast_log2(sva1), -24.0f);
-    const float lvb0 = lb0 + fmaxf(fast_log2(svb0), -24.0f);
-    const float lvb1 = lb1 + fmaxf(fast_log2(svb1), -24.0f);
-    const float lmax = fmaxf(fmaxf(lva0, lva1), fmaxf(lvb0, lvb1));
-    if (__any_sync(0xffffffffu, lmax > m_run + kLazy)) {
+    float pa0 = va0 ? fast_exp2(la0 - m_run) : 0.0f;
+    float pa1 = va1 ? fast_exp2(la1 - m_run) : 0.0f;
+    float pb0v = vb0 ? fast_exp2(lb0 - m_run) : 0.0f;
+    float pb1v = vb1 ? fast_exp2(lb1 - m_run) : 0.0f;
+    constexpr float kSvMin = 0x1p-24f;
+    const float cmax = fmaxf(fmaxf(pa0 * fmaxf(sva0, kSvMin), pa1 * fmaxf(sva1, kSvMin)),
+                             fmaxf(pb0v * fmaxf(svb0, kSvMin), pb1v * fmaxf(svb1, kSvMin)));
+    if (__any_sync(0xffffffffu, !(cmax <= 0x1p8f))) {
+      static_assert(kLazy == 8.0f, "the weight test above uses 2^kLazy = 2^8");
+      const float lva0 = la0 + fmaxf(fast_log2(sva0), -24.0f);
+      const float lva1 = la1 + fmaxf(fast_log2(sva1), -24.0f);
+      const float lvb0 = lb0 + fmaxf(fast_log2(svb0), -24.0f);
+      const float lvb1 = lb1 + fmaxf(fast_log2(svb1), -24.0f);
+      const float lmax = fmaxf(fmaxf(lva0, lva1), fmaxf(lvb0, lvb1));
       float pm = lmax;
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
@@ -520,11 +548,11 @@ __device__ __forceinline__ void process_pair(WarpState& st, const uint32_t (&qf)
         z_run *= f;
         m_run = pm;
       }
+      pa0 = va0 ? fast_exp2(la0 - m_run) : 0.0f;
+      pa1 = va1 ? fast_exp2(la1 - m_run) : 0.0f;
+      pb0v = vb0 ? fast_exp2(lb0 - m_run) : 0.0f;
+      pb1v = vb1 ? fast_exp2(lb1 - m_run) : 0.0f;
     }
-    const float pa0 = va0 ? fast_exp2(la0 - m_run) : 0.0f;
-    const float pa1 = va1 ? fast_exp2(la1 - m_run) : 0.0f;
-    const float pb0v = vb0 ? fast_exp2(lb0 - m_run) : 0.0f;
-    const float pb1v = vb1 ? fast_exp2(lb1 - m_run) : 0.0f;
     l_run += (pa0 + pa1) + (pb0v + pb1v);
     constexpr float kWScale = 64.0f;      // 2^(14 - kLazy)
     float Pa0 = 0.0f, Pa1 = 0.0f, Pb0 = 0.0f, Pb1 = 0.0f;
@@ -723,7 +751,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     ws.z_run += __shfl_xor_sync(0xffffffffu, ws.z_run, off);
   }
   // undo the code scale (2^-17 for even m-blocks, 2^-15 for odd ones) and the
-  // weight scale 2^(14 - kLazy) = 2^6; the residual column carries a further 2^11
+  // weight scale 2^(14 - kLazy) = 2^6; the residual column adds in unscaled
   constexpr float kInvEven = 2048.0f;   // 2^(17 - 6)
   constexpr float kInvOdd = 512.0f;     // 2^(15 - 6)
   if (GPH == 1) {
@@ -739,8 +767,8 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
 #pragma unroll
       for (int mb = 0; mb < 8; ++mb) {
         const float inv = (mb & 1) ? kInvOdd : kInvEven;
-        const float o0 = fmaf(fmaf(ws.acc[mb][1], 1.0f / 2048.0f, ws.acc[mb][0]), inv, ws.z_run);
-        const float o1 = fmaf(fmaf(ws.acc[mb][3], 1.0f / 2048.0f, ws.acc[mb][2]), inv, ws.z_run);
+        const float o0 = fmaf(ws.acc[mb][1] + ws.acc[mb][0], inv, ws.z_run);
+        const float o1 = fmaf(ws.acc[mb][3] + ws.acc[mb][2], inv, ws.z_run);
         p[4 + 16 * mb + g] = any ? o0 + 0.0f : 0.0f;
         p[4 + 16 * mb + g + 8] = any ? o1 + 0.0f : 0.0f;
       }
@@ -755,8 +783,8 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
       const float inv = (mb & 1) ? kInvOdd : kInvEven;
-      sm.o[warp][t][16 * mb + g] = fmaf(fmaf(ws.acc[mb][1], 1.0f / 2048.0f, ws.acc[mb][0]), inv, ws.z_run);
-      sm.o[warp][t][16 * mb + g + 8] = fmaf(fmaf(ws.acc[mb][3], 1.0f / 2048.0f, ws.acc[mb][2]), inv, ws.z_run);
+      sm.o[warp][t][16 * mb + g] = fmaf(ws.acc[mb][1] + ws.acc[mb][0], inv, ws.z_run);
+      sm.o[warp][t][16 * mb + g + 8] = fmaf(ws.acc[mb][3] + ws.acc[mb][2], inv, ws.z_run);
     }
     if (g == 0) {
       sm.m[warp][t] = ws.m_run;
