@@ -24,6 +24,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <cstdint>
 #include <vector>
 
 #include "kvq_internal.cuh"
@@ -37,10 +38,16 @@ constexpr int kD = kDim;
 // Batched fp32 GEMM: C[b] = alpha * op(A[b]) * op(B[b]) + beta * C[b], row-major.
 // op(A) is M x K: A[m * lda + k], or, transposed, A stored K x M: A[k * lda + m].
 // op(B) is K x N: B[k * ldb + n], or, transposed, B stored N x K: B[n * ldb + k].
-// 64 x 64 tile per CTA, k-slices of 16 staged in shared memory, 4 x 4 outputs
-// per thread.  beta == 0 does not read C.  With ksplit > 1 the K range is cut
-// into ksplit chunks (blockIdx.z = batch * ksplit + chunk) whose partial
-// products are added to C atomically (C zeroed beforehand when beta == 0).
+// Two kernels: gemm_tile_kernel<BM, BK> (BM x BM tile, BK-deep k-slices (64
+// for the 32-wide tile, 32 for the 64-wide one) double-buffered in shared
+// memory with the next slice's 16-byte loads in flight while the current one
+// is multiplied, 4 x 4 outputs per thread) when M and N are multiples of 32, K
+// of 64, and every row starts on 16 bytes;
+// otherwise gemm_kernel (64 x 64 tile, scalar guarded loads).  beta == 0 does
+// not read C; diag adds diag * I (square C, ksplit 1).  With ksplit > 1 the K
+// range is cut into ksplit chunks (blockIdx.z = batch * ksplit + chunk) whose
+// partial products are added to C atomically (C zeroed beforehand when
+// beta == 0).
 // ---------------------------------------------------------------------------
 struct Gemm {
   const float* A;
@@ -51,6 +58,7 @@ struct Gemm {
   float alpha, beta;
   int ta, tb;
   int ksplit, kchunk;
+  float diag;
 };
 
 __global__ void __launch_bounds__(256) gemm_kernel(Gemm g) {
@@ -114,7 +122,124 @@ __global__ void __launch_bounds__(256) gemm_kernel(Gemm g) {
       if (g.ksplit > 1)
         atomicAdd(c, g.alpha * acc[i][j]);
       else
-        *c = g.beta == 0.0f ? g.alpha * acc[i][j] : fmaf(g.alpha, acc[i][j], g.beta * *c);
+        *c = (g.beta == 0.0f ? g.alpha * acc[i][j] : fmaf(g.alpha, acc[i][j], g.beta * *c)) +
+             (m == n ? g.diag : 0.0f);
+    }
+  }
+}
+
+template <int BM, int BK>
+__global__ void __launch_bounds__((BM / 4) * (BM / 4)) gemm_tile_kernel(Gemm g) {
+  constexpr int TPR = BM / 4, NT = TPR * TPR, KQ = BK / 4;
+  constexpr int PER = BM * BK / 4 / NT;          // 16-byte loads per operand slice per thread
+  __shared__ __align__(16) float As[2][BK][BM + 4];
+  __shared__ __align__(16) float Bs[2][BK][BM + 4];
+  const int bz = blockIdx.z / g.ksplit, kz = blockIdx.z % g.ksplit;
+  const int kbeg = kz * g.kchunk, kend = min(g.K, kbeg + g.kchunk);
+  const float* A = g.A + bz * g.sA;
+  const float* B = g.B + bz * g.sB;
+  float* C = g.C + bz * g.sC;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BM;
+  const int tid = threadIdx.x, tx = tid % TPR, ty = tid / TPR;
+  float4 ra[PER], rb[PER];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      const int f = tid + p * NT;
+      if (g.ta) {        // A stored K x M: rows of M
+        const int kk = f / TPR, mm = 4 * (f % TPR);
+        ra[p] = *reinterpret_cast<const float4*>(A + static_cast<long long>(k0 + kk) * g.lda + m0 + mm);
+      } else {           // A stored M x K: rows of K
+        const int mm = f / KQ, kk = 4 * (f % KQ);
+        ra[p] = *reinterpret_cast<const float4*>(A + static_cast<long long>(m0 + mm) * g.lda + k0 + kk);
+      }
+      if (g.tb) {        // B stored N x K
+        const int nn = f / KQ, kk = 4 * (f % KQ);
+        rb[p] = *reinterpret_cast<const float4*>(B + static_cast<long long>(n0 + nn) * g.ldb + k0 + kk);
+      } else {           // B stored K x N
+        const int kk = f / TPR, nn = 4 * (f % TPR);
+        rb[p] = *reinterpret_cast<const float4*>(B + static_cast<long long>(k0 + kk) * g.ldb + n0 + nn);
+      }
+    }
+  };
+  // Shared-memory column of element m in k-row kk: 4-element groups are
+  // XOR-swizzled by (kk / 4) mod 8, so the transposing scalar stores of 4
+  // consecutive k from 8 (or 16) rows spread over all banks while each group
+  // stays one aligned 16-byte read.
+  const auto col = [](int kk, int m) { return m ^ (((kk >> 2) & 7) << 2); };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int p = 0; p < PER; ++p) {
+      const int f = tid + p * NT;
+      if (g.ta) {
+        const int kk = f / TPR, mm = 4 * (f % TPR);
+        *reinterpret_cast<float4*>(&As[buf][kk][col(kk, mm)]) = ra[p];
+      } else {
+        const int mm = f / KQ, kk = 4 * (f % KQ);
+        As[buf][kk][col(kk, mm)] = ra[p].x;
+        As[buf][kk + 1][col(kk + 1, mm)] = ra[p].y;
+        As[buf][kk + 2][col(kk + 2, mm)] = ra[p].z;
+        As[buf][kk + 3][col(kk + 3, mm)] = ra[p].w;
+      }
+      if (g.tb) {
+        const int nn = f / KQ, kk = 4 * (f % KQ);
+        Bs[buf][kk][col(kk, nn)] = rb[p].x;
+        Bs[buf][kk + 1][col(kk + 1, nn)] = rb[p].y;
+        Bs[buf][kk + 2][col(kk + 2, nn)] = rb[p].z;
+        Bs[buf][kk + 3][col(kk + 3, nn)] = rb[p].w;
+      } else {
+        const int kk = f / TPR, nn = 4 * (f % TPR);
+        *reinterpret_cast<float4*>(&Bs[buf][kk][col(kk, nn)]) = rb[p];
+      }
+    }
+  };
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  int buf = 0;
+  if (kbeg < kend) {
+    load(kbeg);
+    store(0);
+  }
+  __syncthreads();
+  for (int k0 = kbeg; k0 < kend; k0 += BK) {
+    const bool more = k0 + BK < kend;
+    if (more) load(k0 + BK);       // in flight during this slice's products
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&As[buf][kk][col(kk, 4 * ty)]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[buf][kk][col(kk, 4 * tx)]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    // the other buffer was last read before the previous barrier
+    if (more) store(buf ^ 1);
+    __syncthreads();
+    buf ^= 1;
+  }
+  const int n = n0 + 4 * tx;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + 4 * ty + i;
+    float* c = C + static_cast<long long>(m) * g.ldc + n;
+    if (g.ksplit > 1) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) atomicAdd(c + j, g.alpha * acc[i][j]);
+    } else {
+      float4 old = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (g.beta != 0.0f) old = *reinterpret_cast<const float4*>(c);
+      const float ov[4] = {old.x, old.y, old.z, old.w};
+      float r[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        r[j] = (g.beta == 0.0f ? g.alpha * acc[i][j] : fmaf(g.alpha, acc[i][j], g.beta * ov[j])) +
+               (m == n + j ? g.diag : 0.0f);
+      *reinterpret_cast<float4*>(c) = make_float4(r[0], r[1], r[2], r[3]);
     }
   }
 }
@@ -322,18 +447,6 @@ __global__ void add_mu_kernel(float* __restrict__ x, const float* __restrict__ m
     x[i] += mu[(i / (rows_per_head * kD)) * kD + (i % kD)];
 }
 
-// Per head (n x n, batch stride n*n): out = a * X + b * I
-__global__ void axpi_kernel(const float* __restrict__ X, float* __restrict__ out, int n, float a,
-                            float b, int heads) {
-  const long long total = static_cast<long long>(heads) * n * n;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long k = i % (static_cast<long long>(n) * n);
-    const int r = static_cast<int>(k / n), c = static_cast<int>(k % n);
-    out[i] = (X ? a * X[i] : 0.0f) + (r == c ? b : 0.0f);
-  }
-}
-
 // S = A - A^T (kD x kD per head)
 __global__ void skew_kernel(const float* __restrict__ A, float* __restrict__ S, int heads) {
   const long long total = static_cast<long long>(heads) * kD * kD;
@@ -345,47 +458,58 @@ __global__ void skew_kernel(const float* __restrict__ A, float* __restrict__ S, 
   }
 }
 
-// M = [[S^T, Gb], [0, S^T]] (2kD x 2kD per head)
-__global__ void block_kernel(const float* __restrict__ S, const float* __restrict__ Gb,
-                             float* __restrict__ M, int heads) {
-  const int n = 2 * kD;
-  const long long total = static_cast<long long>(heads) * n * n;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long h = i / (n * n), k = i % (n * n);
-    const int r = static_cast<int>(k / n), c = static_cast<int>(k % n);
-    const float* Sh = S + h * kD * kD;
-    float v = 0.0f;
-    if (r < kD && c < kD) v = Sh[c * kD + r];
-    else if (r < kD) v = Gb[h * kD * kD + r * kD + (c - kD)];
-    else if (c >= kD) v = Sh[(c - kD) * kD + (r - kD)];
-    M[i] = v;
-  }
-}
-
-// gA = X - X^T where X is the upper-right kD x kD block of M (2kD x 2kD per head)
-__global__ void grad_from_block_kernel(const float* __restrict__ M, float* __restrict__ gA,
-                                       int heads) {
-  const int n = 2 * kD;
+// out = s * op(X) + d * I for kD x kD matrices (op = transpose when tr); head
+// strides sx, so (in floats)
+__global__ void scale_kernel(const float* __restrict__ X, long long sx, int tr, float* __restrict__ out,
+                             long long so, float s, float d, int heads) {
   const long long total = static_cast<long long>(heads) * kD * kD;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long h = i / (kD * kD), k = i % (kD * kD);
     const int r = static_cast<int>(k / kD), c = static_cast<int>(k % kD);
-    const float* Mh = M + h * n * n;
-    gA[i] = Mh[r * n + kD + c] - Mh[c * n + kD + r];
+    const float x = X[h * sx + (tr ? c * kD + r : r * kD + c)];
+    out[h * so + r * kD + c] = s * x + (r == c ? d : 0.0f);
   }
 }
 
-// max over columns of sum |X| (the 1-norm), per head, into norm[head] (as int
-// bits: non-negative floats order like their bit patterns)
-__global__ void norm1_kernel(const float* __restrict__ X, int n, unsigned int* __restrict__ norm) {
-  const int h = blockIdx.y, c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= n) return;
-  const float* Xh = X + static_cast<long long>(h) * n * n;
+// gA = V - V^T (kD x kD per head, V with head stride sv)
+__global__ void skew_of_kernel(const float* __restrict__ V, long long sv, float* __restrict__ gA,
+                               int heads) {
+  const long long total = static_cast<long long>(heads) * kD * kD;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long h = i / (kD * kD), k = i % (kD * kD);
+    const int r = static_cast<int>(k / kD), c = static_cast<int>(k % kD);
+    gA[i] = V[h * sv + r * kD + c] - V[h * sv + c * kD + r];
+  }
+}
+
+// 1-norm (max over columns of sum |.|) per head of X, or with Y != nullptr of
+// the block matrix [[X, Y], [0, X]]: its column sums are those of X (left
+// half) and of X plus Y (right half).  Into norm[head] as int bits
+// (non-negative floats order like their bit patterns).
+// One CTA of 1024 threads per head: thread (q, c) sums 16 rows of column c.
+__global__ void __launch_bounds__(1024) norm1_kernel(const float* __restrict__ X,
+                                                     const float* __restrict__ Y, long long sxy,
+                                                     unsigned int* __restrict__ norm) {
+  __shared__ float part[8][kD];
+  const int h = blockIdx.y, c = threadIdx.x % kD, q = threadIdx.x / kD;
+  const float* Xh = X + h * sxy;
+  const float* Yh = Y ? Y + h * sxy : nullptr;
   float s = 0.0f;
-  for (int r = 0; r < n; ++r) s += fabsf(Xh[static_cast<long long>(r) * n + c]);
-  atomicMax(norm + h, __float_as_uint(s));
+#pragma unroll
+  for (int r = 16 * q; r < 16 * q + 16; ++r) {
+    s += fabsf(Xh[r * kD + c]);
+    if (Yh) s += fabsf(Yh[r * kD + c]);
+  }
+  part[q][c] = s;
+  __syncthreads();
+  if (q == 0) {
+    float t = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) t += part[u][c];
+    atomicMax(norm + h, __float_as_uint(t));
+  }
 }
 
 __global__ void adam_kernel(float* __restrict__ A, const float* __restrict__ g,
@@ -425,26 +549,40 @@ struct Ctx {
   void check() { if (err == cudaSuccess) err = cudaGetLastError(); }
 };
 
-// C = alpha op(A) op(B) + beta C for every head (strides sA, sB, sC per head)
+// C = alpha op(A) op(B) + beta C + diag I for every head (strides sA, sB, sC
+// per head)
 void gemm(Ctx& c, const float* A, int ta, long long sA, int lda, const float* B, int tb,
           long long sB, int ldb, float* C, long long sC, int ldc, int M, int N, int K, float alpha,
-          float beta) {
+          float beta, float diag = 0.0f) {
+  const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool tiled = M % 32 == 0 && N % 32 == 0 && K % 64 == 0 && lda % 4 == 0 && ldb % 4 == 0 &&
+                     ldc % 4 == 0 && sA % 4 == 0 && sB % 4 == 0 && sC % 4 == 0 && a16(A) &&
+                     a16(B) && a16(C);
+  // the 64-wide tile where it still gives a full wave of CTAs, else 32
+  const int bm = (tiled && M % 64 == 0 && N % 64 == 0 &&
+                  static_cast<long long>(M / 64) * (N / 64) * c.H >= 152) ? 64
+               : tiled ? 32 : 64;
   // Few output tiles and a long K (the T-long reductions): cut K so that the
   // grid covers the GPU; partial products are added atomically (beta 0 or 1).
-  const long long tiles = static_cast<long long>((N + 63) / 64) * ((M + 63) / 64) * c.H;
+  const long long tiles = static_cast<long long>((N + bm - 1) / bm) * ((M + bm - 1) / bm) * c.H;
   int ksplit = 1;
-  if (tiles < 512 && K >= 1024 && (beta == 0.0f || beta == 1.0f) &&
+  if (diag == 0.0f && tiles < 512 && K >= 1024 && (beta == 0.0f || beta == 1.0f) &&
       (beta == 1.0f || (ldc == N && sC == static_cast<long long>(M) * N))) {
     ksplit = static_cast<int>(std::min<long long>(K / 256, (1024 + tiles - 1) / tiles));
     if (ksplit < 2) ksplit = 1;
   }
-  const int kchunk = ksplit > 1 ? ((K + ksplit - 1) / ksplit + 15) / 16 * 16 : K;
+  const int kchunk = ksplit > 1 ? ((K + ksplit - 1) / ksplit + 63) / 64 * 64 : K;
   if (ksplit > 1) ksplit = (K + kchunk - 1) / kchunk;
   if (ksplit > 1 && beta == 0.0f && c.err == cudaSuccess)
     c.err = cudaMemsetAsync(C, 0, static_cast<size_t>(c.H) * M * N * sizeof(float), c.st);
-  Gemm g{A, B, C, M, N, K, lda, ldb, ldc, sA, sB, sC, alpha, beta, ta, tb, ksplit, kchunk};
-  dim3 grid((N + 63) / 64, (M + 63) / 64, c.H * ksplit);
-  gemm_kernel<<<grid, 256, 0, c.st>>>(g);
+  Gemm g{A, B, C, M, N, K, lda, ldb, ldc, sA, sB, sC, alpha, beta, ta, tb, ksplit, kchunk, diag};
+  dim3 grid((N + bm - 1) / bm, (M + bm - 1) / bm, c.H * ksplit);
+  if (!tiled)
+    gemm_kernel<<<grid, 256, 0, c.st>>>(g);
+  else if (bm == 64)
+    gemm_tile_kernel<64, 32><<<grid, 256, 0, c.st>>>(g);
+  else
+    gemm_tile_kernel<32, 64><<<grid, 64, 0, c.st>>>(g);
   c.check();
 }
 
@@ -457,7 +595,7 @@ struct Ws {
   float *att, *gatt;                                // [Nq*G][D]
   float *e, *ge;                                    // [Nq][Dm]
   float *A, *m, *v, *S, *E, *R, *gR, *Gb, *gA;      // [D][D]
-  float *X2, *P2, *Q2;                              // [2D][2D] (expm scratch)
+  float *X2, *P2, *Q2;                              // 4 [D][D] each (expm scratch pairs)
   float *kl, *errsum;                               // [H]
   unsigned int* norm;                               // [H]
   uint8_t* flag;                                    // [T][D]
@@ -515,18 +653,28 @@ Ws carve(uint8_t* base, int H, int T, int Nq, int G, int Dm) {
   return w;
 }
 
-// exp(M) for every head (n x n, n = kD or 2 kD): scaling by 2^j with |M / 2^j|_1
-// <= 1/2, a degree-8 Taylor polynomial (truncation error <= 0.5^9 / 9! ~ 5e-9,
-// below fp32 rounding), then j squarings.  The squarings carry
-// F = exp(X) - I (F <- 2F + F F), so rounding errors stay relative to F rather
-// than to I: the rotation stays orthogonal to fp32 accuracy.  Result in `out`
-// (which may be X); X, P, Q are scratch (n x n per head); M is read only to
-// form X, so it may be Q.  Reads the 1-norms (syncs the stream).
-void expm(Ctx& c, Ws& w, const float* M, int n, float* out, float* X, float* P, float* Q) {
+// exp(M) for every head (kD x kD): scaling by 2^j with |M / 2^j|_1 <= 1/2, a
+// degree-8 Taylor polynomial (truncation error <= 0.5^9 / 9! ~ 5e-9, below fp32
+// rounding), then j squarings.  The squarings carry F = exp(X) - I
+// (F <- 2F + F F), so rounding errors stay relative to F rather than to I: the
+// rotation stays orthogonal to fp32 accuracy.
+//
+// With Mb != nullptr the same is done for the block matrix [[M, Mb], [0, M]],
+// kept as the pair (u, v) of its diagonal and upper-right blocks: products of
+// such matrices stay of that form, (u1, v1)(u2, v2) = (u1 u2, u1 v2 + v1 u2), so
+// each product is three kD x kD products instead of one of twice the size.
+// Then `out` receives the upper-right block of the exponential (the Frechet
+// derivative of exp at M in the direction Mb) instead of exp(M).
+//
+// M (or its transpose, trM) and Mb have head stride kD * kD; the scratch pairs
+// live in the (4 kD^2 per head) buffers X2, P2, Q2.  Reads the 1-norms (syncs
+// the stream).
+void expm(Ctx& c, Ws& w, const float* M, int trM, const float* Mb, float* out) {
   if (c.err != cudaSuccess) return;
-  const long long nn = static_cast<long long>(n) * n;
+  const long long DD = static_cast<long long>(kD) * kD, S4 = 4 * DD;
+  const bool pair = Mb != nullptr;
   c.err = cudaMemsetAsync(w.norm, 0, c.H * sizeof(unsigned int), c.st);
-  norm1_kernel<<<dim3((n + 127) / 128, c.H), 128, 0, c.st>>>(M, n, w.norm);
+  norm1_kernel<<<dim3(1, c.H), 8 * kD, 0, c.st>>>(M, Mb, DD, w.norm);
   c.check();
   std::vector<unsigned int> nb(c.H);
   if (c.err == cudaSuccess)
@@ -534,35 +682,57 @@ void expm(Ctx& c, Ws& w, const float* M, int n, float* out, float* X, float* P, 
   if (c.err == cudaSuccess) c.err = cudaStreamSynchronize(c.st);
   if (c.err != cudaSuccess) return;
   float nmax = 0.0f;
-  for (unsigned int b : nb) {
+  for (unsigned int bits : nb) {
     float f;
-    memcpy(&f, &b, 4);
+    memcpy(&f, &bits, 4);
     nmax = std::max(nmax, f);
   }
   int j = 0;
   while (nmax / ldexpf(1.0f, j) > 0.5f && j < 60) ++j;
   const float sc = ldexpf(1.0f, -j);
-  const int g = grid_for(c.H * nn);
-  axpi_kernel<<<g, 256, 0, c.st>>>(M, X, n, sc, 0.0f, c.H);             // X = M / 2^j
-  axpi_kernel<<<g, 256, 0, c.st>>>(nullptr, P, n, 0.0f, 1.0f, c.H);     // P = I
+  const int g = grid_for(c.H * DD);
+  float* Xu = w.X2;
+  float* Xv = w.X2 + DD;
+  float* cu = w.P2;
+  float* cv = w.P2 + DD;
+  float* nu = w.Q2;
+  float* nv = w.Q2 + DD;
+  scale_kernel<<<g, 256, 0, c.st>>>(M, DD, trM, Xu, S4, sc, 0.0f, c.H);           // X = M / 2^j
+  // Horner from the inside: P = I + X/8, then P <- I + X P / k for k = 7..2
+  scale_kernel<<<g, 256, 0, c.st>>>(M, DD, trM, cu, S4, sc / 8.0f, 1.0f, c.H);
+  if (pair) {
+    scale_kernel<<<g, 256, 0, c.st>>>(Mb, DD, 0, Xv, S4, sc, 0.0f, c.H);
+    scale_kernel<<<g, 256, 0, c.st>>>(Mb, DD, 0, cv, S4, sc / 8.0f, 0.0f, c.H);
+  }
   c.check();
-  // Horner down to P = I + X/2 (I + X/3 (... (I + X/8))); then F = exp(X) - I = X P
-  float* cur = P;
-  float* nxt = Q;
-  for (int k = 8; k >= 2; --k) {
-    axpi_kernel<<<g, 256, 0, c.st>>>(nullptr, nxt, n, 0.0f, 1.0f, c.H);
-    c.check();
-    gemm(c, X, 0, nn, n, cur, 0, nn, n, nxt, nn, n, n, n, n, 1.0f / k, 1.0f);
-    std::swap(cur, nxt);
-  }
-  gemm(c, X, 0, nn, n, cur, 0, nn, n, nxt, nn, n, n, n, n, 1.0f, 0.0f);
-  std::swap(cur, nxt);                                                   // cur = F
+  // (u, v) <- X (u, v) * alpha + (beta-scaled old, diag I on u)
+  auto prod = [&](float alpha, float diag) {
+    gemm(c, Xu, 0, S4, kD, cu, 0, S4, kD, nu, S4, kD, kD, kD, kD, alpha, 0.0f, diag);
+    if (pair) {
+      gemm(c, Xu, 0, S4, kD, cv, 0, S4, kD, nv, S4, kD, kD, kD, kD, alpha, 0.0f);
+      gemm(c, Xv, 0, S4, kD, cu, 0, S4, kD, nv, S4, kD, kD, kD, kD, alpha, 1.0f);
+    }
+    std::swap(cu, nu);
+    std::swap(cv, nv);
+  };
+  for (int k = 7; k >= 2; --k) prod(1.0f / k, 1.0f);
+  prod(1.0f, 0.0f);                                                                 // F = X P
   for (int s = 0; s < j && c.err == cudaSuccess; ++s) {
-    c.err = cudaMemcpyAsync(nxt, cur, c.H * nn * sizeof(float), cudaMemcpyDeviceToDevice, c.st);
-    gemm(c, cur, 0, nn, n, cur, 0, nn, n, nxt, nn, n, n, n, n, 1.0f, 2.0f);   // 2F + F F
-    std::swap(cur, nxt);
+    // F <- 2F + F F: (u, v) <- (2u + u u, 2v + u v + v u)
+    c.err = cudaMemcpy2DAsync(nu, S4 * sizeof(float), cu, S4 * sizeof(float), (pair ? 2 : 1) * DD * sizeof(float),
+                              c.H, cudaMemcpyDeviceToDevice, c.st);
+    gemm(c, cu, 0, S4, kD, cu, 0, S4, kD, nu, S4, kD, kD, kD, kD, 1.0f, 2.0f);
+    if (pair) {
+      gemm(c, cu, 0, S4, kD, cv, 0, S4, kD, nv, S4, kD, kD, kD, kD, 1.0f, 2.0f);
+      gemm(c, cv, 0, S4, kD, cu, 0, S4, kD, nv, S4, kD, kD, kD, kD, 1.0f, 1.0f);
+    }
+    std::swap(cu, nu);
+    std::swap(cv, nv);
   }
-  axpi_kernel<<<g, 256, 0, c.st>>>(cur, out, n, 1.0f, 1.0f, c.H);       // out = F + I
+  if (pair)
+    scale_kernel<<<g, 256, 0, c.st>>>(cv, S4, 0, out, DD, 1.0f, 0.0f, c.H);         // upper-right block
+  else
+    scale_kernel<<<g, 256, 0, c.st>>>(cu, S4, 0, out, DD, 1.0f, 1.0f, c.H);         // F + I
   c.check();
 }
 
@@ -571,19 +741,18 @@ void rotation(Ctx& c, Ws& w, const float* R0) {
   const long long DD = static_cast<long long>(kD) * kD;
   skew_kernel<<<grid_for(c.H * DD), 256, 0, c.st>>>(w.A, w.S, c.H);
   c.check();
-  expm(c, w, w.S, kD, w.E, w.X2, w.P2, w.Q2);
+  expm(c, w, w.S, 0, nullptr, w.E);
   gemm(c, R0, 0, DD, kD, w.E, 0, DD, kD, w.R, DD, kD, kD, kD, kD, 1.0f, 0.0f);
 }
 
-// d loss / dA from d loss / dR (in w.gR): Gb = R0^T gR, then the Frechet adjoint.
+// d loss / dA from d loss / dR (in w.gR): Gb = R0^T gR, then the Frechet
+// adjoint L_exp(S^T, Gb) (upper-right block of exp([[S^T, Gb], [0, S^T]])),
+// whose skew part is the gradient.
 void rotation_backward(Ctx& c, Ws& w, const float* R0) {
-  const long long DD = static_cast<long long>(kD) * kD, D4 = 4 * DD;
+  const long long DD = static_cast<long long>(kD) * kD;
   gemm(c, R0, 1, DD, kD, w.gR, 0, DD, kD, w.Gb, DD, kD, kD, kD, kD, 1.0f, 0.0f);
-  // the block matrix in P2; expm reads it once (into X2, scaled) before P2 is reused
-  block_kernel<<<grid_for(c.H * D4), 256, 0, c.st>>>(w.S, w.Gb, w.P2, c.H);
-  c.check();
-  expm(c, w, w.P2, 2 * kD, w.X2, w.X2, w.Q2, w.P2);
-  grad_from_block_kernel<<<grid_for(c.H * DD), 256, 0, c.st>>>(w.X2, w.gA, c.H);
+  expm(c, w, w.S, 1, w.Gb, w.Gb);      // Gb is read once, at the start
+  skew_of_kernel<<<grid_for(c.H * DD), 256, 0, c.st>>>(w.Gb, DD, w.gA, c.H);
   c.check();
 }
 
