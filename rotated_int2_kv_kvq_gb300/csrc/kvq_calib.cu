@@ -25,6 +25,8 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <initializer_list>
+#include <utility>
 #include <vector>
 
 #include "kvq_internal.cuh"
@@ -484,31 +486,56 @@ __global__ void skew_of_kernel(const float* __restrict__ V, long long sv, float*
   }
 }
 
-// 1-norm (max over columns of sum |.|) per head of X, or with Y != nullptr of
-// the block matrix [[X, Y], [0, X]]: its column sums are those of X (left
-// half) and of X plus Y (right half).  Into norm[head] as int bits
-// (non-negative floats order like their bit patterns).
-// One CTA of 1024 threads per head: thread (q, c) sums 16 rows of column c.
+// 1-norms (max over columns of sum |.|) per head of X and, if Y != nullptr, of
+// Y, into norm[2 head] and norm[2 head + 1] as int bits (non-negative floats
+// order like their bit patterns).  One CTA of 1024 threads per head: thread
+// (q, c) sums 16 rows of column c.
 __global__ void __launch_bounds__(1024) norm1_kernel(const float* __restrict__ X,
                                                      const float* __restrict__ Y, long long sxy,
                                                      unsigned int* __restrict__ norm) {
-  __shared__ float part[8][kD];
+  __shared__ float part[2][8][kD];
   const int h = blockIdx.y, c = threadIdx.x % kD, q = threadIdx.x / kD;
   const float* Xh = X + h * sxy;
   const float* Yh = Y ? Y + h * sxy : nullptr;
-  float s = 0.0f;
+  float sx = 0.0f, sy = 0.0f;
 #pragma unroll
   for (int r = 16 * q; r < 16 * q + 16; ++r) {
-    s += fabsf(Xh[r * kD + c]);
-    if (Yh) s += fabsf(Yh[r * kD + c]);
+    sx += fabsf(Xh[r * kD + c]);
+    if (Yh) sy += fabsf(Yh[r * kD + c]);
   }
-  part[q][c] = s;
+  part[0][q][c] = sx;
+  part[1][q][c] = sy;
   __syncthreads();
-  if (q == 0) {
+  if (q < 2) {
     float t = 0.0f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) t += part[u][c];
-    atomicMax(norm + h, __float_as_uint(t));
+    for (int u = 0; u < 8; ++u) t += part[q][u][c];
+    atomicMax(norm + 2 * h + q, __float_as_uint(t));
+  }
+}
+
+// out = sum_i c[i] in[i] (+ d I on the first kD x kD block of each head), over
+// `len` floats per head at head stride `stride` (inputs and output alike)
+struct LinComb {
+  const float* in[5];
+  float c[5];
+  int n;
+  float d;
+  float* out;
+  long long stride;
+  int len;
+};
+
+__global__ void lincomb_kernel(LinComb L, int heads) {
+  const long long total = static_cast<long long>(heads) * L.len;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long h = i / L.len;
+    const int k = static_cast<int>(i % L.len);
+    const long long at = h * L.stride + k;
+    float v = (k < kD * kD && k / kD == k % kD) ? L.d : 0.0f;
+    for (int t = 0; t < L.n; ++t) v = fmaf(L.c[t], L.in[t][at], v);
+    L.out[at] = v;
   }
 }
 
@@ -597,7 +624,7 @@ struct Ws {
   float *A, *m, *v, *S, *E, *R, *gR, *Gb, *gA;      // [D][D]
   float *X2, *P2, *Q2;                              // 4 [D][D] each (expm scratch pairs)
   float *kl, *errsum;                               // [H]
-  unsigned int* norm;                               // [H]
+  unsigned int* norm;                               // [2H]
   uint8_t* flag;                                    // [T][D]
   int *amax, *amin;                                 // [T]
   size_t total;
@@ -645,7 +672,7 @@ Ws carve(uint8_t* base, int H, int T, int Nq, int G, int Dm) {
   w.Q2 = reinterpret_cast<float*>(take(D2));
   w.kl = reinterpret_cast<float*>(take(hd * 4));
   w.errsum = reinterpret_cast<float*>(take(hd * 4));
-  w.norm = reinterpret_cast<unsigned int*>(take(hd * 4));
+  w.norm = reinterpret_cast<unsigned int*>(take(hd * 8));
   w.flag = take(hd * T * kD);
   w.amax = reinterpret_cast<int*>(take(hd * T * 4));
   w.amin = reinterpret_cast<int*>(take(hd * T * 4));
@@ -653,9 +680,11 @@ Ws carve(uint8_t* base, int H, int T, int Nq, int G, int Dm) {
   return w;
 }
 
-// exp(M) for every head (kD x kD): scaling by 2^j with |M / 2^j|_1 <= 1/2, a
-// degree-8 Taylor polynomial (truncation error <= 0.5^9 / 9! ~ 5e-9, below fp32
-// rounding), then j squarings.  The squarings carry F = exp(X) - I
+// exp(M) for every head (kD x kD): scaling by 2^j with |M / 2^j|_1 <= 1/2, the
+// degree-8 Taylor polynomial of exp(X) - I (truncation error <= 0.5^9 / 9! ~
+// 5e-9, below fp32 rounding) by Paterson-Stockmeyer, F = B0 + X^4 B1 with
+// B0 = X + X^2/2 + X^3/6, B1 = I/24 + X/120 + X^2/720 + X^3/5040 + X^4/40320
+// (4 matrix products), then j squarings.  The squarings carry F = exp(X) - I
 // (F <- 2F + F F), so rounding errors stay relative to F rather than to I: the
 // rotation stays orthogonal to fp32 accuracy.
 //
@@ -663,8 +692,10 @@ Ws carve(uint8_t* base, int H, int T, int Nq, int G, int Dm) {
 // kept as the pair (u, v) of its diagonal and upper-right blocks: products of
 // such matrices stay of that form, (u1, v1)(u2, v2) = (u1 u2, u1 v2 + v1 u2), so
 // each product is three kD x kD products instead of one of twice the size.
-// Then `out` receives the upper-right block of the exponential (the Frechet
-// derivative of exp at M in the direction Mb) instead of exp(M).
+// Then `out` receives the upper-right block of the exponential, the Frechet
+// derivative of exp at M in the direction Mb.  That block is linear in Mb, so
+// Mb enters scaled by a power of two c with c |Mb|_1 <= 1/4 and the result is
+// divided by c: the direction does not add squarings.
 //
 // M (or its transpose, trM) and Mb have head stride kD * kD; the scratch pairs
 // live in the (4 kD^2 per head) buffers X2, P2, Q2.  Reads the 1-norms (syncs
@@ -673,66 +704,84 @@ void expm(Ctx& c, Ws& w, const float* M, int trM, const float* Mb, float* out) {
   if (c.err != cudaSuccess) return;
   const long long DD = static_cast<long long>(kD) * kD, S4 = 4 * DD;
   const bool pair = Mb != nullptr;
-  c.err = cudaMemsetAsync(w.norm, 0, c.H * sizeof(unsigned int), c.st);
+  c.err = cudaMemsetAsync(w.norm, 0, 2 * c.H * sizeof(unsigned int), c.st);
   norm1_kernel<<<dim3(1, c.H), 8 * kD, 0, c.st>>>(M, Mb, DD, w.norm);
   c.check();
-  std::vector<unsigned int> nb(c.H);
+  std::vector<unsigned int> nb(2 * c.H);
   if (c.err == cudaSuccess)
-    c.err = cudaMemcpyAsync(nb.data(), w.norm, c.H * sizeof(unsigned int), cudaMemcpyDeviceToHost, c.st);
+    c.err = cudaMemcpyAsync(nb.data(), w.norm, 2 * c.H * sizeof(unsigned int), cudaMemcpyDeviceToHost,
+                            c.st);
   if (c.err == cudaSuccess) c.err = cudaStreamSynchronize(c.st);
   if (c.err != cudaSuccess) return;
-  float nmax = 0.0f;
-  for (unsigned int bits : nb) {
-    float f;
-    memcpy(&f, &bits, 4);
-    nmax = std::max(nmax, f);
+  std::vector<float> nx(c.H), ny(c.H);
+  float nymax = 0.0f;
+  for (int h = 0; h < c.H; ++h) {
+    memcpy(&nx[h], &nb[2 * h], 4);
+    memcpy(&ny[h], &nb[2 * h + 1], 4);
+    nymax = std::max(nymax, ny[h]);
   }
+  int kb = 0;                                   // direction scale c = 2^-kb
+  while (pair && nymax * ldexpf(1.0f, -kb) > 0.25f && kb < 120) ++kb;
+  float nmax = 0.0f;
+  for (int h = 0; h < c.H; ++h) nmax = std::max(nmax, nx[h] + (pair ? ldexpf(ny[h], -kb) : 0.0f));
   int j = 0;
   while (nmax / ldexpf(1.0f, j) > 0.5f && j < 60) ++j;
   const float sc = ldexpf(1.0f, -j);
-  const int g = grid_for(c.H * DD);
-  float* Xu = w.X2;
-  float* Xv = w.X2 + DD;
-  float* cu = w.P2;
-  float* cv = w.P2 + DD;
-  float* nu = w.Q2;
-  float* nv = w.Q2 + DD;
-  scale_kernel<<<g, 256, 0, c.st>>>(M, DD, trM, Xu, S4, sc, 0.0f, c.H);           // X = M / 2^j
-  // Horner from the inside: P = I + X/8, then P <- I + X P / k for k = 7..2
-  scale_kernel<<<g, 256, 0, c.st>>>(M, DD, trM, cu, S4, sc / 8.0f, 1.0f, c.H);
-  if (pair) {
-    scale_kernel<<<g, 256, 0, c.st>>>(Mb, DD, 0, Xv, S4, sc, 0.0f, c.H);
-    scale_kernel<<<g, 256, 0, c.st>>>(Mb, DD, 0, cv, S4, sc / 8.0f, 0.0f, c.H);
-  }
+  const int g = grid_for(c.H * DD), g2 = grid_for(c.H * 2 * DD);
+  const int len = pair ? 2 * static_cast<int>(DD) : static_cast<int>(DD);
+  // pairs: X, X^2 in X2; X^3, X^4 in P2; B0 (then F), B1 in Q2
+  float* X1 = w.X2;
+  float* X2p = w.X2 + 2 * DD;
+  float* X3 = w.P2;
+  float* X4 = w.P2 + 2 * DD;
+  float* F = w.Q2;
+  float* B1 = w.Q2 + 2 * DD;
+  scale_kernel<<<g, 256, 0, c.st>>>(M, DD, trM, X1, S4, sc, 0.0f, c.H);             // X = M / 2^j
+  if (pair) scale_kernel<<<g, 256, 0, c.st>>>(Mb, DD, 0, X1 + DD, S4, ldexpf(sc, -kb), 0.0f, c.H);
   c.check();
-  // (u, v) <- X (u, v) * alpha + (beta-scaled old, diag I on u)
-  auto prod = [&](float alpha, float diag) {
-    gemm(c, Xu, 0, S4, kD, cu, 0, S4, kD, nu, S4, kD, kD, kD, kD, alpha, 0.0f, diag);
+  // C = alpha A B + beta C (+ diag I on u), A B as pairs when `pair`
+  auto prod = [&](const float* A, const float* B, float* C, float alpha, float beta, float diag) {
+    gemm(c, A, 0, S4, kD, B, 0, S4, kD, C, S4, kD, kD, kD, kD, alpha, beta, diag);
     if (pair) {
-      gemm(c, Xu, 0, S4, kD, cv, 0, S4, kD, nv, S4, kD, kD, kD, kD, alpha, 0.0f);
-      gemm(c, Xv, 0, S4, kD, cu, 0, S4, kD, nv, S4, kD, kD, kD, kD, alpha, 1.0f);
+      gemm(c, A, 0, S4, kD, B + DD, 0, S4, kD, C + DD, S4, kD, kD, kD, kD, alpha, beta);
+      gemm(c, A + DD, 0, S4, kD, B, 0, S4, kD, C + DD, S4, kD, kD, kD, kD, alpha, 1.0f);
     }
-    std::swap(cu, nu);
-    std::swap(cv, nv);
   };
-  for (int k = 7; k >= 2; --k) prod(1.0f / k, 1.0f);
-  prod(1.0f, 0.0f);                                                                 // F = X P
+  auto lincomb = [&](float* o, std::initializer_list<std::pair<const float*, float>> terms, float d) {
+    LinComb L{};
+    L.n = 0;
+    for (const auto& t : terms) {
+      L.in[L.n] = t.first;
+      L.c[L.n] = t.second;
+      ++L.n;
+    }
+    L.d = d;
+    L.out = o;
+    L.stride = S4;
+    L.len = len;
+    lincomb_kernel<<<pair ? g2 : g, 256, 0, c.st>>>(L, c.H);
+    c.check();
+  };
+  prod(X1, X1, X2p, 1.0f, 0.0f, 0.0f);                                              // X^2
+  prod(X2p, X1, X3, 1.0f, 0.0f, 0.0f);                                              // X^3
+  prod(X2p, X2p, X4, 1.0f, 0.0f, 0.0f);                                             // X^4
+  lincomb(F, {{X1, 1.0f}, {X2p, 1.0f / 2}, {X3, 1.0f / 6}}, 0.0f);
+  lincomb(B1, {{X1, 1.0f / 120}, {X2p, 1.0f / 720}, {X3, 1.0f / 5040}, {X4, 1.0f / 40320}},
+          1.0f / 24);
+  prod(X4, B1, F, 1.0f, 1.0f, 0.0f);                                                // F = B0 + X^4 B1
+  float* cur = F;
+  float* nxt = B1;
   for (int s = 0; s < j && c.err == cudaSuccess; ++s) {
     // F <- 2F + F F: (u, v) <- (2u + u u, 2v + u v + v u)
-    c.err = cudaMemcpy2DAsync(nu, S4 * sizeof(float), cu, S4 * sizeof(float), (pair ? 2 : 1) * DD * sizeof(float),
-                              c.H, cudaMemcpyDeviceToDevice, c.st);
-    gemm(c, cu, 0, S4, kD, cu, 0, S4, kD, nu, S4, kD, kD, kD, kD, 1.0f, 2.0f);
-    if (pair) {
-      gemm(c, cu, 0, S4, kD, cv, 0, S4, kD, nv, S4, kD, kD, kD, kD, 1.0f, 2.0f);
-      gemm(c, cv, 0, S4, kD, cu, 0, S4, kD, nv, S4, kD, kD, kD, kD, 1.0f, 1.0f);
-    }
-    std::swap(cu, nu);
-    std::swap(cv, nv);
+    c.err = cudaMemcpy2DAsync(nxt, S4 * sizeof(float), cur, S4 * sizeof(float), len * sizeof(float), c.H,
+                              cudaMemcpyDeviceToDevice, c.st);
+    prod(cur, cur, nxt, 1.0f, 2.0f, 0.0f);
+    std::swap(cur, nxt);
   }
   if (pair)
-    scale_kernel<<<g, 256, 0, c.st>>>(cv, S4, 0, out, DD, 1.0f, 0.0f, c.H);         // upper-right block
+    scale_kernel<<<g, 256, 0, c.st>>>(cur + DD, S4, 0, out, DD, ldexpf(1.0f, kb), 0.0f, c.H);
   else
-    scale_kernel<<<g, 256, 0, c.st>>>(cu, S4, 0, out, DD, 1.0f, 1.0f, c.H);         // F + I
+    scale_kernel<<<g, 256, 0, c.st>>>(cur, S4, 0, out, DD, 1.0f, 1.0f, c.H);        // F + I
   c.check();
 }
 
