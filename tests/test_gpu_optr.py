@@ -2,8 +2,9 @@
 against the float64 oracle (oracle/optr.py) on synthetic calibration traces.
 
 * the key and value objectives and their straight-through gradients at A = 0
-  and at random generators: losses within 1e-3 and gradients within 2e-3
-  relative (L2) of the oracle;
+  and at random generators (small ones, and one large enough for the matrix
+  exponentials to need squarings), also at sizes off the GEMM tiles: losses
+  within 1e-3 and gradients within 2e-3 relative (L2) of the oracle;
 * a short calibration: the loss history within 1e-2 of the oracle's (Adam's
   first steps follow the gradient's signs, so entries whose gradient is near
   zero may step differently), the calibrated rotations orthogonal to 1e-5;
@@ -42,9 +43,14 @@ def _rel(a, b):
     return float(np.linalg.norm(np.asarray(a) - np.asarray(b)) / max(np.linalg.norm(b), 1e-30))
 
 
-@pytest.mark.parametrize("scale", [0.0, 0.02])
-def test_objectives_and_gradients_match_the_oracle(scale):
-    wl, gpu, host = _setup()
+@pytest.mark.parametrize("scale,shape", [(0.0, (256, 32, 256)), (0.02, (256, 32, 256)),
+                                         (0.02, (200, 20, 200)), (0.3, (256, 32, 256))])
+def test_objectives_and_gradients_match_the_oracle(scale, shape):
+    """(200, 20, 200): T, Nq * G and d_model off every GEMM tile (the guarded
+    GEMM); scale 0.3: a generator large enough that the exponentials need
+    squarings."""
+    T, Nq, Dm = shape
+    wl, gpu, host = _setup(T=T, Nq=Nq, Dm=Dm)
     H = host["K"].shape[0]
     rng = np.random.default_rng(17)
     A_k = (rng.standard_normal((H, 128, 128)) * scale).astype(np.float32)
