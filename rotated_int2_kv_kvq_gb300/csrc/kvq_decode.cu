@@ -513,11 +513,15 @@ __device__ __forceinline__ void process_pair(WarpState& st, const uint32_t (&qf)
     // ---- online softmax.  The value weights P = p * s_v feed fp16 operands, so
     // the running max m is kept over lv = logit + log2(max(s_v, 2^-24)) and
     // raised only when some lv exceeds m + kLazy: then p * s_v <= 2^kLazy for
-    // every token seen and P * 2^(14 - kLazy) stays below 2^14.  p = 2^(logit - m)
-    // itself may be large (at most 2^(kLazy + 24)); it is only summed in fp32.
-    // The test lv > m + kLazy is taken as p * max(s_v, 2^-24) > 2^kLazy on the
-    // weights against the current m (true for p = inf when m is still -inf),
-    // so the logarithms are computed only on the rare stages that raise m.
+    // every token seen.  m_run holds m - 6, so p = 2^(logit - m_run) already
+    // carries the weight scale 2^(14 - kLazy) = 2^6 and P = p * max(s_v, 2^-24)
+    // stays below 2^14 (max() changes nothing: fp16 s_v is 0 or >= 2^-24, and
+    // s_v = 0 gives code 0).  p itself may be large (at most 2^(kLazy + 30)); it
+    // is only summed in fp32, and l_run, z_run carry the 2^6 too (removed in
+    // the epilogue).  The test lv > m + kLazy is taken as P > 2^14 on the
+    // weights against the current max (true for p = inf while m is -inf), so
+    // the logarithms are computed only on the rare stages that raise m.
+    static_assert(kLazy == 8.0f, "P <= 2^14 is p * s_v <= 2^kLazy with the 2^6 scale");
     const float sva0 = half_lo(mta.z), sva1 = half_lo(mta.w);
     const float svb0 = half_lo(mtb.z), svb1 = half_lo(mtb.w);
     float pa0 = va0 ? fast_exp2(la0 - m_run) : 0.0f;
@@ -525,10 +529,12 @@ __device__ __forceinline__ void process_pair(WarpState& st, const uint32_t (&qf)
     float pb0v = vb0 ? fast_exp2(lb0 - m_run) : 0.0f;
     float pb1v = vb1 ? fast_exp2(lb1 - m_run) : 0.0f;
     constexpr float kSvMin = 0x1p-24f;
-    const float cmax = fmaxf(fmaxf(pa0 * fmaxf(sva0, kSvMin), pa1 * fmaxf(sva1, kSvMin)),
-                             fmaxf(pb0v * fmaxf(svb0, kSvMin), pb1v * fmaxf(svb1, kSvMin)));
-    if (__any_sync(0xffffffffu, !(cmax <= 0x1p8f))) {
-      static_assert(kLazy == 8.0f, "the weight test above uses 2^kLazy = 2^8");
+    const float sa0 = fmaxf(sva0, kSvMin), sa1 = fmaxf(sva1, kSvMin);
+    const float sb0 = fmaxf(svb0, kSvMin), sb1 = fmaxf(svb1, kSvMin);
+    float Pa0 = va0 ? pa0 * sa0 : 0.0f, Pa1 = va1 ? pa1 * sa1 : 0.0f;
+    float Pb0 = vb0 ? pb0v * sb0 : 0.0f, Pb1 = vb1 ? pb1v * sb1 : 0.0f;
+    const float cmax = fmaxf(fmaxf(Pa0, Pa1), fmaxf(Pb0, Pb1));
+    if (__any_sync(0xffffffffu, !(cmax <= 0x1p14f))) {
       const float lva0 = la0 + fmaxf(fast_log2(sva0), -24.0f);
       const float lva1 = la1 + fmaxf(fast_log2(sva1), -24.0f);
       const float lvb0 = lb0 + fmaxf(fast_log2(svb0), -24.0f);
@@ -538,28 +544,31 @@ __device__ __forceinline__ void process_pair(WarpState& st, const uint32_t (&qf)
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
       pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-      if (pm > m_run) {
-        const float f = fast_exp2(m_run - pm);
+      const float pms = pm - 6.0f;
+      if (pms > m_run) {
+        const float f = fast_exp2(m_run - pms);
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
           for (int q = 0; q < 4; ++q) acc[mb][q] *= f;
         l_run *= f;
         z_run *= f;
-        m_run = pm;
+        m_run = pms;
       }
       pa0 = va0 ? fast_exp2(la0 - m_run) : 0.0f;
       pa1 = va1 ? fast_exp2(la1 - m_run) : 0.0f;
       pb0v = vb0 ? fast_exp2(lb0 - m_run) : 0.0f;
       pb1v = vb1 ? fast_exp2(lb1 - m_run) : 0.0f;
+      Pa0 = va0 ? pa0 * sa0 : 0.0f;
+      Pa1 = va1 ? pa1 * sa1 : 0.0f;
+      Pb0 = vb0 ? pb0v * sb0 : 0.0f;
+      Pb1 = vb1 ? pb1v * sb1 : 0.0f;
     }
     l_run += (pa0 + pa1) + (pb0v + pb1v);
-    constexpr float kWScale = 64.0f;      // 2^(14 - kLazy)
-    float Pa0 = 0.0f, Pa1 = 0.0f, Pb0 = 0.0f, Pb1 = 0.0f;
-    if (va0) { Pa0 = pa0 * (sva0 * kWScale); z_run = fmaf(pa0, half_hi(mta.z), z_run); }
-    if (va1) { Pa1 = pa1 * (sva1 * kWScale); z_run = fmaf(pa1, half_hi(mta.w), z_run); }
-    if (vb0) { Pb0 = pb0v * (svb0 * kWScale); z_run = fmaf(pb0v, half_hi(mtb.z), z_run); }
-    if (vb1) { Pb1 = pb1v * (svb1 * kWScale); z_run = fmaf(pb1v, half_hi(mtb.w), z_run); }
+    if (va0) z_run = fmaf(pa0, half_hi(mta.z), z_run);
+    if (va1) z_run = fmaf(pa1, half_hi(mta.w), z_run);
+    if (vb0) z_run = fmaf(pb0v, half_hi(mtb.z), z_run);
+    if (vb1) z_run = fmaf(pb1v, half_hi(mtb.w), z_run);
 
     // ---- values of both pages
     uint32_t fa0, fa1, fb0, fb1;
@@ -751,7 +760,8 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     ws.z_run += __shfl_xor_sync(0xffffffffu, ws.z_run, off);
   }
   // undo the code scale (2^-17 for even m-blocks, 2^-15 for odd ones) and the
-  // weight scale 2^(14 - kLazy) = 2^6; the residual column adds in unscaled
+  // weight scale 2^(14 - kLazy) = 2^6 (also on l_run, z_run and m_run); the
+  // residual column adds in unscaled
   constexpr float kInvEven = 2048.0f;   // 2^(17 - 6)
   constexpr float kInvOdd = 512.0f;     // 2^(15 - 6)
   if (GPH == 1) {
@@ -764,17 +774,18 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
       float* p = a.part + ((static_cast<size_t>(b) * a.H + kv * a.G + t) * a.splits + split) *
                               kPartStride;
       const bool any = ws.m_run > -INFINITY;
+      const float zr = ws.z_run * 0x1p-6f;
 #pragma unroll
       for (int mb = 0; mb < 8; ++mb) {
         const float inv = (mb & 1) ? kInvOdd : kInvEven;
-        const float o0 = fmaf(ws.acc[mb][1] + ws.acc[mb][0], inv, ws.z_run);
-        const float o1 = fmaf(ws.acc[mb][3] + ws.acc[mb][2], inv, ws.z_run);
+        const float o0 = fmaf(ws.acc[mb][1] + ws.acc[mb][0], inv, zr);
+        const float o1 = fmaf(ws.acc[mb][3] + ws.acc[mb][2], inv, zr);
         p[4 + 16 * mb + g] = any ? o0 + 0.0f : 0.0f;
         p[4 + 16 * mb + g + 8] = any ? o1 + 0.0f : 0.0f;
       }
       if (g == 0) {
-        p[0] = ws.m_run;
-        p[1] = any ? ws.l_run : 0.0f;
+        p[0] = ws.m_run + 6.0f;
+        p[1] = any ? ws.l_run * 0x1p-6f : 0.0f;
       }
     }
     return;
@@ -783,12 +794,12 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
       const float inv = (mb & 1) ? kInvOdd : kInvEven;
-      sm.o[warp][t][16 * mb + g] = fmaf(ws.acc[mb][1] + ws.acc[mb][0], inv, ws.z_run);
-      sm.o[warp][t][16 * mb + g + 8] = fmaf(ws.acc[mb][3] + ws.acc[mb][2], inv, ws.z_run);
+      sm.o[warp][t][16 * mb + g] = fmaf(ws.acc[mb][1] + ws.acc[mb][0], inv, ws.z_run * 0x1p-6f);
+      sm.o[warp][t][16 * mb + g + 8] = fmaf(ws.acc[mb][3] + ws.acc[mb][2], inv, ws.z_run * 0x1p-6f);
     }
     if (g == 0) {
-      sm.m[warp][t] = ws.m_run;
-      sm.l[warp][t] = ws.l_run;
+      sm.m[warp][t] = ws.m_run + 6.0f;
+      sm.l[warp][t] = ws.l_run * 0x1p-6f;
     }
   }
   __syncthreads();
