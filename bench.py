@@ -487,12 +487,18 @@ def run_ours(args):
 
     # The OptR setting: 64 sink + 256 recent tokens kept in BF16 beside the INT2
     # cache.  A step appends the new token to both caches (the INT2 copy is there
-    # for when the token leaves the window) and decodes with the window.
+    # for when the token leaves the window) and decodes with the window: one
+    # kvq_append_decode_window call (3 launches); the same step as three separate
+    # calls (5 launches) is timed beside it.
     window = None
     if bf16_pool is not None:
         sink, recent = 64, 256
 
         def window_step():
+            K.kvq_append_decode_window(h, pool, npool, bf16_pool, npool, pt, kd_new, vd_new, qd, pt,
+                                       seq_lens, sink, recent, out, ws, splits)
+
+        def window_step_separate():
             K.kvq_append(h, pool, npool, kd_new, vd_new, sid, pos, pt)
             K.kvq_bf16_append(h, bf16_pool, npool, kd_new, vd_new, sid, pos, pt)
             K.kvq_decode_window(h, pool, npool, bf16_pool, npool, pt, qd, pt, seq_lens, sink,
@@ -500,6 +506,7 @@ def run_ours(args):
 
         wms, _ = timed(window_step, args.steps, args.warmup)
         _, wkern = timed(window_step, args.steps, max(3, args.warmup // 4), profile=True)
+        wsep, _ = timed(window_step_separate, args.steps, args.warmup)
         n_win = [min(int(L), sink + recent) for L in lens]
         wbytes = Hkv * sum((int(L) - n) * W.cache_bytes_per_token_head("int2") +
                            n * W.cache_bytes_per_token_head("bf16") for L, n in zip(lens, n_win))
@@ -510,7 +517,9 @@ def run_ours(args):
                   "int2_kernel_ms": wkern[0] / max(1, wkern[1]),
                   "effective_bits": W.effective_bits_window(ctx, sink, recent),
                   "effective_bits_64k": W.effective_bits_window(65536, sink, recent),
-                  "launches_per_step": 5}
+                  "launches_per_step": 3,
+                  "separate_calls_ms_per_step": wsep / args.steps,
+                  "separate_calls": "kvq_append + kvq_bf16_append + kvq_decode_window"}
         assert K.kvq_get_status(h) == 0, "device status bits set during the window benchmark"
 
     cpu = None

@@ -289,6 +289,28 @@ int kvq_decode_window(kvq_handle* h, const void* pool, int num_pool_pages,
                       int batch, int sink, int recent, float* out, void* workspace,
                       size_t ws_bytes, int num_splits, void* stream);
 
+/* ---- append and window decode in one call -------------------------------------
+ * The decode step of the windowed setting above: every sequence b with
+ * seq_lens[b] >= 1 gets one new token at position seq_lens[b] - 1, stored in
+ * both caches (the INT2 copy serves once the token leaves the window), then
+ * attends as kvq_decode_window.  Equal, byte for byte in both pools and bit for
+ * bit in out, to
+ *     kvq_append(K_new[b], V_new[b] at (b, seq_lens[b] - 1) for each such b)
+ *     kvq_bf16_append(the same tokens into bf16_pool through bf16_page_table)
+ *     kvq_decode_window(...same arguments...)
+ * in three kernel launches instead of five.
+ *   K_new, V_new : device bf16 [batch][Hkv][D], 4-byte aligned.
+ *   pool, bf16_pool : written (the new tokens' slots) and read.
+ * Other arguments, errors and status bits as for those calls (a new position
+ * without a valid INT2 or BF16 page sets KVQ_STATUS_BAD_PAGE; that copy of the
+ * token is not stored). */
+int kvq_append_decode_window(kvq_handle* h, void* pool, int num_pool_pages, void* bf16_pool,
+                             int bf16_num_pool_pages, const int32_t* bf16_page_table,
+                             const uint16_t* K_new, const uint16_t* V_new, const uint16_t* q,
+                             const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                             int batch, int sink, int recent, float* out, void* workspace,
+                             size_t ws_bytes, int num_splits, void* stream);
+
 /* ---- test export -----------------------------------------------------------
  * Dequantise positions [start, start+len) of sequence `seq` to fp32 in the
  * rotated (and, for keys, centred) basis: K_out[i][kv][d] = fmaf(code, s, z),

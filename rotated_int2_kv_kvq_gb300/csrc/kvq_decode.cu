@@ -296,6 +296,28 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
   }
   sm.x[0][i] = __fsub_rn(__uint_as_float(static_cast<uint32_t>(kbits) << 16), mui);
   sm.x[1][i] = __uint_as_float(static_cast<uint32_t>(vbits) << 16);
+  if (st.bf16_pool != nullptr && p >= 0 && seq_len <= a.max_pages * kPage) {
+    // the BF16 window cache's copy of the token (same placement as the BF16
+    // append kernel: fragment order of the BF16 page record)
+    const int page = st.bf16_page_table[static_cast<size_t>(b) * a.max_pages + p / kPage];
+    if (page >= 0 && page < st.bf16_num_pool_pages) {
+      uint8_t* base = st.bf16_pool + (static_cast<size_t>(page) * a.Hkv + kv) * kBf16Rec;
+      const int tau = p % kPage;
+      {
+        const int w = i >> 4, r = i & 15, h = r >> 3, t = (r >> 1) & 3, e = r & 1;
+        const int L = 4 * (tau & 7) + t, reg = (tau >> 3) + 2 * h;
+        *reinterpret_cast<uint16_t*>(base + 512 * w + 16 * L + 4 * reg + 2 * e) = kbits;
+      }
+      {
+        const int m = i >> 4, r = i & 15, g = r & 7, dh = r >> 3;
+        const int t = (tau & 7) >> 1, e = tau & 1, th = tau >> 3;
+        const int L = 4 * g + t, reg = 2 * th + dh;
+        *reinterpret_cast<uint16_t*>(base + 4096 + 512 * m + 16 * L + 4 * reg + 2 * e) = vbits;
+      }
+    } else if (i == 0) {
+      atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+    }
+  }
   const bool ok = mbar_wait_bounded(bar, 0);
   if (__syncthreads_or(!ok)) {
     if (i == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);

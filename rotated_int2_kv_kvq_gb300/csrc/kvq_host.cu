@@ -403,6 +403,33 @@ int kvq_append_decode(kvq_handle* h, void* pool, int num_pool_pages, const uint1
                        out, workspace, ws_bytes, num_splits, stream, Window(), &step);
 }
 
+int kvq_append_decode_window(kvq_handle* h, void* pool, int num_pool_pages, void* bf16_pool,
+                             int bf16_num_pool_pages, const int32_t* bf16_page_table,
+                             const uint16_t* K_new, const uint16_t* V_new, const uint16_t* q,
+                             const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                             int batch, int sink, int recent, float* out, void* workspace,
+                             size_t ws_bytes, int num_splits, void* stream) {
+  if (!K_new || !V_new) return KVQ_EINVAL;
+  if (reinterpret_cast<uintptr_t>(K_new) % 4 || reinterpret_cast<uintptr_t>(V_new) % 4)
+    return KVQ_EINVAL;
+  Window win;
+  win.bf16_pool = bf16_pool;
+  win.bf16_num_pool_pages = bf16_num_pool_pages;
+  win.bf16_page_table = bf16_page_table;
+  win.sink = sink;
+  win.recent = recent;
+  win.on = true;
+  kvq::StepArgs step;
+  step.pool = static_cast<uint8_t*>(pool);
+  step.K = K_new;
+  step.V = V_new;
+  step.bf16_pool = static_cast<uint8_t*>(bf16_pool);
+  step.bf16_num_pool_pages = bf16_num_pool_pages;
+  step.bf16_page_table = bf16_page_table;
+  return decode_common(h, true, pool, num_pool_pages, q, page_table, max_pages, seq_lens, batch,
+                       out, workspace, ws_bytes, num_splits, stream, win, &step);
+}
+
 int kvq_bf16_decode(kvq_handle* h, const void* pool, int num_pool_pages, const uint16_t* q,
                     const int32_t* page_table, int max_pages, const int32_t* seq_lens, int batch,
                     float* out, void* workspace, size_t ws_bytes, int num_splits, void* stream) {

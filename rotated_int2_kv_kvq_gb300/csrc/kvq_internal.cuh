@@ -85,6 +85,11 @@ struct StepArgs {
   const float* mu;           // [Hkv][D]
   float clip_k, clip_v;
   int q_rotated;             // 1: q is already q R_K
+  // BF16 window cache: the token is also copied there (kvq_append_decode_window);
+  // bf16_pool == nullptr for kvq_append_decode
+  uint8_t* bf16_pool = nullptr;
+  int bf16_num_pool_pages = 0;
+  const int32_t* bf16_page_table = nullptr;
 };
 
 // ---- launchers (defined in the .cu files) --------------------------------

@@ -50,6 +50,8 @@ SIGNATURES = {
     "kvq_append_decode": ([_P, _P, _I, _P, _P, _P, _P, _I, _P, _I, _P, _P, _SZ, _I, _P], _I),
     "kvq_decode_window": ([_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _P, _P, _SZ, _I,
                            _P], _I),
+    "kvq_append_decode_window": ([_P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _P,
+                                  _P, _SZ, _I, _P], _I),
     "kvq_get_status": ([_P, _P, _P], _I),
     "kvq_auto_splits": ([_P, _I, _I], _I),
     "kvq_profile_enable": ([_P, _I], _I),
@@ -273,6 +275,24 @@ def kvq_decode_window(h, pool, num_pool_pages, bf16_pool, bf16_num_pool_pages, b
         _ptr(seq_lens, _I32, "seq_lens"), batch, int(sink), int(recent), _ptr(out, _F32, "out"),
         _ptr(workspace, _U8, "workspace"), int(workspace.numel()), int(num_splits),
         _stream(stream)))
+
+
+def kvq_append_decode_window(h, pool, num_pool_pages, bf16_pool, bf16_num_pool_pages,
+                             bf16_page_table, K_new, V_new, q, page_table, seq_lens, sink, recent,
+                             out, workspace, num_splits=0, stream=None):
+    """One windowed decode step: append K_new[b], V_new[b] ([B, Hkv, 128] bf16) at
+    position seq_lens[b] - 1 to the INT2 and the BF16 cache, then decode as
+    kvq_decode_window."""
+    batch, max_pages = int(page_table.shape[0]), int(page_table.shape[1])
+    if tuple(bf16_page_table.shape) != (batch, max_pages):
+        raise ValueError("bf16_page_table must have the shape of page_table")
+    _check("kvq_append_decode_window", load_library().kvq_append_decode_window(
+        h.ptr, _ptr(pool, _U8, "pool"), int(num_pool_pages), _ptr(bf16_pool, _U8, "bf16_pool"),
+        int(bf16_num_pool_pages), _ptr(bf16_page_table, _I32, "bf16_page_table"),
+        _ptr(K_new, _BF16, "K_new"), _ptr(V_new, _BF16, "V_new"), _ptr(q, _BF16, "q"),
+        _ptr(page_table, _I32, "page_table"), max_pages, _ptr(seq_lens, _I32, "seq_lens"), batch,
+        int(sink), int(recent), _ptr(out, _F32, "out"), _ptr(workspace, _U8, "workspace"),
+        int(workspace.numel()), int(num_splits), _stream(stream)))
 
 
 def kvq_dequant(h, pool, num_pool_pages, page_table, seq, start, length, K_out=None, V_out=None,

@@ -88,6 +88,8 @@ def test_host_only_paths(lib):
                                  0, None) == 1
     assert lib.kvq_decode_window(None, None, 0, None, 0, None, None, None, 0, None, 0, 64, 256,
                                  None, None, 0, 0, None) == 1
+    assert lib.kvq_append_decode_window(None, None, 0, None, 0, None, None, None, None, None, 0,
+                                        None, 0, 64, 256, None, None, 0, 0, None) == 1
     # a layout with both folding flags is valid; an unknown flag is not
     both = kvq.make_layout(32, 8, out_rotated=True, q_rotated=True)
     assert both.flags == kvq.KVQ_OUT_ROTATED | kvq.KVQ_Q_ROTATED

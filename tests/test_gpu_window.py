@@ -158,3 +158,54 @@ def test_window_rejects_rotated_query(tiny):
         K.kvq_decode_window(cq.h, cq.pool, cq.npool, cb.pool, cb.npool, cb.pt, q, cq.pt, sl, 64,
                             256, out, ws, 2)
     assert e.value.code == K.KVQ_EINVAL
+
+
+def _step_tokens(wl, lens, Hkv):
+    Kn = np.stack([W.token_at(wl, 0, b, 0, int(L))[:Hkv] for b, L in enumerate(lens)])
+    Vn = np.stack([W.token_at(wl, 0, b, 1, int(L))[:Hkv] for b, L in enumerate(lens)])
+    return Kn, Vn
+
+
+@pytest.mark.parametrize("sink,recent,splits", [(64, 256, 0), (5, 37, 3)])
+def test_append_decode_window_equals_separate_calls(sink, recent, splits):
+    """kvq_append_decode_window against kvq_append + kvq_bf16_append +
+    kvq_decode_window on identical caches: both pools byte for byte and the
+    outputs bit for bit, over three steps with ragged lengths and a sequence
+    that takes no token in one step."""
+    from kvq_testlib import i32, u16
+    from rotated_int2_kv_kvq_gb300 import kvq as K
+    wl = W.WORKLOADS["qwen3_8b_32k"]
+    lens = np.concatenate([np.array([0, 1, 15, 16, 17, 300, 1000, 2047]), np.array([700] * 8)])
+    pairs = []
+    for _ in range(2):
+        ci, cb = Cache(wl), Cache(wl, kind="bf16")
+        Ks, Vs = ci.append_range(range(len(lens)), 0, [int(x) for x in lens])
+        for b, L in enumerate(lens):
+            if L:
+                cb.append(Ks[b][:, :ci.Hkv].copy(), Vs[b][:, :ci.Hkv].copy(), np.full(L, b),
+                          np.arange(L))
+        pairs.append((ci, cb))
+    (a, ab), (s, sb) = pairs
+    B = len(lens)
+    for step in range(3):
+        Kn, Vn = _step_tokens(wl, lens, a.Hkv)
+        q = W.queries(wl, 0, 60 + step)
+        lens_after = lens + 1
+        if step == 1:
+            lens_after[0] = 0              # sequence 0 takes no token this step
+        out = torch.empty((B, a.H, 128), dtype=torch.float32, device="cuda")
+        ws = torch.empty(K.kvq_workspace_bytes(a.h, B, splits), dtype=torch.uint8, device="cuda")
+        K.kvq_append_decode_window(a.h, a.pool, a.npool, ab.pool, ab.npool, ab.pt, u16(Kn), u16(Vn),
+                                   u16(q), a.pt, i32(lens_after), sink, recent, out, ws, splits)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        sel = [b for b, L in enumerate(lens_after) if L >= 1]
+        pos = np.array([lens_after[b] - 1 for b in sel])
+        s.append(Kn[sel], Vn[sel], np.array(sel), pos)
+        sb.append(Kn[sel], Vn[sel], np.array(sel), pos)
+        want = window_decode(s, sb, q, lens_after, sink, recent, splits).astype(np.float32)
+        assert np.array_equal(a.pool_host(), s.pool_host()), f"INT2 pool differs at step {step}"
+        assert np.array_equal(ab.pool_host(), sb.pool_host()), f"BF16 pool differs at step {step}"
+        assert np.array_equal(got, want), f"output differs at step {step}"
+        lens = np.maximum(lens_after, lens)
+    assert a.status() == 0 and s.status() == 0 and ab.status() == 0
