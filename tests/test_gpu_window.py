@@ -209,3 +209,27 @@ def test_append_decode_window_equals_separate_calls(sink, recent, splits):
         assert np.array_equal(got, want), f"output differs at step {step}"
         lens = np.maximum(lens_after, lens)
     assert a.status() == 0 and s.status() == 0 and ab.status() == 0
+
+
+def test_append_decode_window_bad_bf16_page_flagged():
+    """A new position whose BF16 page id is out of range: the status bit is set,
+    the BF16 pool is left as it was, the INT2 copy is still stored."""
+    from kvq_testlib import i32, u16
+    from rotated_int2_kv_kvq_gb300 import kvq as K
+    wl = W.WORKLOADS["tiny_1k"]
+    ci = Cache(wl)
+    pt = np.arange(64, dtype=np.int32).reshape(1, 64)
+    pt[0, 10] = 9999                                  # the BF16 page of position 160
+    cb = Cache(wl, kind="bf16", page_table=pt, num_pool_pages=64)
+    Ks, Vs = ci.append_range([0], 0, 160)
+    cb.append(Ks[0][:, :ci.Hkv].copy(), Vs[0][:, :ci.Hkv].copy(), np.zeros(160), np.arange(160))
+    before_b, before_i = cb.pool_host().copy(), ci.pool_host().copy()
+    Kn, Vn = _step_tokens(wl, [160], ci.Hkv)
+    out = torch.empty((1, ci.H, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(K.kvq_workspace_bytes(ci.h, 1, 2), dtype=torch.uint8, device="cuda")
+    K.kvq_append_decode_window(ci.h, ci.pool, ci.npool, cb.pool, cb.npool, cb.pt, u16(Kn), u16(Vn),
+                               u16(W.queries(wl)), ci.pt, i32([161]), 16, 16, out, ws, 2)
+    torch.cuda.synchronize()
+    assert ci.status() & K.KVQ_STATUS_BAD_PAGE
+    assert np.array_equal(cb.pool_host(), before_b)
+    assert not np.array_equal(ci.pool_host(), before_i)
