@@ -76,6 +76,26 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
   }
   bool r_ready = false;
 
+  // The tile's tokens: 16-byte pieces (8 bf16) of [kTile][128], loaded one tile
+  // ahead into registers so that the loads of tile i+1 are in flight while the
+  // rotation of tile i runs.
+  constexpr int kPieces = kTile * (kDim / 8);
+  constexpr int kPre = (kPieces + kAppThreads - 1) / kAppThreads;
+  uint4 pre[kPre];
+  auto load_tile = [&](int t0) {
+#pragma unroll
+    for (int r = 0; r < kPre; ++r) {
+      const int idx = tid + r * kAppThreads;
+      const int k = idx % kTile, ch = idx / kTile;
+      const int tok = t0 + k;
+      pre[r] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx < kPieces && tok < a.n)
+        pre[r] = *reinterpret_cast<const uint4*>(X + (static_cast<size_t>(tok) * a.Hkv + kv) * kDim +
+                                                 ch * 8);
+    }
+  };
+  if (static_cast<long long>(blockIdx.x) * kTile < a.n) load_tile(blockIdx.x * kTile);
+
   for (int tile = blockIdx.x; tile * kTile < a.n; tile += gridDim.x) {
     const int tok0 = tile * kTile;
     // (1) record address of each token of the tile (or -1 if it is skipped)
@@ -100,30 +120,26 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
       }
       rec[tid] = r;      // record byte offset * 16 + slot
     }
-    // (2) load the tile, centre keys (fp32 subtract), store transposed: Cs[j][k]
-    for (int idx = tid; idx < kTile * (kDim / 8); idx += kAppThreads) {
-      const int k = idx % kTile, ch = idx / kTile;
-      const int tok = tok0 + k;
-      float v[8];
-      if (tok < a.n) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(
-            X + (static_cast<size_t>(tok) * a.Hkv + kv) * kDim + ch * 8);
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    // (2) the prefetched tile: centre keys (fp32 subtract), store transposed: Cs[j][k]
+#pragma unroll
+    for (int r = 0; r < kPre; ++r) {
+      const int idx = tid + r * kAppThreads;
+      if (idx < kPieces) {
+        const int k = idx % kTile, ch = idx / kTile;
+        const uint32_t w4[4] = {pre[r].x, pre[r].y, pre[r].z, pre[r].w};
+        float v[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           v[2 * e] = bf16_to_f32(w4[e] & 0xffffu);
           v[2 * e + 1] = bf16_to_f32(w4[e] >> 16);
         }
-        if (mu) {
+        if (mu && tok0 + k < a.n) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) v[e] = __fsub_rn(v[e], mu[ch * 8 + e]);
         }
-      } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+        for (int e = 0; e < 8; ++e) Cs[(ch * 8 + e) * kTile + k] = v[e];
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) Cs[(ch * 8 + e) * kTile + k] = v[e];
     }
     if (!r_ready) {
       // every thread waits (bounded); the CTA leaves together if any gave up
@@ -135,6 +151,8 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
       r_ready = true;
     }
     __syncthreads();
+    // the next tile's tokens, in flight during this tile's rotation
+    if (static_cast<long long>(tile + gridDim.x) * kTile < a.n) load_tile((tile + gridDim.x) * kTile);
 
     // (3) rotate: r_i = fmaf chain over j = 0..127 in order, for TPW tokens x 4 outputs
     float acc[TPW][4];
