@@ -389,7 +389,7 @@ int kvq_decode_static(kvq_handle* h, const void* pool, int num_pool_pages,
  *                and after the last one (keys, then values).
  *   workspace  : device, >= kvq_optr_workspace_bytes(...) bytes, 256-byte aligned.
  * The call returns when the calibration has finished (it synchronises `stream`
- * once per matrix exponential).  Shapes: 1 <= Hkv <= 64, 1 <= Nq <= T,
+ * once per evaluation of an objective, to size the matrix exponential).  Shapes: 1 <= Hkv <= 64, 1 <= Nq <= T,
  * 1 <= G <= 8, Dm >= 1; D is 128. */
 size_t kvq_optr_workspace_bytes(int num_kv_heads, int T, int Nq, int G, int Dm);
 int kvq_optr_calibrate(int num_kv_heads, int T, int Nq, int G, int Dm,

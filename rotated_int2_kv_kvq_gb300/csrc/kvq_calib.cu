@@ -20,7 +20,8 @@
 // gradient with respect to S is the adjoint of the Frechet derivative of exp,
 // L_exp(S^T, G), read from the upper-right block of exp([[S^T, G], [0, S^T]]).
 // The host needs each step's largest |S| to pick the number of squarings, so a
-// calibration call synchronises its stream once per matrix exponential.
+// calibration call synchronises its stream once per objective evaluation (the
+// adjoint's exponential reuses the forward one's norm).
 #include <math.h>
 
 #include <algorithm>
@@ -460,17 +461,19 @@ __global__ void skew_kernel(const float* __restrict__ A, float* __restrict__ S, 
   }
 }
 
-// out = s * op(X) + d * I for kD x kD matrices (op = transpose when tr); head
-// strides sx, so (in floats)
+// out = s * f_h * op(X) + d * I for kD x kD matrices (op = transpose when tr);
+// f_h = hf[2 h] if hf != nullptr, else 1; head strides sx, so (in floats)
 __global__ void scale_kernel(const float* __restrict__ X, long long sx, int tr, float* __restrict__ out,
-                             long long so, float s, float d, int heads) {
+                             long long so, float s, float d, int heads,
+                             const float* __restrict__ hf = nullptr) {
   const long long total = static_cast<long long>(heads) * kD * kD;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long h = i / (kD * kD), k = i % (kD * kD);
     const int r = static_cast<int>(k / kD), c = static_cast<int>(k % kD);
     const float x = X[h * sx + (tr ? c * kD + r : r * kD + c)];
-    out[h * so + r * kD + c] = s * x + (r == c ? d : 0.0f);
+    const float sh = hf ? s * hf[2 * h] : s;
+    out[h * so + r * kD + c] = sh * x + (r == c ? d : 0.0f);
   }
 }
 
@@ -512,6 +515,19 @@ __global__ void __launch_bounds__(1024) norm1_kernel(const float* __restrict__ X
     for (int u = 0; u < 8; ++u) t += part[q][u][c];
     atomicMax(norm + 2 * h + q, __float_as_uint(t));
   }
+}
+
+// Per head, the power of two c = 2^-k (k >= 0) with c |Y|_1 <= 1/4 from the
+// 1-norms of norm1_kernel: dscale[2h] = c, dscale[2h + 1] = 1/c.
+__global__ void dir_scale_kernel(const unsigned int* __restrict__ norm, float* __restrict__ dscale,
+                                 int heads) {
+  const int h = threadIdx.x;
+  if (h >= heads) return;
+  const float ny = __uint_as_float(norm[2 * h + 1]);
+  int k = 0;
+  while (ldexpf(ny, -k) > 0.25f && k < 120) ++k;
+  dscale[2 * h] = ldexpf(1.0f, -k);
+  dscale[2 * h + 1] = ldexpf(1.0f, k);
 }
 
 // out = sum_i c[i] in[i] (+ d I on the first kD x kD block of each head), over
@@ -573,6 +589,7 @@ struct Ctx {
   cudaStream_t st;
   int H, T, Nq, G, Dm;
   cudaError_t err = cudaSuccess;
+  float norm_S = -1.0f;     // max over heads of |S|_1 from the last rotation(), -1 if unknown
   void check() { if (err == cudaSuccess) err = cudaGetLastError(); }
 };
 
@@ -625,6 +642,7 @@ struct Ws {
   float *X2, *P2, *Q2;                              // 4 [D][D] each (expm scratch pairs)
   float *kl, *errsum;                               // [H]
   unsigned int* norm;                               // [2H]
+  float* dscale;                                    // [2H] direction scale and its inverse
   uint8_t* flag;                                    // [T][D]
   int *amax, *amin;                                 // [T]
   size_t total;
@@ -673,6 +691,7 @@ Ws carve(uint8_t* base, int H, int T, int Nq, int G, int Dm) {
   w.kl = reinterpret_cast<float*>(take(hd * 4));
   w.errsum = reinterpret_cast<float*>(take(hd * 4));
   w.norm = reinterpret_cast<unsigned int*>(take(hd * 8));
+  w.dscale = reinterpret_cast<float*>(take(hd * 8));
   w.flag = take(hd * T * kD);
   w.amax = reinterpret_cast<int*>(take(hd * T * 4));
   w.amin = reinterpret_cast<int*>(take(hd * T * 4));
@@ -694,36 +713,45 @@ Ws carve(uint8_t* base, int H, int T, int Nq, int G, int Dm) {
 // each product is three kD x kD products instead of one of twice the size.
 // Then `out` receives the upper-right block of the exponential, the Frechet
 // derivative of exp at M in the direction Mb.  That block is linear in Mb, so
-// Mb enters scaled by a power of two c with c |Mb|_1 <= 1/4 and the result is
-// divided by c: the direction does not add squarings.
+// Mb enters scaled by a power of two c_h with c_h |Mb_h|_1 <= 1/4 (chosen on the
+// device) and the result is divided by c_h: the direction does not add
+// squarings.
 //
 // M (or its transpose, trM) and Mb have head stride kD * kD; the scratch pairs
-// live in the (4 kD^2 per head) buffers X2, P2, Q2.  Reads the 1-norms (syncs
-// the stream).
+// live in the (4 kD^2 per head) buffers X2, P2, Q2.  The number of squarings
+// comes from the 1-norm of M, read on the host (a stream synchronisation)
+// except for the adjoint's M = S^T right after the forward exponential of the
+// same S, whose norm is remembered in c.norm_S.
 void expm(Ctx& c, Ws& w, const float* M, int trM, const float* Mb, float* out) {
   if (c.err != cudaSuccess) return;
   const long long DD = static_cast<long long>(kD) * kD, S4 = 4 * DD;
   const bool pair = Mb != nullptr;
   c.err = cudaMemsetAsync(w.norm, 0, 2 * c.H * sizeof(unsigned int), c.st);
   norm1_kernel<<<dim3(1, c.H), 8 * kD, 0, c.st>>>(M, Mb, DD, w.norm);
+  // the direction's per-head scale c_h (c_h |Mb_h|_1 <= 1/4) is set on the device
+  if (pair) dir_scale_kernel<<<1, 64, 0, c.st>>>(w.norm, w.dscale, c.H);
   c.check();
-  std::vector<unsigned int> nb(2 * c.H);
-  if (c.err == cudaSuccess)
-    c.err = cudaMemcpyAsync(nb.data(), w.norm, 2 * c.H * sizeof(unsigned int), cudaMemcpyDeviceToHost,
-                            c.st);
-  if (c.err == cudaSuccess) c.err = cudaStreamSynchronize(c.st);
-  if (c.err != cudaSuccess) return;
-  std::vector<float> nx(c.H), ny(c.H);
-  float nymax = 0.0f;
-  for (int h = 0; h < c.H; ++h) {
-    memcpy(&nx[h], &nb[2 * h], 4);
-    memcpy(&ny[h], &nb[2 * h + 1], 4);
-    nymax = std::max(nymax, ny[h]);
-  }
-  int kb = 0;                                   // direction scale c = 2^-kb
-  while (pair && nymax * ldexpf(1.0f, -kb) > 0.25f && kb < 120) ++kb;
   float nmax = 0.0f;
-  for (int h = 0; h < c.H; ++h) nmax = std::max(nmax, nx[h] + (pair ? ldexpf(ny[h], -kb) : 0.0f));
+  if (pair && c.norm_S >= 0.0f) {
+    // M = S^T and |S^T|_1 = |S|_1 (S is skew), known from this step's forward
+    // exponential: no host read needed, the block matrix's norm is at most
+    // |S|_1 + 1/4
+    nmax = c.norm_S + 0.25f;
+  } else {
+    std::vector<unsigned int> nb(2 * c.H);
+    if (c.err == cudaSuccess)
+      c.err = cudaMemcpyAsync(nb.data(), w.norm, 2 * c.H * sizeof(unsigned int),
+                              cudaMemcpyDeviceToHost, c.st);
+    if (c.err == cudaSuccess) c.err = cudaStreamSynchronize(c.st);
+    if (c.err != cudaSuccess) return;
+    for (int h = 0; h < c.H; ++h) {
+      float f;
+      memcpy(&f, &nb[2 * h], 4);
+      nmax = std::max(nmax, f);
+    }
+    if (!pair) c.norm_S = trM ? -1.0f : nmax;
+    if (pair) nmax += 0.25f;
+  }
   int j = 0;
   while (nmax / ldexpf(1.0f, j) > 0.5f && j < 60) ++j;
   const float sc = ldexpf(1.0f, -j);
@@ -737,7 +765,7 @@ void expm(Ctx& c, Ws& w, const float* M, int trM, const float* Mb, float* out) {
   float* F = w.Q2;
   float* B1 = w.Q2 + 2 * DD;
   scale_kernel<<<g, 256, 0, c.st>>>(M, DD, trM, X1, S4, sc, 0.0f, c.H);             // X = M / 2^j
-  if (pair) scale_kernel<<<g, 256, 0, c.st>>>(Mb, DD, 0, X1 + DD, S4, ldexpf(sc, -kb), 0.0f, c.H);
+  if (pair) scale_kernel<<<g, 256, 0, c.st>>>(Mb, DD, 0, X1 + DD, S4, sc, 0.0f, c.H, w.dscale);
   c.check();
   // C = alpha A B + beta C (+ diag I on u), A B as pairs when `pair`
   auto prod = [&](const float* A, const float* B, float* C, float alpha, float beta, float diag) {
@@ -778,8 +806,8 @@ void expm(Ctx& c, Ws& w, const float* M, int trM, const float* Mb, float* out) {
     prod(cur, cur, nxt, 1.0f, 2.0f, 0.0f);
     std::swap(cur, nxt);
   }
-  if (pair)
-    scale_kernel<<<g, 256, 0, c.st>>>(cur + DD, S4, 0, out, DD, ldexpf(1.0f, kb), 0.0f, c.H);
+  if (pair)   // undo the direction's scale
+    scale_kernel<<<g, 256, 0, c.st>>>(cur + DD, S4, 0, out, DD, 1.0f, 0.0f, c.H, w.dscale + 1);
   else
     scale_kernel<<<g, 256, 0, c.st>>>(cur, S4, 0, out, DD, 1.0f, 1.0f, c.H);        // F + I
   c.check();
