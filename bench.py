@@ -227,6 +227,51 @@ def cpu_oracle_rate(wl, min_seconds=10.0, max_steps=None, warmup=0, max_seconds=
     return bytes_per_step * n / el / 1e9, n, el
 
 
+def _oracle_proc(wl_name, seq, kv, seconds, barrier, q):
+    """One process of the all-cores oracle baseline: build the (seq, kv) sample,
+    wait for the others, then run oracle steps for `seconds`."""
+    wl = W.WORKLOADS[wl_name]
+    s = oracle_sample_setup(wl, seq, kv)
+    oracle_step(wl, s)
+    barrier.wait(timeout=600)
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        oracle_step(wl, s)
+        n += 1
+    q.put((n, time.perf_counter() - t0))
+
+
+def cpu_oracle_rate_all_cores(wl, seconds=10.0):
+    """The same oracle step on every core this process may run on, one process
+    per core, each on its own (sequence, KV head) sample, started together
+    (spawned processes: CUDA is already initialised here).  Returns (cache GB/s
+    over all processes, processes, steps, seconds) or None if a process failed."""
+    import multiprocessing as mp
+
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    ctx = mp.get_context("spawn")
+    barrier, q = ctx.Barrier(cores), ctx.Queue()
+    units = [(u % wl.batch, (u // wl.batch) % wl.num_kv_heads) for u in range(cores)]
+    procs = [ctx.Process(target=_oracle_proc, args=(wl.name, sq, kv, seconds, barrier, q))
+             for sq, kv in units]
+    for p in procs:
+        p.start()
+    try:
+        res = [q.get(timeout=900) for _ in procs]
+    except Exception:
+        res = None
+    for p in procs:
+        p.join(timeout=60)
+        if p.is_alive():
+            p.kill()
+    if not res or any(p.exitcode != 0 for p in procs):
+        return None
+    steps = sum(n for n, _ in res)
+    wall = max(el for _, el in res)
+    bytes_per_step = wl.ctx * W.cache_bytes_per_token_head("int2")
+    return bytes_per_step * steps / wall / 1e9, cores, steps, wall
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -529,6 +574,12 @@ def run_ours(args):
                "sample": f"float64 oracle on sequence 0 / KV head 0: re-quantise one token and "
                          f"decode {H // Hkv} query heads over {ctx} tokens per step, "
                          f"{n_cpu} steps in {el_cpu:.1f} s"}
+        allc = cpu_oracle_rate_all_cores(wl, seconds=10.0)
+        if allc is not None:
+            cpu["all_cores"] = {"value": allc[0], "unit": UNIT, "cores": allc[1], "kind": "oracle",
+                                "sample": f"the same step, one process per core on its own "
+                                          f"(sequence, KV head): {allc[2]} steps in "
+                                          f"{allc[3]:.1f} s"}
 
     launches = 3 * args.steps       # append + q-rotation, split-K attention, split merge
     line = {
