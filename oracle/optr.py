@@ -21,7 +21,7 @@ pith.science review of arXiv 2608.02691):
     keys before values; the objective is taken over the last 64 query
     positions of a calibration chunk (causal attention).
 
-Readings where the pages are silent (listed in the design notes too):
+Readings where the pages are silent:
   * KL(p || p~) with p the attention of the unquantised keys (teacher);
   * the losses are averaged over the calibration queries; the KL is summed
     over the G query heads of the KV head, and the post-W_O error of a query is
@@ -163,7 +163,7 @@ def key_loss(A, R0, K, V, Q, W, mu, clip, lam=1.0, scale=None, mode="int2"):
     g_r = quantise_backward(g_rt, info)
     g_R += kc.T @ g_r
     g_S = expm_adjoint(S, R0.T @ g_R)
-    return L, g_S - g_S.T, {"kl": kl, "err": err, "pt": pt, "R": R}
+    return L, g_S - g_S.T, {"kl": kl, "err": err, "pt": pt, "R": R, "e": e}
 
 
 def value_loss(A, R0, V, pt, W, clip, mode="int2"):
@@ -186,7 +186,7 @@ def value_loss(A, R0, V, pt, W, clip, mode="int2"):
     g_r = quantise_backward(g_rt, info)
     g_R += V.T @ g_r
     g_S = expm_adjoint(S, R0.T @ g_R)
-    return L, g_S - g_S.T, {"R": R}
+    return L, g_S - g_S.T, {"R": R, "e": e}
 
 
 # ---- Adam and the calibration loop ----------------------------------------------

@@ -8,8 +8,7 @@ against the float64 oracle (oracle/optr.py) on synthetic calibration traces.
 * a short calibration: the loss history within 1e-2 of the oracle's (Adam's
   first steps follow the gradient's signs, so entries whose gradient is near
   zero may step differently), the calibrated rotations orthogonal to 1e-5;
-* a longer calibration lowers the key objective of every head and the mean
-  value objective.
+* a longer calibration lowers both objectives of every head.
 """
 import numpy as np
 import pytest
@@ -101,10 +100,9 @@ def test_calibration_lowers_both_objectives():
                                    wl.clip_k, wl.clip_v, lr=1e-3, steps=40)
     hist = hist.cpu().numpy()
     assert np.all(hist[0, -1] < 0.8 * hist[0, 0]), hist[0]
-    # Adam on a straight-through objective is not monotone: the mean falls and
-    # every head reaches a lower value loss than its start
-    assert hist[1, -1].mean() < hist[1, 0].mean(), hist[1]
-    assert np.all(hist[1, 1:].min(axis=0) < hist[1, 0]), hist[1]
+    # every head ends below its start (the float64 oracle on these traces ends
+    # at 0.53-0.78 of the start: no head is near the bound)
+    assert np.all(hist[1, -1] < hist[1, 0]), hist[1]
     Rn = R.cpu().numpy().astype(np.float64)
     for which in range(2):
         for h in range(4):

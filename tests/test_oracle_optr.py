@@ -162,3 +162,71 @@ def test_rotation_stays_orthogonal_and_calibration_lowers_the_losses():
     for R in (RK, RV):
         assert np.abs(R.T @ R - np.eye(D)).max() < 1e-12
     assert h["key"][-1] < h["key"][0] and h["value"][-1] < h["value"][0]
+
+
+def _attend(Q, Kx, Vx, W, scale):
+    """Post-W_O outputs y [Nq, Dm] of causal attention, by explicit loops:
+    y_q = sum_h (sum_t p_qht v_t) W[h]^T."""
+    T = Kx.shape[0]
+    Nq, G, _ = Q.shape
+    y = np.zeros((Nq, W.shape[1]))
+    P = np.zeros((Nq, G, T))
+    for i in range(Nq):
+        pos = T - Nq + i
+        for h in range(G):
+            logit = np.array([scale * (Q[i, h] @ Kx[t]) for t in range(pos + 1)])
+            w = np.exp(logit - logit.max())
+            w /= w.sum()
+            P[i, h, :pos + 1] = w
+            o = sum(w[t] * Vx[t] for t in range(pos + 1))
+            y[i] += W[h] @ o
+    return y, P
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_objectives_follow_the_post_wo_error_decomposition(seed):
+    """Eq. 8 ("What carries the argument"): with k~, v~ the dequantised keys and
+    values, y~ - y = (sum_t (p~_t - p_t) v_t) W_O^T + (sum_t p~_t (v~_t - v_t)) W_O^T.
+    The two error vectors the objectives use are checked against y~ - y built
+    from attention computed by loops, which pins their signs, which attention
+    each term is taken at and the normalisation of both losses and of the KL."""
+    import scipy.linalg
+    K, V, Q, W, mu, R0, A = _case(seed, G=3)
+    rng = np.random.default_rng(40 + seed)
+    R0v = _orth(rng, K.shape[1])
+    B = rng.standard_normal(A.shape) * 0.05
+    clip_k, clip_v, lam = 0.96, 0.92, 0.7
+    D = K.shape[1]
+    scale = 1.0 / np.sqrt(D)
+    Nq = Q.shape[0]
+    Lk, _, ak = optr.key_loss(A, R0, K, V, Q, W, mu, clip_k, lam=lam)
+    Lv, _, av = optr.value_loss(B, R0v, V, ak["pt"], W, clip_v)
+    # dequantised keys and values, rotations built here from their definition
+    RK = R0 @ scipy.linalg.expm(A - A.T)
+    RV = R0v @ scipy.linalg.expm(B - B.T)
+    kt = optr.quantise((K - mu) @ RK, clip_k)[0] @ RK.T + mu
+    vt = optr.quantise(V @ RV, clip_v)[0] @ RV.T
+    y, p = _attend(Q, K, V, W, scale)
+    y_k, pt = _attend(Q, kt, V, W, scale)          # keys quantised, values exact
+    y_kv, _ = _attend(Q, kt, vt, W, scale)         # both quantised
+    dy = y_kv - y
+    tol = 1e-12 * np.linalg.norm(dy)
+    assert np.linalg.norm(pt - ak["pt"]) <= 1e-12 * np.linalg.norm(pt)
+    assert np.linalg.norm(ak["e"] - (y_k - y)) <= tol          # key-induced term
+    assert np.linalg.norm(av["e"] - (y_kv - y_k)) <= tol       # value-induced term
+    assert np.linalg.norm(ak["e"] + av["e"] - dy) <= tol
+    # the same split with the attention of exact keys and an explicit cross term
+    y_v, _ = _attend(Q, K, vt, W, scale)
+    cross = dy - (y_k - y) - (y_v - y)
+    assert np.linalg.norm((y_k - y) + (y_v - y) + cross - dy) <= tol
+    assert np.linalg.norm(cross) > 1e-6 * np.linalg.norm(dy)   # the cross term is not zero
+    # normalisation: mean over queries of squared norms; KL summed over heads
+    err_k = (np.linalg.norm(y_k - y, axis=1) ** 2).mean()
+    err_v = (np.linalg.norm(y_kv - y_k, axis=1) ** 2).mean()
+    kl = sum(p[i, h, t] * np.log(p[i, h, t] / pt[i, h, t])
+             for i in range(Nq) for h in range(Q.shape[1]) for t in range(K.shape[0])
+             if p[i, h, t] > 0) / Nq
+    assert abs(ak["err"] - err_k) <= 1e-12 * err_k
+    assert abs(ak["kl"] - kl) <= 1e-10 * kl
+    assert abs(Lk - (kl + lam * err_k)) <= 1e-10 * Lk
+    assert abs(Lv - err_v) <= 1e-12 * err_v
