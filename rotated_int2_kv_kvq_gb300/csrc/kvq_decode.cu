@@ -17,8 +17,9 @@
 // serves KV head w / (8/HPC) of the group and takes every (8/HPC)-th page of
 // the split.  Each warp streams its own pages through its own ring of stages:
 // lane 0 issues 1-D TMA bulk copies (cp.async.bulk, mbarrier completion) of the
-// head's 1152-byte records, two pages per stage (two independent tensor-core
-// chains in flight), and refills a stage as soon as the warp has read it.  No
+// head's 1152-byte records, four pages per stage and two stages per warp, and
+// refills a stage as soon as the warp has read it.  The warp takes a stage's
+// pages in pairs (two independent tensor-core chains in flight).  No
 // stage is shared between warps, so a warp that runs ahead never waits for a
 // slower one (sharing one copy of a page between the CTA's heads made every
 // warp keep the pace of the slowest and cost 6 %).  A page record holds the 16
@@ -40,6 +41,7 @@
 #include "kvq_internal.cuh"
 
 #include <math.h>
+
 
 namespace kvq {
 
@@ -476,30 +478,24 @@ __device__ __forceinline__ void half2_residuals(uint32_t X, float P0, float P1, 
 // B fragments of the value product from this lane's weights of tokens g and
 // g+8 (head t): column 2*head holds the fp16 weight, column 2*head+1 the fp16
 // residual P - fp16(P) (at most 2^-11 P; for weights below 2^-3 it is an fp16
-// subnormal, a negligible loss next to the weight itself).  Lane (g, t) needs
-// head g>>1, tokens 2t, 2t+1, 2t+8, 2t+9, held by lanes 4*(2t) + (g>>1) and
-// 4*(2t+1) + (g>>1).
-__device__ __forceinline__ void weights_to_b(float P0, float P1, int g, int t, uint32_t& pb0,
-                                             uint32_t& pb1) {
+// subnormal, a negligible loss next to the weight itself).  The lane's pairs
+// {weight, residual} of token g (and of token g+8) are row g, columns 2t and
+// 2t+1 of an 8 x 8 matrix of 16-bit values (rows = tokens, columns = 2*head +
+// part) in mma fragment order; its transpose (movmatrix) gives lane (g, t)
+// tokens 2t and 2t+1 of column g, which is the B fragment.
+__device__ __forceinline__ void weights_to_b(float P0, float P1, uint32_t& pb0, uint32_t& pb1) {
   const uint32_t X = pack_half2(P0, P1);
   float r0, r1;
   half2_residuals(X, P0, P1, r0, r1);
   const uint32_t Y = pack_half2(r0, r1);
-  const int src0 = 4 * (2 * t) + (g >> 1);
-  const uint32_t xa = __shfl_sync(0xffffffffu, X, src0);
-  const uint32_t ya = __shfl_sync(0xffffffffu, Y, src0);
-  const uint32_t xb = __shfl_sync(0xffffffffu, X, src0 + 4);
-  const uint32_t yb = __shfl_sync(0xffffffffu, Y, src0 + 4);
-  const uint32_t va = (g & 1) ? ya : xa;
-  const uint32_t vb = (g & 1) ? yb : xb;
-  pb0 = __byte_perm(va, vb, 0x5410);
-  pb1 = __byte_perm(va, vb, 0x7632);
+  pb0 = movmatrix_trans(__byte_perm(X, Y, 0x5410));
+  pb1 = movmatrix_trans(__byte_perm(X, Y, 0x7632));
 }
 
 // Weights are kept <= 2^kLazy relative to the running max before it is raised.
 constexpr float kLazy = 8.0f;
 
-// Online-softmax update with the two pages (A, B) of one stage for this lane:
+// Online-softmax update with one pair of pages (A, B) of a stage for this lane:
 // scores, running max, weights, value accumulation.  kMasked = false is the
 // common case of two full, valid pages: no per-token masks at all.
 struct WarpState {
@@ -546,13 +542,13 @@ __device__ __forceinline__ void process_pair(WarpState& st, const uint32_t (&qf)
     static_assert(kLazy == 8.0f, "P <= 2^14 is p * s_v <= 2^kLazy with the 2^6 scale");
     const float sva0 = half_lo(mta.z), sva1 = half_lo(mta.w);
     const float svb0 = half_lo(mtb.z), svb1 = half_lo(mtb.w);
+    constexpr float kSvMin = 0x1p-24f;
+    const float sa0 = fmaxf(sva0, kSvMin), sa1 = fmaxf(sva1, kSvMin);
+    const float sb0 = fmaxf(svb0, kSvMin), sb1 = fmaxf(svb1, kSvMin);
     float pa0 = va0 ? fast_exp2(la0 - m_run) : 0.0f;
     float pa1 = va1 ? fast_exp2(la1 - m_run) : 0.0f;
     float pb0v = vb0 ? fast_exp2(lb0 - m_run) : 0.0f;
     float pb1v = vb1 ? fast_exp2(lb1 - m_run) : 0.0f;
-    constexpr float kSvMin = 0x1p-24f;
-    const float sa0 = fmaxf(sva0, kSvMin), sa1 = fmaxf(sva1, kSvMin);
-    const float sb0 = fmaxf(svb0, kSvMin), sb1 = fmaxf(svb1, kSvMin);
     float Pa0 = va0 ? pa0 * sa0 : 0.0f, Pa1 = va1 ? pa1 * sa1 : 0.0f;
     float Pb0 = vb0 ? pb0v * sb0 : 0.0f, Pb1 = vb1 ? pb1v * sb1 : 0.0f;
     const float cmax = fmaxf(fmaxf(Pa0, Pa1), fmaxf(Pb0, Pb1));
@@ -594,48 +590,57 @@ __device__ __forceinline__ void process_pair(WarpState& st, const uint32_t (&qf)
 
     // ---- values of both pages
     uint32_t fa0, fa1, fb0, fb1;
-    weights_to_b(Pa0, Pa1, g, t, fa0, fa1);
-    weights_to_b(Pb0, Pb1, g, t, fb0, fb1);
+    weights_to_b(Pa0, Pa1, fa0, fa1);
+    weights_to_b(Pb0, Pb1, fb0, fb1);
     page_values(vwa, fa0, fa1, acc);
     page_values(vwb, fb0, fb1, acc);
 }
 
 constexpr int kW = kInt2Warps;                 // warps per CTA
-constexpr int kNS = 4;                         // pipeline stages
+constexpr int kPPS = 4;                        // pages per stage (two pairs)
+constexpr int kNS = 2;                         // pipeline stages per warp
 constexpr int kMaxIds = 1024;                  // page ids staged per sub-chunk
 
 // Every warp streams its own KV head's records through its own ring: no stage
 // is shared between warps, so no warp waits for another to release a slot.
-struct Int2Smem {
-  uint8_t ring[kW][kNS][2 * kInt2Rec];
-  uint64_t full[kW][kNS];
-  int ids[kMaxIds];
+struct Int2Merge {
   float o[kW][kMaxG][kDim];
   float m[kW][kMaxG];
   float l[kW][kMaxG];
 };
+struct Int2Smem {
+  union {
+    uint8_t ring[kW][kNS][kPPS * kInt2Rec];
+    Int2Merge mg;
+  };
+  uint64_t full[kW][kNS];
+  int ids[kMaxIds];
+};
 
-// Fill stage k of warp `warp` (pages 2k and 2k+1 of the warp's share of the
-// sub-chunk: local page index gi + GPH * j).  Lane 0 only.
+// Fill stage k of warp `warp` (pages kPPS*k .. kPPS*k + kPPS - 1 of the warp's
+// share of the sub-chunk: local page index gi + GPH * j), one bulk copy per
+// page.  Lane 0 only.
 __device__ __forceinline__ void issue_warp_stage(Int2Smem& sm, const DecodeArgs& a, int warp, int k,
                                                  int slot, int npw, int gi, int GPH, int kv) {
-  const int j0 = 2 * k, j1 = j0 + 1;
-  const int li0 = gi + GPH * j0, li1 = gi + GPH * j1;
-  const int id0 = j0 < npw ? sm.ids[li0] : -1;
-  const int id1 = j1 < npw ? sm.ids[li1] : -1;
-  const uint32_t bytes = (id0 >= 0 ? kInt2Rec : 0) + (id1 >= 0 ? kInt2Rec : 0);
+  int id[kPPS];
+  uint32_t bytes = 0;
+#pragma unroll
+  for (int u = 0; u < kPPS; ++u) {
+    const int j = kPPS * k + u;
+    id[u] = j < npw ? sm.ids[gi + GPH * j] : -1;
+    bytes += id[u] >= 0 ? kInt2Rec : 0;
+  }
   const uint32_t bar = smem_u32(&sm.full[warp][slot]);
   if (bytes == 0) {
     mbar_arrive(bar);
     return;
   }
   mbar_arrive_expect_tx(bar, bytes);
-  if (id0 >= 0)
-    bulk_g2s(smem_u32(&sm.ring[warp][slot][0]),
-             a.pool + (static_cast<size_t>(id0) * a.Hkv + kv) * kInt2Rec, kInt2Rec, bar);
-  if (id1 >= 0)
-    bulk_g2s(smem_u32(&sm.ring[warp][slot][kInt2Rec]),
-             a.pool + (static_cast<size_t>(id1) * a.Hkv + kv) * kInt2Rec, kInt2Rec, bar);
+#pragma unroll
+  for (int u = 0; u < kPPS; ++u)
+    if (id[u] >= 0)
+      bulk_g2s(smem_u32(&sm.ring[warp][slot][u * kInt2Rec]),
+               a.pool + (static_cast<size_t>(id[u]) * a.Hkv + kv) * kInt2Rec, kInt2Rec, bar);
 }
 
 __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
@@ -720,7 +725,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     }
     const bool all_ids_ok = __syncthreads_and(ids_ok);
     const int npw = nsub > gi ? (nsub - gi + GPH - 1) / GPH : 0;   // this warp's pages
-    const int nst = (npw + 1) >> 1;
+    const int nst = (npw + kPPS - 1) / kPPS;
     if (lane == 0)
       for (int k = 0; k < kNS && k < nst; ++k)
         issue_warp_stage(sm, a, warp, k, (gs + k) % kNS, npw, gi, GPH, kv);
@@ -732,36 +737,44 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
         timed_out = true;
         break;
       }
-      const int ua = gi + GPH * (2 * k), ub = ua + GPH;
-      // both pages present, valid and all their tokens in [lo, hi)
-      const bool full = all_ids_ok && 2 * k + 1 < npw && (p0 + sub + ub + 1) * kPage <= hi &&
-                        (p0 + sub + ua) * kPage >= lo;
-      const uint8_t* sta = &sm.ring[warp][slot][0];
-      const uint8_t* stb = &sm.ring[warp][slot][kInt2Rec];
-      const uint4 kwa = *reinterpret_cast<const uint4*>(sta + 16 * lane);
-      const uint4 vwa = *reinterpret_cast<const uint4*>(sta + 512 + 16 * lane);
-      const uint4 mta = *reinterpret_cast<const uint4*>(sta + 1024 + 16 * g);
-      const uint4 kwb = *reinterpret_cast<const uint4*>(stb + 16 * lane);
-      const uint4 vwb = *reinterpret_cast<const uint4*>(stb + 512 + 16 * lane);
-      const uint4 mtb = *reinterpret_cast<const uint4*>(stb + 1024 + 16 * g);
-      __syncwarp();
-      if (lane == 0 && k + kNS < nst) {
-        fence_proxy_async();
-        issue_warp_stage(sm, a, warp, k + kNS, slot, npw, gi, GPH, kv);
-      }
-      if (full) {
-        process_pair<false>(ws, qf, kappa, zeta, g, t, kwa, vwa, mta, kwb, vwb, mtb, true, true,
-                            true, true);
-      } else {
-        const bool oka = 2 * k < npw && sm.ids[ua] >= 0;
-        const bool okb = 2 * k + 1 < npw && sm.ids[ub] >= 0;
-        const int posa = (p0 + sub + ua) * kPage, posb = (p0 + sub + ub) * kPage;
-        const bool va0 = oka && posa + g >= lo && posa + g < hi;
-        const bool va1 = oka && posa + g + 8 >= lo && posa + g + 8 < hi;
-        const bool vb0 = okb && posb + g >= lo && posb + g < hi;
-        const bool vb1 = okb && posb + g + 8 >= lo && posb + g + 8 < hi;
-        process_pair<true>(ws, qf, kappa, zeta, g, t, kwa, vwa, mta, kwb, vwb, mtb, va0, va1, vb0,
-                           vb1);
+      static_assert(kPPS % 2 == 0, "stages hold whole pairs of pages");
+#pragma unroll
+      for (int h = 0; h < kPPS / 2; ++h) {
+        const int j = kPPS * k + 2 * h;            // the warp's page index of page a
+        const int ua = gi + GPH * j, ub = ua + GPH;
+        const uint8_t* sta = &sm.ring[warp][slot][2 * h * kInt2Rec];
+        const uint8_t* stb = sta + kInt2Rec;
+        const uint4 kwa = *reinterpret_cast<const uint4*>(sta + 16 * lane);
+        const uint4 vwa = *reinterpret_cast<const uint4*>(sta + 512 + 16 * lane);
+        const uint4 mta = *reinterpret_cast<const uint4*>(sta + 1024 + 16 * g);
+        const uint4 kwb = *reinterpret_cast<const uint4*>(stb + 16 * lane);
+        const uint4 vwb = *reinterpret_cast<const uint4*>(stb + 512 + 16 * lane);
+        const uint4 mtb = *reinterpret_cast<const uint4*>(stb + 1024 + 16 * g);
+        if (h == kPPS / 2 - 1) {
+          __syncwarp();
+          if (lane == 0 && k + kNS < nst) {
+            fence_proxy_async();
+            issue_warp_stage(sm, a, warp, k + kNS, slot, npw, gi, GPH, kv);
+          }
+        }
+        if (j >= npw) continue;
+        // both pages present, valid and all their tokens in [lo, hi)
+        const bool full = all_ids_ok && j + 1 < npw && (p0 + sub + ub + 1) * kPage <= hi &&
+                          (p0 + sub + ua) * kPage >= lo;
+        if (full) {
+          process_pair<false>(ws, qf, kappa, zeta, g, t, kwa, vwa, mta, kwb, vwb, mtb, true, true,
+                              true, true);
+        } else {
+          const bool oka = sm.ids[ua] >= 0;
+          const bool okb = j + 1 < npw && sm.ids[ub] >= 0;
+          const int posa = (p0 + sub + ua) * kPage, posb = (p0 + sub + ub) * kPage;
+          const bool va0 = oka && posa + g >= lo && posa + g < hi;
+          const bool va1 = oka && posa + g + 8 >= lo && posa + g + 8 < hi;
+          const bool vb0 = okb && posb + g >= lo && posb + g < hi;
+          const bool vb1 = okb && posb + g + 8 >= lo && posb + g + 8 < hi;
+          process_pair<true>(ws, qf, kappa, zeta, g, t, kwa, vwa, mta, kwb, vwb, mtb, va0, va1,
+                             vb0, vb1);
+        }
       }
     }
     gs += nst;
@@ -816,12 +829,12 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
       const float inv = (mb & 1) ? kInvOdd : kInvEven;
-      sm.o[warp][t][16 * mb + g] = fmaf(ws.acc[mb][1] + ws.acc[mb][0], inv, ws.z_run * 0x1p-6f);
-      sm.o[warp][t][16 * mb + g + 8] = fmaf(ws.acc[mb][3] + ws.acc[mb][2], inv, ws.z_run * 0x1p-6f);
+      sm.mg.o[warp][t][16 * mb + g] = fmaf(ws.acc[mb][1] + ws.acc[mb][0], inv, ws.z_run * 0x1p-6f);
+      sm.mg.o[warp][t][16 * mb + g + 8] = fmaf(ws.acc[mb][3] + ws.acc[mb][2], inv, ws.z_run * 0x1p-6f);
     }
     if (g == 0) {
-      sm.m[warp][t] = ws.m_run + 6.0f;
-      sm.l[warp][t] = ws.l_run * 0x1p-6f;
+      sm.mg.m[warp][t] = ws.m_run + 6.0f;
+      sm.mg.l[warp][t] = ws.l_run * 0x1p-6f;
     }
   }
   __syncthreads();
@@ -830,15 +843,15 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     const int h2 = idx / kDim, d = idx % kDim;
     for (int h = 0; h < a.G; ++h) {
       float M = -INFINITY;
-      for (int u = 0; u < GPH; ++u) M = fmaxf(M, sm.m[h2 * GPH + u][h]);
+      for (int u = 0; u < GPH; ++u) M = fmaxf(M, sm.mg.m[h2 * GPH + u][h]);
       float L = 0.0f, o = 0.0f;
       if (M > -INFINITY) {
         for (int u = 0; u < GPH; ++u) {
           const int w = h2 * GPH + u;
-          if (sm.m[w][h] == -INFINITY) continue;
-          const float f = fast_exp2(sm.m[w][h] - M);
-          L = fmaf(f, sm.l[w][h], L);
-          o = fmaf(f, sm.o[w][h][d], o);
+          if (sm.mg.m[w][h] == -INFINITY) continue;
+          const float f = fast_exp2(sm.mg.m[w][h] - M);
+          L = fmaf(f, sm.mg.l[w][h], L);
+          o = fmaf(f, sm.mg.o[w][h][d], o);
         }
       }
       float* p = a.part + ((static_cast<size_t>(b) * a.H + (hg * HPC + h2) * a.G + h) * a.splits + split) *
