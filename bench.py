@@ -51,6 +51,8 @@ def parse():
                     help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison kernel")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (tiny_1k, long_128k, ragged_64, full_stack_36l)")
     return ap.parse_args()
 
 
@@ -98,6 +100,38 @@ def whole_job_rate(units_per_rank, max_ms, world):
     """Weak scaling: every rank processes units_per_rank; the job takes the
     slowest rank's time."""
     return units_per_rank * world / (max_ms * 1e-3)
+
+
+def l2_bytes(torch):
+    """L2 cache size of the current device (cudaDevAttrL2CacheSize)."""
+    prop = torch.cuda.get_device_properties(torch.cuda.current_device())
+    v = getattr(prop, "L2_cache_size", 0)
+    if v:
+        return int(v)
+    import ctypes
+
+    rt = ctypes.CDLL("libcudart.so")
+    out = ctypes.c_int(0)
+    rt.cudaDeviceGetAttribute(ctypes.byref(out), 89, torch.cuda.current_device())
+    return int(out.value)
+
+
+def replicas_for(bytes_per_step, l2):
+    """Copies of a cache that one timed loop cycles through so that successive
+    steps never find their cache in L2: enough for at least twice the L2 size."""
+    if bytes_per_step >= 2 * l2:
+        return 1
+    return int(min(4096, -(-2 * l2 // max(1, bytes_per_step))))
+
+
+def l2_note(bytes_per_step, replicas, l2):
+    mb = bytes_per_step / 1e6
+    if replicas > 1:
+        return (f"cache {mb:.2f} MB per step is smaller than twice L2 ({l2 / 1e6:.1f} MB): "
+                f"steps cycle through {replicas} replicas ({replicas * mb:.0f} MB), no flush")
+    if bytes_per_step >= 2 * l2:
+        return f"inputs larger than L2: {mb:.0f} MB of cache per step vs L2 {l2 / 1e6:.1f} MB, no flush"
+    return f"cache {mb:.0f} MB per step vs L2 {l2 / 1e6:.1f} MB (between 1x and 2x L2), no flush"
 
 
 class Clocks:
@@ -181,7 +215,7 @@ def oracle_sample_setup(wl, seq=0, kv=0):
     """One (sequence, KV head) of the workload, built by the oracle alone."""
     import oracle
 
-    ctx = wl.ctx
+    ctx = int(W.seq_lens(wl)[seq])
     pages = ctx // 16
     pt = np.arange(pages, dtype=np.int32)[None, :]
     pool = np.zeros(pages * 1152, np.uint8)
@@ -193,25 +227,26 @@ def oracle_sample_setup(wl, seq=0, kv=0):
                        wl.clip_k, wl.clip_v)
     G = wl.num_heads // wl.num_kv_heads
     q = W.queries(wl)[seq:seq + 1, kv * G:(kv + 1) * G].copy()
-    return dict(pool=pool, pages=pages, pt=pt, R=R, mu=mu, K=Kt[-1:], V=Vt[-1:], q=q, G=G)
+    return dict(pool=pool, pages=pages, pt=pt, R=R, mu=mu, K=Kt[-1:], V=Vt[-1:], q=q, G=G, ctx=ctx,
+                Kall=Kt, Vall=Vt, seq=seq, kv=kv)
 
 
 def oracle_step(wl, s):
     """Append the last token again and decode the G query heads of the sample."""
     import oracle
 
-    ctx = wl.ctx
+    ctx = s["ctx"]
     oracle.append_int2(s["pool"], s["pages"], 1, s["K"], s["V"], [0], [ctx - 1], s["pt"], s["R"],
                        s["mu"], wl.clip_k, wl.clip_v)
     oracle.decode_pairs("int2", s["pool"], s["pages"], s["G"], 1, s["q"], s["pt"], [ctx],
                         [[0, h] for h in range(s["G"])], R=s["R"])
 
 
-def cpu_oracle_rate(wl, min_seconds=10.0, max_steps=None, warmup=0, max_seconds=None):
+def cpu_oracle_rate(wl, min_seconds=10.0, max_steps=None, warmup=0, max_seconds=None, sample=None):
     """Cache GB/s of the oracle on (sequence 0, KV head 0): each step reads that
     head's whole context once for its G query heads.  Stops after max_steps
     steps, or after max_seconds if that comes first."""
-    s = oracle_sample_setup(wl)
+    s = sample if sample is not None else oracle_sample_setup(wl)
     for _ in range(warmup):
         oracle_step(wl, s)
     n, t0 = 0, time.perf_counter()
@@ -223,7 +258,7 @@ def cpu_oracle_rate(wl, min_seconds=10.0, max_steps=None, warmup=0, max_seconds=
             break
         if max_seconds is not None and el >= max_seconds:
             break
-    bytes_per_step = wl.ctx * W.cache_bytes_per_token_head("int2")
+    bytes_per_step = s["ctx"] * W.cache_bytes_per_token_head("int2")
     return bytes_per_step * n / el / 1e9, n, el
 
 
@@ -272,6 +307,49 @@ def cpu_oracle_rate_all_cores(wl, seconds=10.0):
     return bytes_per_step * steps / wall / 1e9, cores, steps, wall
 
 
+def parity_sample(pool_np, pt_np, s, wl):
+    """Codes, scales and zeros of the library's pool against the oracle's own
+    append of the cpu_baseline sample (one sequence, one KV head, the whole
+    context): differing codes are split into those whose pre-rounding value
+    lies within 1 ulp of a rounding boundary (allowed, counted) and others."""
+    import oracle
+
+    rec = 1152
+    Hkv = wl.num_kv_heads
+    gpu = pool_np.reshape(-1, Hkv, rec)
+    ref = s["pool"].reshape(-1, rec)
+    ctx, seq, kv = s["ctx"], s["seq"], s["kv"]
+    near = other = 0
+    for j in range((ctx + 15) // 16):
+        g, o = gpu[pt_np[seq, j], kv], ref[j]
+        if np.array_equal(g, o):
+            continue
+        for tau in range(min(16, ctx - 16 * j)):
+            p = 16 * j + tau
+            for which in (0, 1):
+                c1, s1, z1 = oracle.int2_load(g, which, tau)
+                c2, s2, z2 = oracle.int2_load(o, which, tau)
+                if (s1, z1) != (s2, z2):
+                    other += 1
+                bad = np.nonzero(np.asarray(c1) != np.asarray(c2))[0]
+                if len(bad) == 0:
+                    continue
+                x = (s["Kall"] if which == 0 else s["Vall"])[p, 0]
+                mu = s["mu"][0] if which == 0 else None
+                clip = wl.clip_k if which == 0 else wl.clip_v
+                t = oracle.quantize(x, s["R"][which, 0], clip, mu=mu)[4]
+                for i in bad:
+                    frac = abs(float(t[i]) - np.floor(float(t[i])) - 0.5)
+                    if frac <= np.spacing(np.float32(t[i])):
+                        near += 1
+                    else:
+                        other += 1
+    return {"boundary_code_mismatches": near, "other_mismatches": other,
+            "codes_compared": 2 * 128 * ctx, "token_heads": ctx,
+            "sample": f"sequence {seq} / KV head {kv}, all {ctx} positions, against the "
+                      f"oracle's append of the same tokens (the cpu_baseline sample)"}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -281,7 +359,8 @@ def run_reference(args):
     gbs, n, el = cpu_oracle_rate(wl, max_steps=max(1, args.steps), warmup=min(max(0, args.warmup), 3),
                                  max_seconds=240.0)
     sample = (f"float64 oracle, sequence 0 / KV head 0 of {wl.name}: per step re-quantise one "
-              f"token and decode {wl.num_heads // wl.num_kv_heads} query heads over {wl.ctx} "
+              f"token and decode {wl.num_heads // wl.num_kv_heads} query heads over "
+              f"{int(W.seq_lens(wl)[0])} "
               f"tokens ({n} steps, {el:.1f} s)")
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": args.gpus,
@@ -300,6 +379,97 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+
+def measure_workload(K, torch, wl, splits_list, steps, warmup, l2, peak, cpu_seconds=0.0):
+    """The decode step (kvq_append_decode: append each sequence's token at
+    position len-1, decode over len tokens) on one of the other workloads.
+    A cache smaller than twice L2 is replicated and the steps cycle through the
+    replicas (one pool, one page table per replica).  Returns one dict per split
+    count, with the oracle's rate on the workload's first (sequence, KV head)
+    when cpu_seconds > 0."""
+    B, H, Hkv = wl.batch, wl.num_heads, wl.num_kv_heads
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+    lens = W.seq_lens(wl)
+    pt_np, npool = W.page_table(wl)
+    cache_bytes = int(lens.sum()) * Hkv * W.cache_bytes_per_token_head("int2")
+    R = replicas_for(cache_bytes, l2)
+    h = K.kvq_create(K.make_layout(H, Hkv, wl.clip_k, wl.clip_v))
+    K.kvq_set_rotation(h, torch.from_numpy(W.rotations(wl)).cuda(),
+                       torch.from_numpy(W.key_mean(wl)).cuda())
+    rec = K.kvq_page_bytes(h)
+    pool = torch.zeros(R * npool * rec, dtype=torch.uint8, device="cuda")
+    pt0 = i32(pt_np)
+    t_build = time.perf_counter()
+    for g0 in range(0, B, 4):
+        seqs = list(range(g0, min(B, g0 + 4)))
+        n = [int(lens[b]) - 1 for b in seqs]
+        Ks = W.tokens_many(wl, 0, seqs, 0, 0, n)
+        Vs = W.tokens_many(wl, 0, seqs, 1, 0, n)
+        for b, k, v, m in zip(seqs, Ks, Vs, n):
+            if m > 0:
+                K.kvq_append(h, pool, R * npool, dev(k), dev(v), i32(np.full(m, b)),
+                             i32(np.arange(m)), pt0)
+    for r in range(1, R):
+        pool[r * npool * rec:(r + 1) * npool * rec].copy_(pool[:npool * rec])
+    pts = i32(np.stack([np.where(pt_np >= 0, pt_np + r * npool, -1) for r in range(R)]))
+    torch.cuda.synchronize()
+    t_build = time.perf_counter() - t_build
+    k_new = np.stack([W.token_at(wl, 0, b, 0, int(lens[b]) - 1) for b in range(B)])
+    v_new = np.stack([W.token_at(wl, 0, b, 1, int(lens[b]) - 1) for b in range(B)])
+    kd, vd, qd, seq_lens = dev(k_new), dev(v_new), dev(W.queries(wl)), i32(lens)
+    out = torch.empty((B, H, 128), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    res = []
+    for sp in splits_list:
+        splits = sp or K.kvq_auto_splits(h, B, pt_np.shape[1])
+        ws = torch.empty(K.kvq_workspace_bytes(h, B, splits), dtype=torch.uint8, device="cuda")
+
+        def run(n, first):
+            for i in range(first, first + n):
+                K.kvq_append_decode(h, pool, R * npool, kd, vd, qd, pts[i % R], seq_lens, out, ws,
+                                    splits)
+
+        run(warmup, 0)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run(steps, warmup)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        K.kvq_profile_enable(h, True)
+        run(steps, warmup + steps)
+        kms, kn = K.kvq_profile_read(h)
+        K.kvq_profile_enable(h, False)
+        kern_ms = kms / max(1, kn)
+        kgbs = cache_bytes / (kern_ms * 1e-3) / 1e9
+        res.append({"splits": splits, "us_per_step": ms * 1e3, "steps_per_s": 1e3 / ms,
+                    "cache_bytes_per_step": cache_bytes,
+                    "cache_gbs": cache_bytes / (ms * 1e-3) / 1e9,
+                    "kernel_us": kern_ms * 1e3, "kernel_gbs": kgbs, "kernel_frac_of_peak": kgbs / peak,
+                    "l2": l2_note(cache_bytes, R, l2), "replicas": R, "steps": steps})
+    assert K.kvq_get_status(h) == 0, f"device status bits set on {wl.name}"
+    cpu = None
+    if cpu_seconds > 0:
+        gbs_cpu, n_cpu, el_cpu = cpu_oracle_rate(wl, min_seconds=cpu_seconds)
+        cpu = {"value": gbs_cpu, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"float64 oracle on sequence 0 / KV head 0 ({int(lens[0])} tokens), "
+                         f"{n_cpu} steps in {el_cpu:.1f} s"}
+    out_d = {"workload": wl.name, "batch": B, "heads": H, "kv_heads": Hkv,
+             "ctx": int(lens.max()) if wl.ragged else int(wl.ctx),
+             "cache_build_s": round(t_build, 1), "cpu_baseline": cpu}
+    if wl.ragged:
+        out_d["ctx_min"] = int(lens.min())
+        out_d["tokens"] = int(lens.sum())
+    if len(res) == 1:
+        out_d.update(res[0])
+    else:
+        out_d["by_splits"] = res
+    del pool
+    return out_d
+
+
 
 def run_ours(args):
     import torch
@@ -567,9 +737,31 @@ def run_ours(args):
                   "separate_calls": "kvq_append + kvq_bf16_append + kvq_decode_window"}
         assert K.kvq_get_status(h) == 0, "device status bits set during the window benchmark"
 
+    # the other workloads of the same path (sub-objects of this line)
+    l2 = l2_bytes(torch)
+    configs = None
+    if not args.no_configs and world == 1 and not args.batch:
+        cs, cw = max(50, min(args.steps, 200)), min(max(3, args.warmup), 20)
+        cpu_s = 0.0 if args.no_cpu else 3.0
+        configs = {
+            "tiny_1k": measure_workload(K, torch, W.WORKLOADS["tiny_1k"], [0], cs, cw, l2, peak,
+                                        cpu_s),
+            "long_128k": measure_workload(K, torch, W.WORKLOADS["long_128k"], [64, 128, 256], cs,
+                                          cw, l2, peak, cpu_s),
+            "ragged_64": measure_workload(K, torch, W.WORKLOADS["ragged_64"], [0], cs, cw, l2,
+                                          peak, cpu_s),
+        }
+        fs, _ = measure_full_stack(K, torch, max(20, min(args.steps, 100)), min(max(3, args.warmup), 10),
+                                   local, None, clocks_on=False)
+        configs["full_stack_36l"] = fs
+        torch.cuda.empty_cache()
+
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        gbs_cpu, n_cpu, el_cpu = cpu_oracle_rate(wl, min_seconds=10.0)
+        sample = oracle_sample_setup(wl)
+        parity = parity_sample(pool.cpu().numpy(), pt_np, sample, wl)
+        gbs_cpu, n_cpu, el_cpu = cpu_oracle_rate(wl, min_seconds=10.0, sample=sample)
         cpu = {"value": gbs_cpu, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"float64 oracle on sequence 0 / KV head 0: re-quantise one token and "
                          f"decode {H // Hkv} query heads over {ctx} tokens per step, "
@@ -589,8 +781,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": wl.name, "batch": B, "ctx": ctx, "heads": H, "kv_heads": Hkv,
                    "head_dim": 128, "page": 16, "splits": splits,
-                   "l2": f"inputs larger than L2: {cache_bytes / 1e6:.0f} MB INT2 cache read per "
-                         f"step, no flush",
+                   "l2": l2_note(cache_bytes, 1, l2),
                    "cache_build_s": round(t_build, 1)},
         "steps_per_s": world * args.steps / (ms * 1e-3),
         "pct_of_hbm_peak": 100.0 * gbs_rank / peak,
@@ -610,6 +801,8 @@ def run_ours(args):
         "two_call_step": two_calls,
         "clocks": clk,
         "gpu_launches": launches,
+        "parity": parity,
+        "configs": configs,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -625,22 +818,13 @@ def run_ours(args):
 FULL_STACK_METRIC = "decode steps/s of a 36-layer stack (append + INT2 decode per layer)"
 
 
-def run_full_stack(args):
-    import torch
-
-    from rotated_int2_kv_kvq_gb300 import kvq as K
+def measure_full_stack(K, torch, steps, warmup, local=0, dist=None, clocks_on=True):
+    """Build the 36 layers' caches (8192-token prefill per sequence), capture
+    one decode step (every layer appends one token per sequence and decodes)
+    as a CUDA graph and time `steps` replays; also the same step run eagerly
+    and as an unfused graph (append and decode as separate calls)."""
     from rotated_int2_kv_kvq_gb300.pipeline import DecodeStepGraph, LayerCache
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    K.load_library()
     wl = W.WORKLOADS["full_stack_36l"]
     B, H, Hkv, L, P, S = (wl.batch, wl.num_heads, wl.num_kv_heads, wl.layers, wl.prefill,
                           wl.decode_steps)
@@ -679,7 +863,7 @@ def run_full_stack(args):
 
     stream = torch.cuda.current_stream()
 
-    def timed(g, steps, warmup, graph=True):
+    def timed(g, n, warm, graph=True):
         """Step i uses the inputs of decode step i mod S (positions P + i mod S)."""
         def one(i):
             s = i % S
@@ -689,67 +873,96 @@ def run_full_stack(args):
             else:
                 g.run()
 
-        for i in range(warmup):
+        for i in range(warm):
             one(i)
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(steps):
-            one(warmup + i)
+        for i in range(n):
+            one(warm + i)
         e1.record(stream)
         torch.cuda.synchronize()
         return max_over_ranks(e0.elapsed_time(e1), dist)
 
-    steps = min(args.steps, 1000)
     fused_g = make(True)
     fused_g.capture()
-    clocks = Clocks(local)
-    clocks.start()
-    ms = timed(fused_g, steps, args.warmup)
-    extra, t_extra = 0, time.time()
-    while clocks.proc is not None and clocks.samples() < 3 and time.time() - t_extra < 10.0:
-        for _ in range(20):
-            fused_g.replay()
-        torch.cuda.synchronize()
-        extra += 20
-    clk = clocks.stop()
-    if clk is not None:
-        clk["window"] = "warm-up + timed steps" + (f" + {extra} untimed steps" if extra else "")
+    clocks = Clocks(local) if clocks_on else None
+    if clocks:
+        clocks.start()
+    ms = timed(fused_g, steps, warmup)
+    clk = None
+    if clocks:
+        extra, t_extra = 0, time.time()
+        while clocks.proc is not None and clocks.samples() < 3 and time.time() - t_extra < 10.0:
+            for _ in range(20):
+                fused_g.replay()
+            torch.cuda.synchronize()
+            extra += 20
+        clk = clocks.stop()
+        if clk is not None:
+            clk["window"] = "warm-up + timed steps" + (f" + {extra} untimed steps" if extra else "")
     n_eager = max(3, steps // 4)
     eager_ms = timed(fused_g, n_eager, 3, graph=False) / n_eager
     unfused_g = make(False)
     unfused_g.capture()
-    unfused_ms = timed(unfused_g, steps, args.warmup) / steps
+    unfused_ms = timed(unfused_g, steps, warmup) / steps
     status = [K.kvq_get_status(c.h) for c in layers]
     assert not any(status), f"device status bits set: {status}"
-
     ms_step = ms / steps
     # algorithmic INT2 cache bytes per step at the mean context of the S steps
     mean_ctx = P + (S + 1) / 2.0
     cache_bytes = L * B * Hkv * mean_ctx * W.cache_bytes_per_token_head("int2")
     peak, peak_kind = measured_peaks()
-    line = {
-        "metric": FULL_STACK_METRIC, "value": world * steps / (ms * 1e-3), "unit": "steps/s",
-        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int2 codes, fp16 mma, fp32 accumulate", "data": "synthetic",
-        "config": {"workload": wl.name, "layers": L, "batch": B, "heads": H, "kv_heads": Hkv,
-                   "prefill": P, "ctx": f"{P + 1}..{P + S}", "splits": fused_g.splits,
-                   "l2": f"inputs larger than L2: {cache_bytes / 1e9:.2f} GB of INT2 cache "
-                         f"per step over {L} pools, no flush",
-                   "cache_build_s": round(t_build, 1)},
-        "per_layer_us": ms_step * 1e3 / L,
+    l2 = l2_bytes(torch)
+    res = {
+        "workload": wl.name, "layers": L, "batch": B, "heads": H, "kv_heads": Hkv, "prefill": P,
+        "ctx": f"{P + 1}..{P + S}", "splits": fused_g.splits, "steps": steps,
+        "steps_per_s": 1e3 / ms_step, "ms_per_step": ms_step, "per_layer_us": ms_step * 1e3 / L,
+        "cache_bytes_per_step": cache_bytes,
         "cache_gbs": cache_bytes / (ms_step * 1e-3) / 1e9,
         "pct_of_hbm_peak": 100.0 * cache_bytes / (ms_step * 1e-3) / 1e9 / peak,
-        "peak_kind": peak_kind,
-        "launches_per_step": 3 * L,
-        "graph": True,
-        "eager_ms_per_step": eager_ms,
-        "unfused_graph_ms_per_step": unfused_ms,
+        "peak_kind": peak_kind, "launches_per_step": 3 * L, "graph": True,
+        "eager_ms_per_step": eager_ms, "unfused_graph_ms_per_step": unfused_ms,
+        "l2": l2_note(cache_bytes, 1, l2) + f" (over {L} pools)",
+        "cache_build_s": round(t_build, 1),
+    }
+    del layers, K_tab, V_tab, q_tab
+    return res, clk
+
+
+def run_full_stack(args):
+    import torch
+
+    from rotated_int2_kv_kvq_gb300 import kvq as K
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    K.load_library()
+    steps = min(args.steps, 1000)
+    r, clk = measure_full_stack(K, torch, steps, args.warmup, local, dist)
+    line = {
+        "metric": FULL_STACK_METRIC, "value": world * r["steps_per_s"], "unit": "steps/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int2 codes, fp16 mma, fp32 accumulate", "data": "synthetic",
+        "config": {k: r[k] for k in ("workload", "layers", "batch", "heads", "kv_heads",
+                                     "prefill", "ctx", "splits", "l2", "cache_build_s")},
+        "per_layer_us": r["per_layer_us"], "cache_gbs": r["cache_gbs"],
+        "pct_of_hbm_peak": r["pct_of_hbm_peak"], "peak_kind": r["peak_kind"],
+        "launches_per_step": r["launches_per_step"], "graph": True,
+        "eager_ms_per_step": r["eager_ms_per_step"],
+        "unfused_graph_ms_per_step": r["unfused_graph_ms_per_step"],
         "clocks": clk,
-        "gpu_launches": 3 * L * steps,
+        "gpu_launches": r["launches_per_step"] * steps,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -51,6 +51,9 @@
  *     never trap.  NaN / Inf inputs are not checked and propagate.
  *   - A handle is not thread-safe; calls on one handle must not overlap on the
  *     host.  Kernels of different handles may run concurrently.
+ *   - A handle belongs to the device that was current when kvq_create ran.
+ *     Calls that take a handle make that device current for their own work and
+ *     give the caller's current device back before they return.
  *
  * Supported shapes: head_dim == 128, group == 128, page_size == 16,
  * num_heads / num_kv_heads in {1, 2, 4}, 1 <= num_kv_heads <= 64.  Other values
@@ -78,7 +81,7 @@ extern "C" {
 #define KVQ_STATUS_BAD_POS     2u  /* position < 0 or >= max_pages*page_size      */
 #define KVQ_STATUS_BAD_SEQLEN  4u  /* seq_len < 0 or > max_pages*page_size        */
 #define KVQ_STATUS_BAD_SEQ     8u  /* seq_idx < 0 or >= batch                     */
-#define KVQ_STATUS_TIMEOUT    16u  /* a bounded wait on a page copy gave up       */
+#define KVQ_STATUS_TIMEOUT    16u  /* a bounded wait on a page copy gave up (2 s)  */
 
 /* ---- layout flags -------------------------------------------------------- */
 /* Decode returns the output in the rotated value basis (o_rot) instead of
@@ -368,8 +371,8 @@ int kvq_decode_static(kvq_handle* h, const void* pool, int num_pool_pages,
  *   keys:   L_K = [ sum_h KL(p_h || p~_h) + lambda_K |sum_h (dp_h V) W_h^T|^2 ] / Nq
  *   values: L_V = [ |sum_h (p~_h dV) W_h^T|^2 ] / Nq,   p~ fixed at the calibrated keys,
  * summed over the last Nq query positions of a causal calibration chunk
- * (the referee report's Eqs. (14), (16); "Gradients computed on the final 64
- * query positions").  p is the attention with the exact keys, p~ with the keys
+ * (the referee report's Eqs. (14), (16); the OptR page's "Assumptions & free
+ * parameters" puts the gradient on the final 64 query positions).  p is the attention with the exact keys, p~ with the keys
  * centred by mu, rotated, quantised by this library's INT2 quantiser (fp16
  * scale and zero), dequantised and rotated back; dV likewise for values.  The
  * straight-through backward replaces the rounding by the identity and
@@ -419,6 +422,15 @@ int kvq_optr_loss_grad(int num_kv_heads, int T, int Nq, int G, int Dm,
 /* Read and clear the handle's device status word (KVQ_STATUS_* bits).
  * Synchronises `stream`. */
 int kvq_get_status(kvq_handle* h, uint32_t* bits, void* stream);
+
+/* Self-test of the bounded waits: launches one CTA on `stream` whose thread
+ * waits on a shared-memory mbarrier that nothing completes, bounded by
+ * limit_us microseconds (1 ... 1,000,000) of the GPU's global timer, the same
+ * wait every page copy uses (there bounded by two seconds).  The wait gives up
+ * and sets KVQ_STATUS_TIMEOUT in the handle's status word; no copy is in
+ * flight, so the context stays usable.  Asynchronous; read the bit with
+ * kvq_get_status.  Lets a test check the give-up path without a fault. */
+int kvq_selftest_wait_timeout(kvq_handle* h, int limit_us, void* stream);
 
 /* The number of splits kvq_decode uses when num_splits == 0. */
 int kvq_auto_splits(const kvq_handle* h, int batch, int max_pages);

@@ -318,12 +318,14 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendArgs a) {
 template <int TPW>
 cudaError_t launch_tpw(const AppendArgs& a, int num_sms, cudaStream_t st) {
   using S = AppendSmem<TPW>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[64] = {};       // per device: the attribute is per context
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(append_int2_kernel<TPW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int tiles = (a.n + S::kTile - 1) / S::kTile;
   // Enough CTAs to fill the GPU about twice; each CTA loops over tiles so the

@@ -476,18 +476,20 @@ __device__ __forceinline__ void half2_residuals(uint32_t X, float P0, float P1, 
 }
 
 // B fragments of the value product from this lane's weights of tokens g and
-// g+8 (head t): column 2*head holds the fp16 weight, column 2*head+1 the fp16
-// residual P - fp16(P) (at most 2^-11 P; for weights below 2^-3 it is an fp16
-// subnormal, a negligible loss next to the weight itself).  The lane's pairs
-// {weight, residual} of token g (and of token g+8) are row g, columns 2t and
-// 2t+1 of an 8 x 8 matrix of 16-bit values (rows = tokens, columns = 2*head +
-// part) in mma fragment order; its transpose (movmatrix) gives lane (g, t)
-// tokens 2t and 2t+1 of column g, which is the B fragment.
+// g+8 (head t): column 2*head holds the fp16 weight X = fp16(P), column
+// 2*head+1 the fp16 residual (P - X) * 2^11 (P - X is exact in fp32; the 2^11
+// keeps the residual a normal fp16 number down to P = 2^-14, so weights far
+// below the running max keep about 22 bits; the epilogue scales that column
+// back).  The lane's pairs {weight, residual} of token g (and of token g+8)
+// are row g, columns 2t and 2t+1 of an 8 x 8 matrix of 16-bit values (rows =
+// tokens, columns = 2*head + part) in mma fragment order; its transpose
+// (movmatrix) gives lane (g, t) tokens 2t and 2t+1 of column g, which is the B
+// fragment.
 __device__ __forceinline__ void weights_to_b(float P0, float P1, uint32_t& pb0, uint32_t& pb1) {
   const uint32_t X = pack_half2(P0, P1);
   float r0, r1;
   half2_residuals(X, P0, P1, r0, r1);
-  const uint32_t Y = pack_half2(r0, r1);
+  const uint32_t Y = pack_half2(r0 * 2048.0f, r1 * 2048.0f);
   pb0 = movmatrix_trans(__byte_perm(X, Y, 0x5410));
   pb1 = movmatrix_trans(__byte_perm(X, Y, 0x7632));
 }
@@ -501,6 +503,7 @@ constexpr float kLazy = 8.0f;
 struct WarpState {
   float acc[8][4];
   float m_run, l_run, z_run;
+  float F;                   // rescale factor owed by the flushed total (see flush_acc)
 };
 
 template <bool kMasked>
@@ -571,6 +574,7 @@ __device__ __forceinline__ void process_pair(WarpState& st, const uint32_t (&qf)
           for (int q = 0; q < 4; ++q) acc[mb][q] *= f;
         l_run *= f;
         z_run *= f;
+        st.F *= f;
         m_run = pms;
       }
       pa0 = va0 ? fast_exp2(la0 - m_run) : 0.0f;
@@ -600,6 +604,24 @@ constexpr int kW = kInt2Warps;                 // warps per CTA
 constexpr int kPPS = 4;                        // pages per stage (two pairs)
 constexpr int kNS = 2;                         // pipeline stages per warp
 constexpr int kMaxIds = 1024;                  // page ids staged per sub-chunk
+constexpr int kFlushStages = 16;               // stages between accumulator flushes
+
+// The tensor cores' fp32 accumulation of P.V is not round-to-nearest: over many
+// pages the running accumulator drifts (about 2e-4 relative after 1,300 pages
+// of one split).  Every kFlushStages stages each lane adds its accumulator
+// into its own fp32 total in shared memory (round-to-nearest fma) and restarts
+// it from zero; F carries the running-max rescales made since the last flush.
+__device__ __forceinline__ void flush_acc(WarpState& ws, float* tot) {
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float* p = tot + 32 * (4 * mb + q);
+      *p = fmaf(*p, ws.F, ws.acc[mb][q]);
+      ws.acc[mb][q] = 0.0f;
+    }
+  ws.F = 1.0f;
+}
 
 // Every warp streams its own KV head's records through its own ring: no stage
 // is shared between warps, so no warp waits for another to release a slot.
@@ -615,6 +637,7 @@ struct Int2Smem {
   };
   uint64_t full[kW][kNS];
   int ids[kMaxIds];
+  float tot[kW][32][32];     // per warp and lane: flushed P.V totals, [acc index][lane]
 };
 
 // Fill stage k of warp `warp` (pages kPPS*k .. kPPS*k + kPPS - 1 of the warp's
@@ -707,6 +730,11 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   ws.l_run = 0.0f;
   ws.z_run = 0.0f;
 
+  ws.F = 1.0f;
+  float* const tot = &sm.tot[warp][0][lane];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) tot[32 * j] = 0.0f;
+
   int gs = 0;            // this warp's stages consumed so far (ring phase)
   bool timed_out = false;
   for (int sub = 0; sub < npg && !timed_out; sub += kMaxIds) {
@@ -776,6 +804,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
                              vb0, vb1);
         }
       }
+      if (((gs + k) % kFlushStages) == kFlushStages - 1) flush_acc(ws, tot);
     }
     gs += nst;
     // sm.ids is reloaded for the next sub-chunk; every warp leaves together
@@ -787,6 +816,11 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     for (int s = 0; s < kNS; ++s) mbar_wait_bounded(smem_u32(&sm.full[warp][s]), 0);
   }
   griddep_launch_dependents();
+  // the flushed totals back into the accumulator
+#pragma unroll
+  for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) ws.acc[mb][q] = fmaf(tot[32 * (4 * mb + q)], ws.F, ws.acc[mb][q]);
 
   // ---- warp epilogue: (m, l, o) of the warp's KV head for its G query heads
 #pragma unroll
@@ -796,7 +830,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   }
   // undo the code scale (2^-17 for even m-blocks, 2^-15 for odd ones) and the
   // weight scale 2^(14 - kLazy) = 2^6 (also on l_run, z_run and m_run); the
-  // residual column adds in unscaled
+  // residual column carries 2^11 more
   constexpr float kInvEven = 2048.0f;   // 2^(17 - 6)
   constexpr float kInvOdd = 512.0f;     // 2^(15 - 6)
   if (GPH == 1) {
@@ -813,8 +847,8 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
 #pragma unroll
       for (int mb = 0; mb < 8; ++mb) {
         const float inv = (mb & 1) ? kInvOdd : kInvEven;
-        const float o0 = fmaf(ws.acc[mb][1] + ws.acc[mb][0], inv, zr);
-        const float o1 = fmaf(ws.acc[mb][3] + ws.acc[mb][2], inv, zr);
+        const float o0 = fmaf(fmaf(ws.acc[mb][1], 0x1p-11f, ws.acc[mb][0]), inv, zr);
+        const float o1 = fmaf(fmaf(ws.acc[mb][3], 0x1p-11f, ws.acc[mb][2]), inv, zr);
         p[4 + 16 * mb + g] = any ? o0 + 0.0f : 0.0f;
         p[4 + 16 * mb + g + 8] = any ? o1 + 0.0f : 0.0f;
       }
@@ -829,8 +863,10 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
       const float inv = (mb & 1) ? kInvOdd : kInvEven;
-      sm.mg.o[warp][t][16 * mb + g] = fmaf(ws.acc[mb][1] + ws.acc[mb][0], inv, ws.z_run * 0x1p-6f);
-      sm.mg.o[warp][t][16 * mb + g + 8] = fmaf(ws.acc[mb][3] + ws.acc[mb][2], inv, ws.z_run * 0x1p-6f);
+      sm.mg.o[warp][t][16 * mb + g] =
+          fmaf(fmaf(ws.acc[mb][1], 0x1p-11f, ws.acc[mb][0]), inv, ws.z_run * 0x1p-6f);
+      sm.mg.o[warp][t][16 * mb + g + 8] =
+          fmaf(fmaf(ws.acc[mb][3], 0x1p-11f, ws.acc[mb][2]), inv, ws.z_run * 0x1p-6f);
     }
     if (g == 0) {
       sm.mg.m[warp][t] = ws.m_run + 6.0f;
@@ -1404,6 +1440,11 @@ cudaError_t set_smem_attr(Kern kern) {
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sizeof(Smem)));
+  // as much of the L1/shared split as possible for shared memory (two INT2
+  // decode CTAs take 221 KB)
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }

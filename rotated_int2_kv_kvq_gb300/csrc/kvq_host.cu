@@ -169,7 +169,8 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
   const kvq::DecodeWs w =
       kvq::decode_ws_layout(batch, h->L.num_kv_heads, h->L.num_heads, splits, int2);
   if (ws_bytes < w.total) return KVQ_ENOSPACE;
-  if (cudaSetDevice(h->device) != cudaSuccess) return KVQ_ECUDA;
+  kvq::DeviceGuard dev_guard(h->device);
+  if (!dev_guard.ok()) return KVQ_ECUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   kvq::DecodeArgs a;
   a.pool = static_cast<const uint8_t*>(pool);
@@ -237,7 +238,8 @@ int append_common(kvq_handle* h, bool int2, void* pool, int num_pool_pages, cons
       reinterpret_cast<uintptr_t>(pool) % 16)
     return KVQ_EINVAL;
   if (int2 && !h->ready) return KVQ_ENOTREADY;
-  if (cudaSetDevice(h->device) != cudaSuccess) return KVQ_ECUDA;
+  kvq::DeviceGuard dev_guard(h->device);
+  if (!dev_guard.ok()) return KVQ_ECUDA;
   kvq::AppendArgs a;
   a.pool = static_cast<uint8_t*>(pool);
   a.num_pool_pages = num_pool_pages;
@@ -263,6 +265,28 @@ int append_common(kvq_handle* h, bool int2, void* pool, int num_pool_pages, cons
 }  // namespace
 
 int kvq::handle_device(const kvq_handle* h) { return h ? h->device : -1; }
+
+namespace {
+
+// One thread waits on an mbarrier that nothing arrives on and no copy
+// completes, with a bound of `limit_ns`: the wait runs out and the status word
+// gets KVQ_STATUS_TIMEOUT, exactly as a decode or append wait that gives up.
+// Nothing is in flight when the CTA leaves.
+__global__ void wait_selftest_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  kvq::mbar_init(kvq::smem_u32(&bar), 1);
+  kvq::fence_mbar_init();
+  if (!kvq::mbar_wait_bounded(kvq::smem_u32(&bar), 0, limit_ns))
+    atomicOr(status, KVQ_STATUS_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t kvq::launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 extern "C" {
 
@@ -291,7 +315,7 @@ int kvq_create(const kvq_layout* layout, kvq_handle** out) {
 
 int kvq_destroy(kvq_handle* h) {
   if (!h) return KVQ_OK;
-  cudaSetDevice(h->device);
+  kvq::DeviceGuard dev_guard(h->device);
   cudaDeviceSynchronize();
   for (int k = 0; k < kvq_handle::kSlots; ++k) {
     if (h->ev[k][0]) cudaEventDestroy(h->ev[k][0]);
@@ -313,7 +337,8 @@ size_t kvq_bf16_page_bytes(const kvq_handle* h) {
 
 int kvq_set_rotation(kvq_handle* h, const float* R, const float* mu, void* stream) {
   if (!h || !R || !mu) return KVQ_EINVAL;
-  if (cudaSetDevice(h->device) != cudaSuccess) return KVQ_ECUDA;
+  kvq::DeviceGuard dev_guard(h->device);
+  if (!dev_guard.ok()) return KVQ_ECUDA;
   const int Hkv = h->L.num_kv_heads;
   if (!h->bank && cudaMalloc(&h->bank, rot_floats(Hkv) * sizeof(float)) != cudaSuccess) {
     h->bank = nullptr;
@@ -444,7 +469,8 @@ int kvq_dequant(kvq_handle* h, const void* pool, int num_pool_pages, const int32
   if (!h || !pool || !page_table || len < 0 || seq < 0 || start < 0) return KVQ_EINVAL;
   if (num_pool_pages < 1 || max_pages < 1) return KVQ_EINVAL;
   if (len == 0 || (!K_out && !V_out)) return KVQ_OK;
-  if (cudaSetDevice(h->device) != cudaSuccess) return KVQ_ECUDA;
+  kvq::DeviceGuard dev_guard(h->device);
+  if (!dev_guard.ok()) return KVQ_ECUDA;
   return cuda_rc(kvq::launch_dequant(static_cast<const uint8_t*>(pool), num_pool_pages,
                                      page_table, max_pages, h->L.num_kv_heads, seq, start, len,
                                      K_out, V_out, h->status, S(stream)));
@@ -452,7 +478,8 @@ int kvq_dequant(kvq_handle* h, const void* pool, int num_pool_pages, const int32
 
 int kvq_get_status(kvq_handle* h, uint32_t* bits, void* stream) {
   if (!h || !bits) return KVQ_EINVAL;
-  if (cudaSetDevice(h->device) != cudaSuccess) return KVQ_ECUDA;
+  kvq::DeviceGuard dev_guard(h->device);
+  if (!dev_guard.ok()) return KVQ_ECUDA;
   cudaStream_t st = S(stream);
   uint32_t v = 0;
   if (cudaMemcpyAsync(&v, h->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -461,6 +488,14 @@ int kvq_get_status(kvq_handle* h, uint32_t* bits, void* stream) {
     return KVQ_ECUDA;
   *bits = v;
   return KVQ_OK;
+}
+
+int kvq_selftest_wait_timeout(kvq_handle* h, int limit_us, void* stream) {
+  if (!h || limit_us < 1 || limit_us > 1000000) return KVQ_EINVAL;
+  kvq::DeviceGuard dev_guard(h->device);
+  if (!dev_guard.ok()) return KVQ_ECUDA;
+  return cuda_rc(kvq::launch_wait_selftest(h->status, 1000ull * static_cast<uint64_t>(limit_us),
+                                           S(stream)));
 }
 
 int kvq_profile_enable(kvq_handle* h, int enable) {

@@ -117,7 +117,32 @@ int optr_loss_grad(int H, int T, int Nq, int G, int Dm, const uint16_t* K, const
                    cudaStream_t st);
 int decode_int2_ctas_per_sm();
 int decode_bf16_ctas_per_sm();
+// Makes `dev` the calling thread's current device while the guard lives and
+// gives the caller's device back afterwards, so that no entry point changes
+// the caller's current device.
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    ok_ = cudaGetDevice(&prev_) == cudaSuccess;
+    if (ok_ && prev_ != dev) {
+      ok_ = cudaSetDevice(dev) == cudaSuccess;
+      changed_ = ok_;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed_) cudaSetDevice(prev_);
+  }
+  DeviceGuard(const DeviceGuard&) = delete;
+  DeviceGuard& operator=(const DeviceGuard&) = delete;
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = 0;
+  bool ok_ = false, changed_ = false;
+};
+
 int handle_device(const kvq_handle* h);   // CUDA device the handle was created on
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t st);
 
 // ---- device helpers -------------------------------------------------------
 #if defined(__CUDACC__)
@@ -173,12 +198,30 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up after about two seconds
-// (20000 attempts of at most 100 us each).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Default bound of every wait on a page copy: two seconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Wait for phase `parity` of an mbarrier, giving up once `limit_ns` of global
+// time have passed (returns false; the caller records KVQ_STATUS_TIMEOUT).
+// Each attempt lets the thread sleep up to 0.1 ms until the phase completes.
+// The attempt count is capped too (2^29 attempts, far beyond any limit used
+// here), so the wait ends even if the timer did not advance.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  for (uint32_t it = 0; it < 20000u; ++it)
-    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 26); ++it) {
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
   return false;
 }
 

@@ -10,6 +10,8 @@
 // library is loaded.  It allocates nothing itself.
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kvq_internal.cuh"
 
 namespace {
@@ -20,17 +22,19 @@ constexpr size_t kStaticWsBytes = static_cast<size_t>(16) << 20;   // 16 MiB
 static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_ws_addr[kMaxDevices] = {};
+std::atomic<void*> g_ws_addr[kMaxDevices] = {};
 
-// Device address of g_static_ws on `dev` (current device), looked up once.
+// Device address of g_static_ws on `dev` (current device), looked up once per
+// device.  Threads that race on the first call all look up the same address
+// and store the same value, so a relaxed load and store suffice.
 int static_ws_address(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) return KVQ_ECUDA;
-  if (!g_ws_addr[dev]) {
-    void* p = nullptr;
+  void* p = g_ws_addr[dev].load(std::memory_order_relaxed);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return KVQ_ECUDA;
-    g_ws_addr[dev] = p;
+    g_ws_addr[dev].store(p, std::memory_order_relaxed);
   }
-  *out = g_ws_addr[dev];
+  *out = p;
   return KVQ_OK;
 }
 
@@ -53,7 +57,8 @@ extern "C" int kvq_decode_static(kvq_handle* h, const void* pool, int num_pool_p
   if (need > kStaticWsBytes) return KVQ_ENOSPACE;   // batch x splits too large for 16 MiB
   // the symbol's address is per device: look it up with the handle's device current
   const int dev = kvq::handle_device(h);
-  if (cudaSetDevice(dev) != cudaSuccess) return KVQ_ECUDA;
+  kvq::DeviceGuard dev_guard(dev);
+  if (!dev_guard.ok()) return KVQ_ECUDA;
   void* ws = nullptr;
   const int rc = static_ws_address(dev, &ws);
   if (rc != KVQ_OK) return rc;

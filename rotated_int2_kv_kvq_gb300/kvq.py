@@ -53,6 +53,7 @@ SIGNATURES = {
     "kvq_append_decode_window": ([_P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _P,
                                   _P, _SZ, _I, _P], _I),
     "kvq_get_status": ([_P, _P, _P], _I),
+    "kvq_selftest_wait_timeout": ([_P, _I, _P], _I),
     "kvq_auto_splits": ([_P, _I, _I], _I),
     "kvq_profile_enable": ([_P, _I], _I),
     "kvq_profile_read": ([_P, _P, _P], _I),
@@ -308,6 +309,11 @@ def kvq_get_status(h: Handle, stream=None) -> int:
     _check("kvq_get_status", load_library().kvq_get_status(h.ptr, ctypes.byref(bits),
                                                            _stream(stream)))
     return int(bits.value)
+
+
+def kvq_selftest_wait_timeout(h: Handle, limit_us: int, stream=None) -> None:
+    _check("kvq_selftest_wait_timeout",
+           load_library().kvq_selftest_wait_timeout(h.ptr, int(limit_us), _stream(stream)))
 
 
 def kvq_profile_enable(h: Handle, enable: bool = True) -> None:

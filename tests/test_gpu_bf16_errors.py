@@ -46,6 +46,24 @@ def test_bf16_qwen_shape():
     assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want, "bf16 qwen")
 
 
+def test_bf16_qwen_full_context():
+    """The BF16 comparison kernel at the full 32K context of two sequences."""
+    wl = W.WORKLOADS["qwen3_8b_32k"]
+    B = 2
+    pt, _ = W.page_table(wl)
+    pt = pt[:B].copy()
+    c = Cache(wl, kind="bf16", page_table=pt, num_pool_pages=int(pt.max()) + 1)
+    for s0 in range(0, wl.ctx, 8192):
+        c.append_range(range(B), s0, 8192)
+    q = W.queries(wl, 0, 3, batch=B)
+    lens = [wl.ctx, wl.ctx - 5]
+    got = c.decode(q, lens, 0)
+    pairs = [[b, h] for b in range(B) for h in (0, 13, 31)]
+    want = c.oracle_decode(c.pool_host(), q, lens, pairs)
+    assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want, "bf16 32k")
+    assert c.status() == 0
+
+
 def test_host_argument_errors():
     wl = W.WORKLOADS["tiny_1k"]
     lay = K.make_layout(4, 1)
@@ -122,3 +140,28 @@ def test_device_data_errors_are_reported_and_skipped():
     # the context is still usable
     got = c.decode(q, [33], 2)
     assert c.status() == 0
+
+
+def test_bounded_wait_gives_up_and_leaves_the_gpu_usable():
+    """A wait that nothing completes runs out after its limit, sets
+    KVQ_STATUS_TIMEOUT and returns; the next decode on the same stream is
+    correct and reports no error."""
+    import time
+    wl = W.WORKLOADS["tiny_1k"]
+    c = Cache(wl)
+    c.append_range([0], 0, 200)
+    assert c.status() == 0
+    t0 = time.perf_counter()
+    K.kvq_selftest_wait_timeout(c.h, 2000)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 1.0
+    assert c.status() == K.KVQ_STATUS_TIMEOUT
+    assert c.status() == 0                        # reading clears the word
+    q = W.queries(wl, 0, 77)
+    got = c.decode(q, [200], 2)
+    want = c.oracle_decode(c.pool_host(), q, [200], [[0, h] for h in range(4)])
+    assert_close_attention(got[0], want, "after a timed-out wait")
+    assert c.status() == 0
+    with pytest.raises(K.KvqError) as e:
+        K.kvq_selftest_wait_timeout(c.h, 0)
+    assert e.value.code == K.KVQ_EINVAL

@@ -14,8 +14,8 @@ import pytest
 import torch
 
 import oracle
-from kvq_testlib import (Cache, assert_close_attention, compare_codes, i32, oracle_window, u16,
-                         window_decode, window_page_table, window_positions)
+from kvq_testlib import (Cache, assert_boundary_count, assert_close_attention, compare_codes, i32,
+                         oracle_window, u16, window_decode, window_page_table, window_positions)
 from rotated_int2_kv_kvq_gb300 import kvq as K
 from rotated_int2_kv_kvq_gb300 import workloads as W
 
@@ -54,7 +54,7 @@ def test_tiny_append_bitexact(tiny):
         # only boundary cases may differ: check token by token
         Ktok, Vtok = (lambda s, p: Kt[p]), (lambda s, p: Vt[p])
         near = compare_codes(c, pool, [(0, p, 0) for p in range(n)], Ktok, Vtok)
-        print("boundary-case code differences:", near)
+        assert_boundary_count(near, n, "tiny")
     assert c.status() == 0
 
 
@@ -150,6 +150,55 @@ def test_gqa_group_sizes(G):
     assert_close_attention(got[0], want, f"G={G}")
 
 
+@pytest.mark.parametrize("Hkv", [2, 4, 6])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_kv_head_counts_sharing_a_cta(Hkv, splits):
+    """Hkv = 2, 4, 6 (G = 4): the decode CTA serves 2, 4 or 2 KV heads, so 4, 2
+    or 4 warps share each head and their partials merge through shared memory."""
+    wl = W.WORKLOADS["qwen3_8b_32k"]
+    B, L = 2, 3001
+    pt, _ = W.page_table(wl)
+    pt = pt[:B].copy()
+    c = Cache(wl, page_table=pt, num_pool_pages=int(pt.max()) + 1, num_heads=4 * Hkv,
+              num_kv_heads=Hkv)
+    c.append_range(range(B), 0, L)
+    q = W.queries(wl, 0, 40 + Hkv, batch=B)[:, :4 * Hkv].copy()
+    lens = [L, L - 1000]
+    got = c.decode(q, lens, splits)
+    pairs = [[b, h] for b in range(B) for h in range(4 * Hkv)]
+    want = c.oracle_decode(c.pool_host(), q, lens, pairs)
+    assert_close_attention(got.reshape(-1, 128), want, f"Hkv={Hkv} splits={splits}")
+    assert c.status() == 0
+
+
+@pytest.mark.parametrize("Hkv", [8, 2])
+def test_single_split_long_context(Hkv):
+    """One split over 21,000 tokens: 1,313 pages, more than the 1,024 page ids
+    a CTA stages at a time, so the second sub-chunk's ids are reloaded (with
+    Hkv = 2 four warps share each head and take every fourth page)."""
+    wl = W.WORKLOADS["qwen3_8b_32k"]
+    L = 21000
+    pt, _ = W.page_table(wl)
+    pt = pt[:1].copy()
+    c = Cache(wl, page_table=pt, num_pool_pages=int(pt.max()) + 1, num_heads=4 * Hkv,
+              num_kv_heads=Hkv)
+    for s0 in range(0, L, 7000):
+        c.append_range([0], s0, 7000)
+    q = W.queries(wl, 0, 50 + Hkv, batch=1)[:, :4 * Hkv].copy()
+    got = c.decode(q, [L], 1)
+    pairs = [[0, h] for h in range(0, 4 * Hkv, 3)]
+    want = c.oracle_decode(c.pool_host(), q, [L], pairs)
+    assert_close_attention(got[0, [p[1] for p in pairs]], want, f"1 split Hkv={Hkv}")
+    # the automatic split count: the same tolerance against the oracle, and
+    # both split counts agree far more closely than that
+    auto = c.decode(q, [L], 0)
+    assert_close_attention(auto[0, [p[1] for p in pairs]], want, f"auto splits Hkv={Hkv}")
+    for h in range(4 * Hkv):
+        d = np.linalg.norm(auto[0, h] - got[0, h]) / np.linalg.norm(got[0, h])
+        assert d <= 1e-4, (h, d)
+    assert c.status() == 0
+
+
 def test_multi_sequence_interleaved_append():
     """Tokens of several sequences in one call, in shuffled order, including
     several tokens of one page: every byte still lands where the oracle puts it."""
@@ -171,7 +220,7 @@ def test_multi_sequence_interleaved_append():
         near = compare_codes(c, pool, [(s, p, kv) for s, p in zip(seqs, pos) for kv in range(8)],
                              lambda s, p: Kt[np.nonzero((seqs == s) & (pos == p))[0][0]],
                              lambda s, p: Vt[np.nonzero((seqs == s) & (pos == p))[0][0]])
-        print("boundary-case code differences:", near)
+        assert_boundary_count(near, len(seqs) * 8, "interleaved")
     q = W.queries(wl, 0, 1, batch=B)
     got = c.decode(q, [n_per] * B, 2)
     pairs = [[b, h] for b in range(B) for h in range(0, 32, 5)]
@@ -207,7 +256,7 @@ def test_qwen32k_codes_sampled(qwen32k):
     samples += [(0, 0, 0), (15, 32767, 7), (3, 16, 2), (9, 32752, 5)]
     Ktok, Vtok = _block_fn(c.wl, 0)
     near = compare_codes(c, c.pool_host(), samples, Ktok, Vtok)
-    print("boundary-case code differences:", near)
+    assert_boundary_count(near, len(samples), "qwen32k")
     assert c.status() == 0
 
 
@@ -284,7 +333,7 @@ def test_ragged_batch_decode():
     assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want, "ragged")
     Ktok, Vtok = _block_fn(wl, 0)
     near = compare_codes(c, c.pool_host(), _sample_tokens(rng, lens, 8, 400), Ktok, Vtok)
-    print("boundary-case code differences:", near)
+    assert_boundary_count(near, 400, "ragged")
     assert c.status() == 0
 
 
@@ -317,5 +366,5 @@ def test_full_stack_sampled_layers(layer):
     rng = np.random.default_rng(24 + layer)
     near = compare_codes(c, c.pool_host(), _sample_tokens(rng, [wl.prefill + 128] * B, 8, 300),
                          Ktok, Vtok)
-    print("boundary-case code differences:", near)
+    assert_boundary_count(near, 300, f"full stack layer {layer}")
     assert c.status() == 0
