@@ -63,6 +63,33 @@ int heads_per_cta(int Hkv) {
   return 1;
 }
 
+// Heads per CTA for a decode with a given split count: the largest divisor of
+// Hkv (at most 8) whose grid fills the GPU's CTA slots best, so that a small
+// batch with a fixed split count (one 128K sequence over 64 splits: 64 CTAs of
+// 8 heads on 152 SMs) spreads its heads over more CTAs.  Fewer heads per CTA
+// means more warps per head and a shared-memory merge of their partials; a
+// count is only taken if each warp still gets at least 16 pages (four stages)
+// of a full chunk.
+int heads_per_cta_for(const kvq_handle* h, int batch, int splits, int chunk_pages) {
+  const int Hkv = h->L.num_kv_heads;
+  const long slots = static_cast<long>(h->num_sms) * h->ctas_int2;
+  const int c_max = heads_per_cta(Hkv);
+  int best = c_max;
+  double best_fill = -1.0;
+  for (int c = c_max; c >= 1; c >>= 1) {
+    if (Hkv % c) continue;
+    if (c != c_max && chunk_pages * c < 16 * kvq::kInt2Warps) continue;
+    const long ctas = static_cast<long>(splits) * (Hkv / c) * batch;
+    const long waves = (ctas + slots - 1) / slots;
+    const double fill = static_cast<double>(ctas) / static_cast<double>(waves * slots);
+    if (fill > best_fill + 0.05) {       // a smaller c must fill clearly better
+      best_fill = fill;
+      best = c;
+    }
+  }
+  return best;
+}
+
 long decode_units(const kvq_handle* h, int batch, bool int2) {
   const int Hkv = h->L.num_kv_heads;
   return static_cast<long>(batch) * (int2 ? Hkv / heads_per_cta(Hkv) : Hkv);
@@ -188,7 +215,7 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
   a.qfrag = reinterpret_cast<const uint32_t*>(ws + w.qfrag_off);
   a.qmeta = reinterpret_cast<const float*>(ws + w.qmeta_off);
   a.part = reinterpret_cast<float*>(ws + w.part_off);
-  a.hpc = heads_per_cta(a.Hkv);
+  a.hpc = int2 ? heads_per_cta_for(h, batch, splits, a.chunk_pages) : heads_per_cta(a.Hkv);
   a.out = out;
   a.RVt = h->bank ? h->bank + static_cast<size_t>(2) * a.Hkv * kDim * kDim : nullptr;
   a.RV = h->bank ? h->bank + static_cast<size_t>(a.Hkv) * kDim * kDim : nullptr;
