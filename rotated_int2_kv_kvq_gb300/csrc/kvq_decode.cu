@@ -1264,7 +1264,7 @@ __device__ float window_partial(const DecodeArgs& a, WindowSmem& ws, int b, int 
 }
 
 template <bool kWindow>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   CombineSmem& sm = *reinterpret_cast<CombineSmem*>(smem_raw);
   WindowSmem& ws = *reinterpret_cast<WindowSmem*>(smem_raw + sizeof(CombineSmem));
@@ -1292,7 +1292,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(DecodeArgs a) 
   griddep_wait();       // the partials come from the decode kernel
   // Thread (h, d) loads element d of its head's first kPre split partials now,
   // so that these loads and the (m, l) loads below share one round trip.
-  constexpr int kPre = 32;
+  constexpr int kPre = 48;
   const float* parts_h = a.part + (static_cast<size_t>(b) * a.H + kv * G + h) * S * kPartStride;
   float v[kPre];
 #pragma unroll
