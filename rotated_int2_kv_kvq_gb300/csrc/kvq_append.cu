@@ -145,7 +145,10 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
       // every thread waits (bounded); the CTA leaves together if any gave up
       const bool ok = mbar_wait_bounded(bar_a, 0);
       if (__syncthreads_or(!ok)) {
-        if (tid == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+        if (tid == 0) {
+          atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+          mbar_drain(bar_a, 0);
+        }
         return;      // nothing was written for this CTA
       }
       r_ready = true;
@@ -275,7 +278,10 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
   }
   if (!r_ready) {
     // no tile for this CTA: still let the staged copy land before exiting
-    if (!mbar_wait_bounded(bar_a, 0) && tid == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+    if (!mbar_wait_bounded(bar_a, 0)) {
+      if (tid == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+      mbar_drain(bar_a, 0);
+    }
   }
 }
 

@@ -196,7 +196,10 @@ __device__ __forceinline__ void qprep_cta(const DecodeArgs& a, const float* __re
   if (rotate) {
     const bool ok = mbar_wait_bounded(bar, 0);
     if (__syncthreads_or(!ok)) {
-      if (i == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+      if (i == 0) {
+        atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+        mbar_drain(bar, 0);
+      }
       return;
     }
     float acc[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -322,7 +325,10 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
   }
   const bool ok = mbar_wait_bounded(bar, 0);
   if (__syncthreads_or(!ok)) {
-    if (i == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+    if (i == 0) {
+      atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+      mbar_drain(bar, 0);
+    }
     return;
   }
   // r_i = fmaf chains over j = 0..127, the vector elements read four j at a time
@@ -737,6 +743,9 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
 
   int gs = 0;            // this warp's stages consumed so far (ring phase)
   bool timed_out = false;
+  // after a wait gave up: this warp's stages still in flight, [drain_k, drain_end)
+  // of the sub-chunk whose stages start at ring position drain_base
+  int drain_k = 0, drain_end = 0, drain_base = 0;
   for (int sub = 0; sub < npg && !timed_out; sub += kMaxIds) {
     const int nsub = min(kMaxIds, npg - sub);
     bool ids_ok = true;
@@ -763,6 +772,10 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
       if (!mbar_wait_bounded(smem_u32(&sm.full[warp][slot]), ((gs + k) / kNS) & 1)) {
         if (lane == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
         timed_out = true;
+        // stages k .. k + kNS - 1 (those below nst) have been issued
+        drain_k = k;
+        drain_end = min(k + kNS, nst);
+        drain_base = gs;
         break;
       }
       static_assert(kPPS % 2 == 0, "stages hold whole pairs of pages");
@@ -810,10 +823,12 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     // sm.ids is reloaded for the next sub-chunk; every warp leaves together
     timed_out = __syncthreads_or(timed_out);
   }
-  if (timed_out) {
-    // A wait gave up: let the copies already issued land (bounded) before the
-    // CTA can exit, so no bulk copy targets freed shared memory.
-    for (int s = 0; s < kNS; ++s) mbar_wait_bounded(smem_u32(&sm.full[warp][s]), 0);
+  // A wait gave up: let this warp's copies still in flight land (bounded), each
+  // on the phase it completes, before the CTA can exit, so no bulk copy targets
+  // freed shared memory.
+  for (int s = drain_k; s < drain_end; ++s) {
+    const int q = drain_base + s;
+    mbar_drain(smem_u32(&sm.full[warp][q % kNS]), (q / kNS) & 1);
   }
   griddep_launch_dependents();
   // the flushed totals back into the accumulator
@@ -1114,8 +1129,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_bf16_kernel(DecodeAr
     bf16_page_update(s, vf, v0, v1, kappa, g, t, acc, m_run, l_run);
   }
   if (i < count) {
-    for (int j = i + 1; j < count && j < i + kStagesBf16; ++j)
-      mbar_wait_bounded(smem_u32(&sm.bar[warp][j % kStagesBf16]), (j / kStagesBf16) & 1);
+    // stage i gave up; it and the stages issued after it may still be in flight
+    for (int j = i; j < count && j < i + kStagesBf16; ++j)
+      mbar_drain(smem_u32(&sm.bar[warp][j % kStagesBf16]), (j / kStagesBf16) & 1);
   }
   griddep_launch_dependents();
 #pragma unroll
@@ -1351,7 +1367,10 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs 
     sm.ot[d][h] = (kWindow && !a.rotate_out) ? owin : o;
     const bool ok = mbar_wait_bounded(bar, 0);
     if (__syncthreads_or(!ok)) {
-      if (tid == 0) atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+      if (tid == 0) {
+        atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+        mbar_drain(bar, 0);
+      }
       return;
     }
     {

@@ -225,6 +225,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// After a bounded wait on phase `parity` of `bar` gave up: wait once more
+// (bounded) so that a copy still in flight into this CTA's shared memory lands
+// before the CTA can exit and its shared memory be given to another CTA.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  (void)mbar_wait_bounded(bar, parity);
+}
+
 // One-dimensional bulk copy global -> shared (TMA, no tensor map), completing
 // `bytes` of transaction count on `bar`.  dst, src 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
