@@ -248,6 +248,200 @@ __global__ void __launch_bounds__((BM / 4) * (BM / 4)) gemm_tile_kernel(Gemm g) 
 }
 
 // ---------------------------------------------------------------------------
+// The same product on the tensor cores, for the large GEMMs (M and N multiples
+// of 64, K of 32): every fp32 operand x is split into two bf16 parts, hi =
+// bf16(x) and lo = bf16(x - hi), as it is staged into shared memory, and
+// op(A) op(B) is taken as Ah Bh + Ah Bl + Al Bh with mma.sync.m16n8k16 (bf16
+// in, fp32 accumulate).  The dropped Al Bl term and the residual of the split
+// are about 2^-16 of each product.  64 x 64 output tile, 32-deep k-slices
+// double-buffered (the next slice's fp32 loads in flight during the current
+// slice's products), 4 warps of 32 x 32; fragments come from shared memory by
+// ldmatrix (the transposing form for an operand kept [k][row]).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// hi and lo bf16 parts of x, packed with y's: {lo16 = part of x, hi16 = part of y}
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <int TA, int TB>
+__global__ void __launch_bounds__(128) gemm_tc_kernel(Gemm g) {
+  constexpr int BM = 64, BK = 32;
+  // An operand whose k is its contiguous index (A stored M x K, B stored N x K)
+  // is kept [row][k] with rows of 40 bf16 (80 B); the other (A stored K x M,
+  // B stored K x N) is kept as stored, [k][row] with rows of 72 bf16 (144 B),
+  // and read with the transposing ldmatrix.  Both strides put the 8 rows of
+  // one ldmatrix in different banks, and every staging store is 8 bytes.
+  constexpr int RK = BK + 8, RR = BM + 8, PLANE = BM * RK;
+  static_assert(BK * RR <= PLANE, "a [k][row] tile fits a plane");
+  __shared__ __align__(16) uint16_t sA[2][2][PLANE];    // [buffer][hi, lo]
+  __shared__ __align__(16) uint16_t sB[2][2][PLANE];
+  const int bz = blockIdx.z / g.ksplit, kz = blockIdx.z % g.ksplit;
+  const int kbeg = kz * g.kchunk, kend = min(g.K, kbeg + g.kchunk);
+  const float* A = g.A + bz * g.sA;
+  const float* B = g.B + bz * g.sB;
+  float* C = g.C + bz * g.sC;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BM;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wm = (warp >> 1) * 32, wn = (warp & 1) * 32;
+  constexpr bool kA = TA == 0, kB = TB == 1;     // k contiguous in global memory
+  float4 ra[4], rb[4];
+  // f-th float4 of a 64 x 32 slice: k-contiguous: row f / 8, k 4 (f % 8);
+  // row-contiguous: k f / 16, row 4 (f % 16)
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int f = tid + 128 * p;
+      ra[p] = kA ? *reinterpret_cast<const float4*>(A + static_cast<long long>(m0 + f / 8) * g.lda +
+                                                    k0 + 4 * (f % 8))
+                 : *reinterpret_cast<const float4*>(A + static_cast<long long>(k0 + f / 16) * g.lda +
+                                                    m0 + 4 * (f % 16));
+      rb[p] = kB ? *reinterpret_cast<const float4*>(B + static_cast<long long>(n0 + f / 8) * g.ldb +
+                                                    k0 + 4 * (f % 8))
+                 : *reinterpret_cast<const float4*>(B + static_cast<long long>(k0 + f / 16) * g.ldb +
+                                                    n0 + 4 * (f % 16));
+    }
+  };
+  auto put = [&](uint16_t* H, uint16_t* L, const float4& v, int f, bool kfast) {
+    const int off = kfast ? (f / 8) * RK + 4 * (f % 8) : (f / 16) * RR + 4 * (f % 16);
+    uint32_t h0, l0, h1, l1;
+    split_bf16x2(v.x, v.y, h0, l0);
+    split_bf16x2(v.z, v.w, h1, l1);
+    *reinterpret_cast<uint2*>(H + off) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(L + off) = make_uint2(l0, l1);
+  };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int f = tid + 128 * p;
+      put(sA[buf][0], sA[buf][1], ra[p], f, kA);
+      put(sB[buf][0], sB[buf][1], rb[p], f, kB);
+    }
+  };
+  float acc[2][4][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.0f;
+  int buf = 0;
+  if (kbeg < kend) {
+    load(kbeg);
+    store(0);
+  }
+  __syncthreads();
+  // Element offsets this lane gives ldmatrix.  A (m16 x k16 tile at row r0,
+  // k ks): matrix j = lane / 8 holds rows 8 (j & 1), k 8 (j >> 1); [row][k]:
+  // lane addresses row r0 + lane % 16, k ks + 8 (lane / 16); [k][row]
+  // (transposed): k ks + lane % 8 + 8 (lane / 16), row r0 + 8 ((lane / 8) % 2).
+  // B (two n8 tiles at row r0): matrix j holds rows 8 (j >> 1), k 8 (j & 1);
+  // [row][k]: row r0 + lane % 8 + 8 (lane / 16), k ks + 8 ((lane / 8) % 2);
+  // [k][row]: k ks + lane % 8 + 8 ((lane / 8) % 2), row r0 + 8 (lane / 16).
+  const int l8 = lane & 7, l16 = lane >> 4, lb = (lane >> 3) & 1;
+  auto a_off = [&](int r0, int ks) {
+    return kA ? (r0 + (lane & 15)) * RK + ks + 8 * l16 : (ks + l8 + 8 * l16) * RR + r0 + 8 * lb;
+  };
+  auto b_off = [&](int r0, int ks) {
+    return kB ? (r0 + l8 + 8 * l16) * RK + ks + 8 * lb : (ks + l8 + 8 * lb) * RR + r0 + 8 * l16;
+  };
+  for (int k0 = kbeg; k0 < kend; k0 += BK) {
+    const bool more = k0 + BK < kend;
+    if (more) load(k0 + BK);
+#pragma unroll
+    for (int ks = 0; ks < BK; ks += 16) {
+      uint32_t ah[2][4], al[2][4], bh[4][2], bl[4][2];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int o = a_off(wm + 16 * mt, ks);
+        const uint32_t h = static_cast<uint32_t>(__cvta_generic_to_shared(sA[buf][0] + o));
+        const uint32_t l = static_cast<uint32_t>(__cvta_generic_to_shared(sA[buf][1] + o));
+        if (kA) {
+          ldsm_x4(h, ah[mt][0], ah[mt][1], ah[mt][2], ah[mt][3]);
+          ldsm_x4(l, al[mt][0], al[mt][1], al[mt][2], al[mt][3]);
+        } else {
+          ldsm_x4_t(h, ah[mt][0], ah[mt][1], ah[mt][2], ah[mt][3]);
+          ldsm_x4_t(l, al[mt][0], al[mt][1], al[mt][2], al[mt][3]);
+        }
+      }
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        const int o = b_off(wn + 16 * np, ks);
+        const uint32_t h = static_cast<uint32_t>(__cvta_generic_to_shared(sB[buf][0] + o));
+        const uint32_t l = static_cast<uint32_t>(__cvta_generic_to_shared(sB[buf][1] + o));
+        if (kB) {
+          ldsm_x4(h, bh[2 * np][0], bh[2 * np][1], bh[2 * np + 1][0], bh[2 * np + 1][1]);
+          ldsm_x4(l, bl[2 * np][0], bl[2 * np][1], bl[2 * np + 1][0], bl[2 * np + 1][1]);
+        } else {
+          ldsm_x4_t(h, bh[2 * np][0], bh[2 * np][1], bh[2 * np + 1][0], bh[2 * np + 1][1]);
+          ldsm_x4_t(l, bl[2 * np][0], bl[2 * np][1], bl[2 * np + 1][0], bl[2 * np + 1][1]);
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          mma_bf16_acc(acc[mt][nt], al[mt], bh[nt][0], bh[nt][1]);
+          mma_bf16_acc(acc[mt][nt], ah[mt], bl[nt][0], bl[nt][1]);
+          mma_bf16_acc(acc[mt][nt], ah[mt], bh[nt][0], bh[nt][1]);
+        }
+    }
+    if (more) store(buf ^ 1);     // the other buffer was last read before the previous barrier
+    __syncthreads();
+    buf ^= 1;
+  }
+  const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int m = m0 + wm + 16 * mt + gq + 8 * hh;
+        const int n = n0 + wn + 8 * nt + 2 * tq;
+        float* c = C + static_cast<long long>(m) * g.ldc + n;
+        const float v0 = acc[mt][nt][2 * hh], v1 = acc[mt][nt][2 * hh + 1];
+        if (g.ksplit > 1) {
+          atomicAdd(c, g.alpha * v0);
+          atomicAdd(c + 1, g.alpha * v1);
+        } else {
+          float2 old = make_float2(0.0f, 0.0f);
+          if (g.beta != 0.0f) old = *reinterpret_cast<const float2*>(c);
+          const float r0 = (g.beta == 0.0f ? g.alpha * v0 : fmaf(g.alpha, v0, g.beta * old.x)) +
+                           (m == n ? g.diag : 0.0f);
+          const float r1 = (g.beta == 0.0f ? g.alpha * v1 : fmaf(g.alpha, v1, g.beta * old.y)) +
+                           (m == n + 1 ? g.diag : 0.0f);
+          *reinterpret_cast<float2*>(c) = make_float2(r0, r1);
+        }
+      }
+}
+
+// ---------------------------------------------------------------------------
 // Row kernels (one warp per row of kD = 128 elements; lane l owns 4l .. 4l+3)
 // ---------------------------------------------------------------------------
 
@@ -602,8 +796,16 @@ void gemm(Ctx& c, const float* A, int ta, long long sA, int lda, const float* B,
   const bool tiled = M % 32 == 0 && N % 32 == 0 && K % 64 == 0 && lda % 4 == 0 && ldb % 4 == 0 &&
                      ldc % 4 == 0 && sA % 4 == 0 && sB % 4 == 0 && sC % 4 == 0 && a16(A) &&
                      a16(B) && a16(C);
+  // Tensor cores (bf16 x 3) for every tiled product with 64-multiple M and N,
+  // except the products by a 128 x 128 matrix (N = K = 128): the rotations
+  // r = X R, r~ R^T and g_r~ = g_k~ R, whose rounding moves codes across the
+  // quantiser's boundaries (the straight-through gradient of a large generator
+  // then missed the float64 oracle by 2.7e-3), and the products of the matrix
+  // exponentials, whose errors the squarings amplify.  Those stay in fp32.
+  const bool tc = tiled && M % 64 == 0 && N % 64 == 0 && K % 32 == 0 && !(N == kD && K == kD);
   // the 64-wide tile where it still gives a full wave of CTAs, else 32
-  const int bm = (tiled && M % 64 == 0 && N % 64 == 0 &&
+  const int bm = tc ? 64
+               : (tiled && M % 64 == 0 && N % 64 == 0 &&
                   static_cast<long long>(M / 64) * (N / 64) * c.H >= 152) ? 64
                : tiled ? 32 : 64;
   // Few output tiles and a long K (the T-long reductions): cut K so that the
@@ -621,7 +823,16 @@ void gemm(Ctx& c, const float* A, int ta, long long sA, int lda, const float* B,
     c.err = cudaMemsetAsync(C, 0, static_cast<size_t>(c.H) * M * N * sizeof(float), c.st);
   Gemm g{A, B, C, M, N, K, lda, ldb, ldc, sA, sB, sC, alpha, beta, ta, tb, ksplit, kchunk, diag};
   dim3 grid((N + bm - 1) / bm, (M + bm - 1) / bm, c.H * ksplit);
-  if (!tiled)
+  if (tc) {
+    if (ta == 0 && tb == 0)
+      gemm_tc_kernel<0, 0><<<grid, 128, 0, c.st>>>(g);
+    else if (ta == 0)
+      gemm_tc_kernel<0, 1><<<grid, 128, 0, c.st>>>(g);
+    else if (tb == 0)
+      gemm_tc_kernel<1, 0><<<grid, 128, 0, c.st>>>(g);
+    else
+      gemm_tc_kernel<1, 1><<<grid, 128, 0, c.st>>>(g);
+  } else if (!tiled)
     gemm_kernel<<<grid, 256, 0, c.st>>>(g);
   else if (bm == 64)
     gemm_tile_kernel<64, 32><<<grid, 256, 0, c.st>>>(g);
