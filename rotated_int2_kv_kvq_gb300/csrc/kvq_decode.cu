@@ -646,17 +646,19 @@ struct Int2Smem {
   float tot[kW][32][32];     // per warp and lane: flushed P.V totals, [acc index][lane]
 };
 
-// Fill stage k of warp `warp` (pages kPPS*k .. kPPS*k + kPPS - 1 of the warp's
-// share of the sub-chunk: local page index gi + GPH * j), one bulk copy per
-// page.  Lane 0 only.
-__device__ __forceinline__ void issue_warp_stage(Int2Smem& sm, const DecodeArgs& a, int warp, int k,
-                                                 int slot, int npw, int gi, int GPH, int kv) {
-  int id[kPPS];
+// Fill stage k of warp `warp`: pages kPPS*k .. kPPS*k + kPPS - 1 of the warp's
+// share of the sub-chunk, one bulk copy per page.  idw: the warp's page ids,
+// contiguous and 16-byte aligned (one shared load per stage); a record is at
+// pool_kv + id * stride.  Lane 0 only.
+__device__ __forceinline__ void issue_warp_stage(Int2Smem& sm, const int* idw, int warp, int k,
+                                                  int slot, int npw, const uint8_t* pool_kv,
+                                                  size_t stride) {
+  const int4 v = *reinterpret_cast<const int4*>(idw + kPPS * k);
+  int id[kPPS] = {v.x, v.y, v.z, v.w};
   uint32_t bytes = 0;
 #pragma unroll
   for (int u = 0; u < kPPS; ++u) {
-    const int j = kPPS * k + u;
-    id[u] = j < npw ? sm.ids[gi + GPH * j] : -1;
+    if (kPPS * k + u >= npw) id[u] = -1;
     bytes += id[u] >= 0 ? kInt2Rec : 0;
   }
   const uint32_t bar = smem_u32(&sm.full[warp][slot]);
@@ -668,8 +670,8 @@ __device__ __forceinline__ void issue_warp_stage(Int2Smem& sm, const DecodeArgs&
 #pragma unroll
   for (int u = 0; u < kPPS; ++u)
     if (id[u] >= 0)
-      bulk_g2s(smem_u32(&sm.ring[warp][slot][u * kInt2Rec]),
-               a.pool + (static_cast<size_t>(id[u]) * a.Hkv + kv) * kInt2Rec, kInt2Rec, bar);
+      bulk_g2s(smem_u32(&sm.ring[warp][slot][u * kInt2Rec]), pool_kv + static_cast<size_t>(id[u]) * stride,
+               kInt2Rec, bar);
 }
 
 __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
@@ -741,6 +743,8 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) tot[32 * j] = 0.0f;
 
+  const uint8_t* const pool_kv = a.pool + static_cast<size_t>(kv) * kInt2Rec;
+  const size_t rec_stride = static_cast<size_t>(a.Hkv) * kInt2Rec;
   int gs = 0;            // this warp's stages consumed so far (ring phase)
   bool timed_out = false;
   // after a wait gave up: this warp's stages still in flight, [drain_k, drain_end)
@@ -756,16 +760,29 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
         const int id = sub == 0 ? spec[r] : ptab[p0 + sub + i];
         const bool ok = id >= 0 && id < a.num_pool_pages;
         if (!ok) atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
-        sm.ids[i] = ok ? id : -1;
+        // local page i goes to warp i % GPH of its head as that warp's page
+        // i / GPH: each warp's ids are contiguous
+        sm.ids[(i & (GPH - 1)) * (kMaxIds / GPH) + i / GPH] = ok ? id : -1;
         ids_ok = ids_ok && ok;
       }
     }
     const bool all_ids_ok = __syncthreads_and(ids_ok);
     const int npw = nsub > gi ? (nsub - gi + GPH - 1) / GPH : 0;   // this warp's pages
     const int nst = (npw + kPPS - 1) / kPPS;
+    const int* idw = sm.ids + gi * (kMaxIds / GPH);
+    // pairs (j, j + 1) with both pages present, valid and all their tokens in
+    // [lo, hi): jlo <= j < jend (page of warp page j: c + GPH j)
+    int jlo = 0, jend = 0;
+    {
+      const int c = p0 + sub + gi;
+      const int L = (lo + kPage - 1) / kPage;
+      jlo = L > c ? (L - c + GPH - 1) / GPH : 0;
+      const int tt = hi / kPage - 1 - c;
+      jend = (all_ids_ok && tt >= 0) ? min(npw - 1, tt / GPH) : 0;
+    }
     if (lane == 0)
       for (int k = 0; k < kNS && k < nst; ++k)
-        issue_warp_stage(sm, a, warp, k, (gs + k) % kNS, npw, gi, GPH, kv);
+        issue_warp_stage(sm, idw, warp, k, (gs + k) % kNS, npw, pool_kv, rec_stride);
 
     for (int k = 0; k < nst; ++k) {
       const int slot = (gs + k) % kNS;
@@ -795,19 +812,18 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
           __syncwarp();
           if (lane == 0 && k + kNS < nst) {
             fence_proxy_async();
-            issue_warp_stage(sm, a, warp, k + kNS, slot, npw, gi, GPH, kv);
+            issue_warp_stage(sm, idw, warp, k + kNS, slot, npw, pool_kv, rec_stride);
           }
         }
         if (j >= npw) continue;
         // both pages present, valid and all their tokens in [lo, hi)
-        const bool full = all_ids_ok && j + 1 < npw && (p0 + sub + ub + 1) * kPage <= hi &&
-                          (p0 + sub + ua) * kPage >= lo;
+        const bool full = j >= jlo && j < jend;
         if (full) {
           process_pair<false>(ws, qf, kappa, zeta, g, t, kwa, vwa, mta, kwb, vwb, mtb, true, true,
                               true, true);
         } else {
-          const bool oka = sm.ids[ua] >= 0;
-          const bool okb = j + 1 < npw && sm.ids[ub] >= 0;
+          const bool oka = idw[j] >= 0;
+          const bool okb = j + 1 < npw && idw[j + 1] >= 0;
           const int posa = (p0 + sub + ua) * kPage, posb = (p0 + sub + ub) * kPage;
           const bool va0 = oka && posa + g >= lo && posa + g < hi;
           const bool va1 = oka && posa + g + 8 >= lo && posa + g + 8 < hi;
