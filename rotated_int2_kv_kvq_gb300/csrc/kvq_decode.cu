@@ -445,16 +445,15 @@ __device__ __forceinline__ uint32_t code_op(uint32_t w) {
 // tok g+8 hi}.
 __device__ __forceinline__ void page_scores(const uint4& kw, const uint32_t (&qf)[16],
                                             float (&s)[4]) {
-  // two accumulators (even / odd k-blocks) halve the dependent tensor-core chain
-  float e[4] = {0.0f, 0.0f, 0.0f, 0.0f}, o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #define KVQ_KSTEP(ACC, P) \
   mma_f16(ACC, code_op<P>(kw.x), code_op<P>(kw.z), code_op<P>(kw.y), code_op<P>(kw.w), \
           qf[2 * (P)], qf[2 * (P) + 1])
-  KVQ_KSTEP(e, 0); KVQ_KSTEP(o, 1); KVQ_KSTEP(e, 2); KVQ_KSTEP(o, 3);
-  KVQ_KSTEP(e, 4); KVQ_KSTEP(o, 5); KVQ_KSTEP(e, 6); KVQ_KSTEP(o, 7);
+  // one accumulator chain per page (the pair's two pages are independent
+  // chains; two chains per page cost four adds and four zeroings more)
+  s[0] = s[1] = s[2] = s[3] = 0.0f;
+  KVQ_KSTEP(s, 0); KVQ_KSTEP(s, 1); KVQ_KSTEP(s, 2); KVQ_KSTEP(s, 3);
+  KVQ_KSTEP(s, 4); KVQ_KSTEP(s, 5); KVQ_KSTEP(s, 6); KVQ_KSTEP(s, 7);
 #undef KVQ_KSTEP
-#pragma unroll
-  for (int k = 0; k < 4; ++k) s[k] = e[k] + o[k];
 }
 
 // O^T[dims][cols] += Vcode^T . P for one page.  vw: the lane's V-code words
