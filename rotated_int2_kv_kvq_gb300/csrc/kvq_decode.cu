@@ -651,8 +651,10 @@ struct Int2Smem {
 // pool_kv + id * stride.  Lane 0 only.
 __device__ __forceinline__ void issue_warp_stage(Int2Smem& sm, const int* idw, int warp, int k,
                                                   int slot, int npw, const uint8_t* pool_kv,
-                                                  size_t stride) {
+                                                  uint32_t stride) {
   const int4 v = *reinterpret_cast<const int4*>(idw + kPPS * k);
+  const uint32_t bar = smem_u32(&sm.full[warp][slot]);
+  const uint32_t dst = smem_u32(&sm.ring[warp][slot][0]);
   int id[kPPS] = {v.x, v.y, v.z, v.w};
   uint32_t bytes = 0;
 #pragma unroll
@@ -660,7 +662,6 @@ __device__ __forceinline__ void issue_warp_stage(Int2Smem& sm, const int* idw, i
     if (kPPS * k + u >= npw) id[u] = -1;
     bytes += id[u] >= 0 ? kInt2Rec : 0;
   }
-  const uint32_t bar = smem_u32(&sm.full[warp][slot]);
   if (bytes == 0) {
     mbar_arrive(bar);
     return;
@@ -669,8 +670,8 @@ __device__ __forceinline__ void issue_warp_stage(Int2Smem& sm, const int* idw, i
 #pragma unroll
   for (int u = 0; u < kPPS; ++u)
     if (id[u] >= 0)
-      bulk_g2s(smem_u32(&sm.ring[warp][slot][u * kInt2Rec]), pool_kv + static_cast<size_t>(id[u]) * stride,
-               kInt2Rec, bar);
+      bulk_g2s(dst + u * kInt2Rec,
+               pool_kv + static_cast<uint64_t>(static_cast<uint32_t>(id[u])) * stride, kInt2Rec, bar);
 }
 
 __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
@@ -743,7 +744,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   for (int j = 0; j < 32; ++j) tot[32 * j] = 0.0f;
 
   const uint8_t* const pool_kv = a.pool + static_cast<size_t>(kv) * kInt2Rec;
-  const size_t rec_stride = static_cast<size_t>(a.Hkv) * kInt2Rec;
+  const uint32_t rec_stride = static_cast<uint32_t>(a.Hkv) * kInt2Rec;   // <= 64 x 1152
   int gs = 0;            // this warp's stages consumed so far (ring phase)
   bool timed_out = false;
   // after a wait gave up: this warp's stages still in flight, [drain_k, drain_end)
