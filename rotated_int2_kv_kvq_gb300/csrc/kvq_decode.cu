@@ -30,9 +30,10 @@
 // with col = 2*head + {hi, lo}: each operand that is not a code is split into an
 // fp16 high part and an fp16 residual (the query's scaled by 2^11 so it stays a
 // normal number), which keeps products at fp32 accuracy.  Codes become fp16 operands
-// with shifts and ANDs: a 2-bit field moved to bits 9-10 (or 7-8) of a 16-bit
-// half is the fp16 number code * 2^-15 (or code * 2^-17), exactly; the powers of
-// two are folded into the query operands and removed in the value epilogue.
+// with one AND each (and one or two shifts per word of 16 codes): a 2-bit field
+// at bit offset B < 9 of a 16-bit half is the fp16 number code * 2^(B - 24),
+// exactly; the powers of two are folded into the query operands and removed in
+// the value epilogue.
 //
 // Kernel chain of one decode call: qprep (or step_prep, which also appends the
 // new token) -> decode -> combine, each launched as a programmatic dependent of
@@ -70,15 +71,20 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Bit offset, within its fp16 half, of the tensor-core operand made from code
+// position P (0..7) of a fragment word (see field_op below): the operand is
+// code * 2^(code_bit(P) - 24).
+__host__ __device__ constexpr int code_bit(int P) { return P < 2 ? 2 * P + 6 : (P < 5 ? 2 * P : 2 * P - 6); }
+
 // ---------------------------------------------------------------------------
 // Query preparation: q_rot = q R_K for the G query heads of one sequence and one
 // KV head per CTA (R_K staged in shared memory by a bulk copy), then the
 // scores' B fragments.  B[row][col] for k-block w holds x = q_rot[head][16w+row]
-// * 2^(e_head), where 2^e_head brings max|q_rot| into [2^13, 2^14): column
-// 2*head is fp16(x), column 2*head+1 the residual (x - fp16(x)) * 2^11.  With
-// codes entering as code * 2^-16 (see the file comment) the score of a token is
-// q_rot . c = 2^(16 - e) * (hi + 2^-11 lo).  (Even k-blocks carry x * 2, odd ones
-// x / 2, matching the code scales 2^-17 and 2^-15 of code_op.)  Per head also: kappa =
+// * 2^(e_head + 8 - code_bit(w)), where 2^e_head brings max|q_rot| into
+// [2^10, 2^11) (so x < 2^15 stays an fp16 number): column 2*head is fp16(x),
+// column 2*head+1 the residual (x - fp16(x)) * 2^11.  Codes of k-block w enter
+// as code * 2^(code_bit(w) - 24), so every product is code * q_rot * 2^(e - 16)
+// and the score of a token is q_rot . c = 2^(16 - e) * (hi + 2^-11 lo).  Per head also: kappa =
 // sm_scale*log2e * 2^(16 - e), zeta = sm_scale*log2e * sum(q_rot) and
 // qmu = sm_scale*log2e * (q . mu), the logit shift that centring the keys took
 // out ("What carries the argument", mechanism 2); only a decode that mixes INT2
@@ -127,7 +133,7 @@ __device__ __forceinline__ void qprep_tail(const DecodeArgs& a, float (&qs)[kMax
       if (m > 0.0f && m < INFINITY) {
         int E;
         frexpf(m, &E);           // m = f * 2^E, f in [0.5, 1)
-        e = 14 - E;              // m * 2^e in [2^13, 2^14)
+        e = 11 - E;              // m * 2^e in [2^10, 2^11)
       }
       e_sm[w] = e;
       float* meta = const_cast<float*>(a.qmeta) + (static_cast<size_t>(b) * a.Hkv + kv) * kQMeta;
@@ -151,9 +157,9 @@ __device__ __forceinline__ void qprep_tail(const DecodeArgs& a, float (&qs)[kMax
       if (head < G) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          // x * 2 for even k-blocks (codes enter as c * 2^-17), x / 2 for odd
-          // ones (c * 2^-15): every product is c * q * 2^(e - 16)
-          const float x = ldexpf(qr[head][row + u], e_sm[head] + ((w & 1) ? -1 : 1));
+          // codes of k-block w enter as c * 2^(code_bit(w) - 24): every
+          // product is c * q * 2^(e - 16)
+          const float x = ldexpf(qr[head][row + u], e_sm[head] + 8 - code_bit(w));
           const __half hi = __float2half_rn(x);
           x2[u] = part ? (x - __half2float(hi)) * 2048.0f : __half2float(hi);
         }
@@ -425,19 +431,27 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
 // ---------------------------------------------------------------------------
 
 // fp16x2 operand of code position P (0..7) of a fragment word: the fields at
-// bits [2P, 2P+1] and [16+2P, 17+2P] moved to bits 9-10 (odd P) or bits 7-8
-// (even P) of their half.  As fp16 numbers these are code * 2^-15 (bit 9 is the
-// top mantissa bit, bit 10 the lowest exponent bit: 0, 2^-15, 2^-14, 3*2^-15)
-// and code * 2^-17, exactly.  One shift serves two positions.  Tensor cores
-// keep (nearly) full product precision for such operands; a field left at the
-// low mantissa bits would lose up to ~13 bits of the product.
-template <int P>
-__device__ __forceinline__ uint32_t code_op(uint32_t w) {
-  constexpr uint32_t kM = (P & 1) ? 0x06000600u : 0x01800180u;
-  constexpr int kShift = 7 - 2 * (P & ~1);     // left shift; negative = right shift
-  if constexpr (kShift >= 0) return (w << kShift) & kM;
-  else return (w >> (-kShift)) & kM;
+// bits [2P, 2P+1] and [16+2P, 17+2P], each moved to bit offset B of its half
+// and isolated by one AND.  A half whose only set bits lie in [0, 10) is the
+// fp16 number (bits) * 2^-24 (subnormal, or the smallest normal binade), so
+// the field is exactly code * 2^(B - 24).  Tensor cores keep fewer product bits
+// the further the field sits below bit 9, about one bit per place (measured on
+// GB300: relative error of a 128-term score 3e-7 with fields at offsets 4..8,
+// 1e-5 at offset 0; of a 16-token value sum 2.6e-6 at offset 4, 4e-5 at
+// offset 0).  Fields 2-4 are used where they are (offsets 4, 6, 8), fields 0-1
+// shifted left by 6 and fields 5-7 right by 6: two shifts and eight ANDs per
+// word of 16 codes.
+template <int P, int B>
+__device__ __forceinline__ uint32_t field_op(uint32_t w) {
+  static_assert(B >= 0 && B + 1 < 10, "the field stays below the exponent's second bit");
+  constexpr uint32_t kM = (3u << B) | (3u << (B + 16));
+  constexpr int kShift = B - 2 * P;
+  if constexpr (kShift > 0) return (w << kShift) & kM;
+  else if constexpr (kShift < 0) return (w >> (-kShift)) & kM;
+  else return w & kM;
 }
+template <int P>
+__device__ __forceinline__ uint32_t code_op(uint32_t w) { return field_op<P, code_bit(P)>(w); }
 
 // Scores of one page for this lane: tokens g and g+8 of head t (qc, before the
 // per-token scale/zero).  kw: the lane's K-code words {tok g h0, tok g h1,
@@ -859,11 +873,10 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     ws.l_run += __shfl_xor_sync(0xffffffffu, ws.l_run, off);
     ws.z_run += __shfl_xor_sync(0xffffffffu, ws.z_run, off);
   }
-  // undo the code scale (2^-17 for even m-blocks, 2^-15 for odd ones) and the
-  // weight scale 2^(14 - kLazy) = 2^6 (also on l_run, z_run and m_run); the
-  // residual column carries 2^11 more
-  constexpr float kInvEven = 2048.0f;   // 2^(17 - 6)
-  constexpr float kInvOdd = 512.0f;     // 2^(15 - 6)
+  // undo the code scale 2^(code_bit(mb) - 24) of m-block mb and the weight
+  // scale 2^(14 - kLazy) = 2^6 (also on l_run, z_run and m_run); the residual
+  // column carries 2^11 more
+  static_assert(kLazy == 8.0f, "the value factors below carry the weight scale 2^6");
   if (GPH == 1) {
     // One warp per KV head: its (m, l, o) is the split partial as it stands,
     // stored straight from registers (a merge through shared memory would be a
@@ -877,7 +890,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
       const float zr = ws.z_run * 0x1p-6f;
 #pragma unroll
       for (int mb = 0; mb < 8; ++mb) {
-        const float inv = (mb & 1) ? kInvOdd : kInvEven;
+        const float inv = static_cast<float>(1u << (18 - code_bit(mb)));
         const float o0 = fmaf(fmaf(ws.acc[mb][1], 0x1p-11f, ws.acc[mb][0]), inv, zr);
         const float o1 = fmaf(fmaf(ws.acc[mb][3], 0x1p-11f, ws.acc[mb][2]), inv, zr);
         p[4 + 16 * mb + g] = any ? o0 + 0.0f : 0.0f;
@@ -893,7 +906,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   if (t < a.G) {
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
-      const float inv = (mb & 1) ? kInvOdd : kInvEven;
+      const float inv = static_cast<float>(1u << (18 - code_bit(mb)));
       sm.mg.o[warp][t][16 * mb + g] =
           fmaf(fmaf(ws.acc[mb][1], 0x1p-11f, ws.acc[mb][0]), inv, ws.z_run * 0x1p-6f);
       sm.mg.o[warp][t][16 * mb + g + 8] =
