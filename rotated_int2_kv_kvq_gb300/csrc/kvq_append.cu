@@ -16,17 +16,53 @@
 namespace kvq {
 namespace {
 
-constexpr int kAppWarps = 8;
-constexpr int kAppThreads = kAppWarps * 32;
 constexpr int kRBytes = kDim * kDim * 4;   // one rotation matrix in fp32
+constexpr int kAUnroll = 8;                // rotation steps unrolled
+// A token's 128 codes (one byte each) take a row of 132 bytes: rows 33 words
+// apart put the eight tokens that a warp's lanes read together in eight
+// different banks during the scatter.
+constexpr int kCodeRow = kDim + 4;
 
-template <int TPW>
+// code = min(max(rint(fl(d / s)), 0), 3), fl the correctly rounded fp32
+// quotient, for s > 0.  The quotient is first taken as d * rcp(s) (rcp.approx:
+// relative error below 2^-22, the product's rounding 2^-24): for |q| < 4 that
+// estimate is within 2^-20 of d / s, and fl(d / s) within 2^-23, so unless the
+// estimate lies within 2^-18 of a half-integer both round to the same integer
+// and the estimate decides the code.  Otherwise (rare) the correctly rounded
+// division decides it, as the format's operation sequence states.  For
+// |q| >= 4 both clamp to 3 (or 0), NaN gives 0 either way.
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+// max / min over the warp's 32 lanes in one instruction (NaN inputs ignored,
+// like fmaxf / fminf)
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float warp_min(float v) {
+  float r;
+  asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ uint32_t clamp_code(float q) {
+  return static_cast<uint32_t>(fminf(fmaxf(rintf(q), 0.0f), 3.0f));
+}
+__device__ __forceinline__ bool near_half(float q) {
+  return fabsf(__fsub_rn(__fsub_rn(q, floorf(q)), 0.5f)) < 0x1p-18f;
+}
+
+template <int TPW, int NW>
 struct AppendSmem {
-  static constexpr int kTile = kAppWarps * TPW;                 // tokens per tile
+  static constexpr int kTile = NW * TPW;                        // tokens per tile
   static constexpr int kR = 0;                                  // float [128][128]
   static constexpr int kC = kR + kRBytes;                       // float [128][kTile]
-  static constexpr int kCodes = kC + kDim * kTile * 4;          // u8 [kTile][128]
-  static constexpr int kSZ = kCodes + kTile * kDim;             // u32 [kTile]
+  static constexpr int kCodes = kC + kDim * kTile * 4;          // u8 [kTile][kCodeRow]
+  static constexpr int kMu = kCodes + kTile * kCodeRow;         // float [128]
+  static constexpr int kSZ = kMu + kDim * 4;                    // u32 [kTile]
   static constexpr int kRec = kSZ + kTile * 4;                  // long long [kTile]
   static constexpr int kBar = kRec + kTile * 8;                 // mbarrier
   static constexpr int kBytes = kBar + 16;
@@ -39,14 +75,16 @@ __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
 // Quantise tiles of tokens for one (KV head, K|V).  TPW = tokens per warp.
 // Warp w owns tokens [w*TPW, (w+1)*TPW) of a tile; lane L owns output elements
 // 4L..4L+3 of each of them.
-template <int TPW>
-__global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) {
-  using S = AppendSmem<TPW>;
+template <int TPW, int NW>
+__global__ void __launch_bounds__(NW * 32) append_int2_kernel(AppendArgs a) {
+  constexpr int kAppThreads = NW * 32;
+  using S = AppendSmem<TPW, NW>;
   constexpr int kTile = S::kTile;
   extern __shared__ __align__(128) uint8_t smem[];
   float* Rs = reinterpret_cast<float*>(smem + S::kR);
   float* Cs = reinterpret_cast<float*>(smem + S::kC);
   uint8_t* codes = smem + S::kCodes;
+  float* mus = reinterpret_cast<float*>(smem + S::kMu);
   uint32_t* sz = reinterpret_cast<uint32_t*>(smem + S::kSZ);
   long long* rec = reinterpret_cast<long long*>(smem + S::kRec);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::kBar);
@@ -69,6 +107,7 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
     mbar_init(bar_a, 1);
     fence_mbar_init();
   }
+  for (int i = tid; i < kDim; i += kAppThreads) mus[i] = mu ? mu[i] : 0.0f;
   __syncthreads();
   if (tid == 0) {
     mbar_arrive_expect_tx(bar_a, kRBytes);
@@ -134,8 +173,11 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
           v[2 * e + 1] = bf16_to_f32(w4[e] >> 16);
         }
         if (mu && tok0 + k < a.n) {
+          const float4 m0 = *reinterpret_cast<const float4*>(mus + ch * 8);
+          const float4 m1 = *reinterpret_cast<const float4*>(mus + ch * 8 + 4);
+          const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = __fsub_rn(v[e], mu[ch * 8 + e]);
+          for (int e = 0; e < 8; ++e) v[e] = __fsub_rn(v[e], mv[e]);
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) Cs[(ch * 8 + e) * kTile + k] = v[e];
@@ -164,11 +206,12 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[t][c] = 0.0f;
     const float4* R4 = reinterpret_cast<const float4*>(Rs);
-#pragma unroll 4
-    for (int j = 0; j < kDim; ++j) {
-      const float4 r = R4[j * (kDim / 4) + lane];
-      const float* cj = Cs + j * kTile + warp * TPW;
-      float c[TPW];
+    const float* cw = Cs + warp * TPW;
+    // operands of step j + 1 are loaded while step j's products run
+    float4 rn = R4[lane];
+    float cn[TPW];
+    auto load_c = [&](int j, float (&c)[TPW]) {
+      const float* cj = cw + j * kTile;
       if constexpr (TPW % 4 == 0) {
 #pragma unroll
         for (int t = 0; t < TPW; t += 4) {
@@ -178,6 +221,18 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
       } else {
 #pragma unroll
         for (int t = 0; t < TPW; ++t) c[t] = cj[t];
+      }
+    };
+    load_c(0, cn);
+#pragma unroll kAUnroll
+    for (int j = 0; j < kDim; ++j) {
+      const float4 r = rn;
+      float c[TPW];
+#pragma unroll
+      for (int t = 0; t < TPW; ++t) c[t] = cn[t];
+      if (j + 1 < kDim) {
+        rn = R4[(j + 1) * (kDim / 4) + lane];
+        load_c(j + 1, cn);
       }
 #pragma unroll
       for (int t = 0; t < TPW; ++t) {
@@ -191,13 +246,8 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
     // (4) group max/min (whole vector), clip, fp16 scale/zero, codes
 #pragma unroll
     for (int t = 0; t < TPW; ++t) {
-      float mx = fmaxf(fmaxf(acc[t][0], acc[t][1]), fmaxf(acc[t][2], acc[t][3]));
-      float mn = fminf(fminf(acc[t][0], acc[t][1]), fminf(acc[t][2], acc[t][3]));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-      }
+      const float mx = warp_max(fmaxf(fmaxf(acc[t][0], acc[t][1]), fmaxf(acc[t][2], acc[t][3])));
+      const float mn = warp_min(fminf(fminf(acc[t][0], acc[t][1]), fminf(acc[t][2], acc[t][3])));
       const float mxc = __fmul_rn(clip, mx);
       const float mnc = __fmul_rn(clip, mn);
       const float s32 = __fdiv_rn(__fsub_rn(mxc, mnc), 3.0f);
@@ -205,17 +255,25 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
       const __half zh = __float2half_rn(mnc);
       const float s = __half2float(sh), z = __half2float(zh);
       uint32_t packed = 0;
+      if (s != 0.0f) {
+        const float rs = rcp_approx(s);
+        float d[4], q[4];
+        bool near = false;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t code = 0;
-        if (s != 0.0f) {
-          const float q = __fdiv_rn(__fsub_rn(acc[t][c], z), s);
-          code = static_cast<uint32_t>(fminf(fmaxf(rintf(q), 0.0f), 3.0f));
+        for (int c = 0; c < 4; ++c) {
+          d[c] = __fsub_rn(acc[t][c], z);
+          q[c] = __fmul_rn(d[c], rs);
+          near = near || near_half(q[c]);
         }
-        packed |= code << (8 * c);
+        if (near) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) q[c] = __fdiv_rn(d[c], s);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) packed |= clamp_code(q[c]) << (8 * c);
       }
       const int k = warp * TPW + t;
-      reinterpret_cast<uint32_t*>(codes)[k * (kDim / 4) + lane] = packed;
+      reinterpret_cast<uint32_t*>(codes)[k * (kCodeRow / 4) + lane] = packed;
       if (lane == 0)
         sz[k] = static_cast<uint32_t>(__half_as_ushort(sh)) |
                 (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
@@ -231,7 +289,7 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
         if (r < 0) continue;
         const int tau = static_cast<int>(r % kPage);
         uint8_t* base = a.pool + r / kPage;
-        const uint8_t* ck = codes + k * kDim;
+        const uint8_t* ck = codes + k * kCodeRow;
         uint32_t word[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -255,7 +313,7 @@ __global__ void __launch_bounds__(kAppThreads) append_int2_kernel(AppendArgs a) 
         if (r < 0) continue;
         const int tau = static_cast<int>(r % kPage);
         uint8_t* base = a.pool + r / kPage;
-        const uint8_t* ck = codes + k * kDim;
+        const uint8_t* ck = codes + k * kCodeRow;
         uint32_t hv = 0;
 #pragma unroll
         for (int m = 0; m < 8; ++m) hv |= static_cast<uint32_t>(ck[16 * m + g + 8 * dh]) << (2 * m);
@@ -321,27 +379,29 @@ __global__ void __launch_bounds__(128) append_bf16_kernel(AppendArgs a) {
   }
 }
 
-template <int TPW>
+template <int TPW, int NW>
 cudaError_t launch_tpw(const AppendArgs& a, int num_sms, cudaStream_t st) {
-  using S = AppendSmem<TPW>;
+  using S = AppendSmem<TPW, NW>;
   static bool attr_set[64] = {};       // per device: the attribute is per context
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(append_int2_kernel<TPW>,
+    cudaError_t e = cudaFuncSetAttribute(append_int2_kernel<TPW, NW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int tiles = (a.n + S::kTile - 1) / S::kTile;
-  // Enough CTAs to fill the GPU about twice; each CTA loops over tiles so the
-  // rotation matrix is staged once per CTA, not once per tile.
+  // One wave of CTAs (two per SM, the shared-memory limit); each CTA loops
+  // over tiles so the rotation matrix is staged once per CTA, not once per
+  // tile (measured: 408 us per 32,767-token prefill against 419 us with two
+  // waves).
   const int per_head = a.Hkv * 2;
-  int gx = (2 * 2 * num_sms + per_head - 1) / per_head;
+  int gx = (2 * num_sms + per_head - 1) / per_head;
   if (gx > tiles) gx = tiles;
   if (gx < 1) gx = 1;
   dim3 grid(gx, a.Hkv, 2);
-  append_int2_kernel<TPW><<<grid, kAppThreads, S::kBytes, st>>>(a);
+  append_int2_kernel<TPW, NW><<<grid, NW * 32, S::kBytes, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -351,8 +411,8 @@ cudaError_t launch_append_int2(const AppendArgs& a, int num_sms, cudaStream_t st
   // Few tokens (decode-time appends): one token per warp keeps the dependent
   // fmaf chains short in wall time.  Many tokens (prefill): eight tokens per
   // warp reuse each staged rotation row eight times.
-  if (a.n <= 8 * num_sms / (a.Hkv > 0 ? a.Hkv : 1)) return launch_tpw<1>(a, num_sms, st);
-  return launch_tpw<8>(a, num_sms, st);
+  if (a.n <= 8 * num_sms / (a.Hkv > 0 ? a.Hkv : 1)) return launch_tpw<1, 8>(a, num_sms, st);
+  return launch_tpw<8, 8>(a, num_sms, st);
 }
 
 cudaError_t launch_append_bf16(const AppendArgs& a, cudaStream_t st) {
