@@ -380,6 +380,35 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def measure_prefill_append(K, torch, h, pool, npool, kd, vd, sid, pos, pt, Hkv, reps=5):
+    """Quantise-on-append of one sequence's prefill (the last sequence of the
+    cache build, appended again: the same bytes are rewritten), `reps` calls
+    back to back on the device.  The kernel is bound by its fixed-order fp32
+    rotation (fmaf chains): 2 x 128 x 128 flop per token, KV head and K|V,
+    against the fp32 FMA rate of the SMs at the maximum SM clock."""
+    n = int(kd.shape[0])
+    for _ in range(2):
+        K.kvq_append(h, pool, npool, kd, vd, sid, pos, pt)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        K.kvq_append(h, pool, npool, kd, vd, sid, pos, pt)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    flop = n * Hkv * 2 * 2 * 128 * 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    peak = sms * 128 * 2 * 2.07e9 / 1e12      # fp32 FMA lanes x 2 flop x 2070 MHz
+    achieved = flop / (us * 1e-6) / 1e12
+    return {"tokens": n, "kv_heads": Hkv, "us_per_call": us, "tokens_per_s": n / (us * 1e-6),
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "kernel": "append_int2_kernel",
+                         "peak_kind": f"nominal fp32 FMA rate: {sms} SMs x 128 lanes x 2 flop x "
+                                      f"2070 MHz (no measured fp32 peak on this pool)"},
+            "calls": reps}
+
+
 def measure_workload(K, torch, wl, splits_list, steps, warmup, l2, peak, cpu_seconds=0.0):
     """The decode step (kvq_append_decode: append each sequence's token at
     position len-1, decode over len tokens) on one of the other workloads.
@@ -522,6 +551,7 @@ def run_ours(args):
                 K.kvq_bf16_append(h, bf16_pool, npool, kd, vd, sid, pos, pt)
     torch.cuda.synchronize()
     t_build = time.perf_counter() - t_build
+    prefill = measure_prefill_append(K, torch, h, pool, npool, kd, vd, sid, pos, pt, Hkv)
     # step inputs: the token at position len-1 of every sequence, and the queries
     k_new = np.stack([W.token_at(wl, 0, b, 0, int(lens[b]) - 1) for b in range(B)])
     v_new = np.stack([W.token_at(wl, 0, b, 1, int(lens[b]) - 1) for b in range(B)])
@@ -796,6 +826,7 @@ def run_ours(args):
         "e2e": {"value": e2e_gbs, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "bf16_comparison": bf16,
+        "prefill_append": prefill,
         "bf16_window": window,
         "folded_rotations": folded,
         "two_call_step": two_calls,
