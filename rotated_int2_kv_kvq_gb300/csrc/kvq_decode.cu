@@ -1348,17 +1348,34 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs 
     // INT2 logits were taken against centred keys: with a window, add q.mu back
     const float qmu =
         kWindow ? a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * kQMeta + 8 + warp] : 0.0f;
-    const float m0 = lane < S ? parts[lane * kPartStride] : -INFINITY;
-    const float l0 = lane < S ? parts[lane * kPartStride + 1] : 0.0f;
-    float M = m0;
-    for (int j = lane + 32; j < S; j += 32) M = fmaxf(M, parts[j * kPartStride]);
+    // (m, l) of splits lane and lane + 32 in the same round trip as the
+    // partials above; only splits beyond 64 are read by a second one
+    constexpr int kML = 2;
+    float mk[kML], lk[kML];
+#pragma unroll
+    for (int k = 0; k < kML; ++k) {
+      const int j = lane + 32 * k;
+      mk[k] = j < S ? parts[j * kPartStride] : -INFINITY;
+      lk[k] = j < S ? parts[j * kPartStride + 1] : 0.0f;
+    }
+    float M = fmaxf(mk[0], mk[1]);
+    for (int j = lane + 32 * kML; j < S; j += 32) M = fmaxf(M, parts[j * kPartStride]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     if (kWindow) M = fmaxf(M + qmu, ws.M[warp]);
     float L = 0.0f;
-    for (int j = lane; j < S; j += 32) {
-      const float mj = j == lane ? m0 : parts[j * kPartStride];
-      const float lj = j == lane ? l0 : parts[j * kPartStride + 1];
+#pragma unroll
+    for (int k = 0; k < kML; ++k) {
+      const int j = lane + 32 * k;
+      if (j < S) {
+        const float w = (mk[k] == -INFINITY) ? 0.0f : fast_exp2(mk[k] + qmu - M);
+        sm.w[warp][j] = w;
+        L = fmaf(w, lk[k], L);
+      }
+    }
+    for (int j = lane + 32 * kML; j < S; j += 32) {
+      const float mj = parts[j * kPartStride];
+      const float lj = parts[j * kPartStride + 1];
       const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj + qmu - M);
       sm.w[warp][j] = w;
       L = fmaf(w, lj, L);
