@@ -1443,6 +1443,128 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs 
   if (h < G) a.out[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + d] = o;
 }
 
+// The same combine with one CTA per query head (b, kv, h), for calls whose
+// (sequence, query head) count fills at most one wave of these CTAs (short
+// contexts with many splits, such as a 36-layer stack at 8K): each CTA merges
+// one head, so the partials a CTA loads and the dependent steps before its
+// store are a quarter of the per-KV-head combine's.  Thread (qq, d), qq =
+// tid / 128: element d of splits qq, qq + 4, ... (four interleaved quarters of
+// the merge, added in a fixed order), then quarter qq of the basis change of
+// element d.  R_V^T is staged by a bulk copy issued before the dependency wait.
+struct HeadCombineSmem {
+  float Rt[kDim * kDim];
+  float w[kMaxSplits];
+  float red[4][kDim];
+  float o[kDim];
+  float linv;
+  uint64_t bar;
+};
+constexpr int kHeadCombineCtasPerSm = 2;
+
+__global__ void __launch_bounds__(kCombineThreads, kHeadCombineCtasPerSm)
+    combine_head_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  HeadCombineSmem& sm = *reinterpret_cast<HeadCombineSmem*>(smem_raw);
+  const int b = blockIdx.x, kv = blockIdx.y, h = blockIdx.z, tid = threadIdx.x;
+  const int qq = tid / kDim, d = tid % kDim;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int S = a.splits, G = a.G;
+  const uint32_t bar = smem_u32(&sm.bar);
+  griddep_launch_dependents();      // as in combine_kernel
+  const bool stage = a.rotate_out != 0;
+  if (stage && tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, kDim * kDim * 4);
+    bulk_g2s(smem_u32(sm.Rt), a.RVt + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
+  }
+  griddep_wait();       // the partials come from the decode kernel
+  const float* parts = a.part + (static_cast<size_t>(b) * a.H + kv * G + h) * S * kPartStride;
+  constexpr int kPreQ = 16;         // splits qq + 4u, u < kPreQ, loaded in the first round trip
+  float v[kPreQ];
+#pragma unroll
+  for (int u = 0; u < kPreQ; ++u) {
+    const int s = qq + 4 * u;
+    v[u] = s < S ? parts[s * kPartStride + 4 + d] : 0.0f;
+  }
+  if (warp == 0) {
+    constexpr int kML = 2;
+    float mk[kML], lk[kML];
+#pragma unroll
+    for (int k = 0; k < kML; ++k) {
+      const int j = lane + 32 * k;
+      mk[k] = j < S ? parts[j * kPartStride] : -INFINITY;
+      lk[k] = j < S ? parts[j * kPartStride + 1] : 0.0f;
+    }
+    float M = fmaxf(mk[0], mk[1]);
+    for (int j = lane + 32 * kML; j < S; j += 32) M = fmaxf(M, parts[j * kPartStride]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kML; ++k) {
+      const int j = lane + 32 * k;
+      if (j < S) {
+        const float w = (mk[k] == -INFINITY) ? 0.0f : fast_exp2(mk[k] - M);
+        sm.w[j] = w;
+        L = fmaf(w, lk[k], L);
+      }
+    }
+    for (int j = lane + 32 * kML; j < S; j += 32) {
+      const float mj = parts[j * kPartStride];
+      const float lj = parts[j * kPartStride + 1];
+      const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj - M);
+      sm.w[j] = w;
+      L = fmaf(w, lj, L);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) sm.linv = (L > 0.0f) ? 1.0f / L : 0.0f;
+  }
+  __syncthreads();
+  float o = 0.0f;
+#pragma unroll
+  for (int u = 0; u < kPreQ; ++u)
+    if (qq + 4 * u < S) o = fmaf(sm.w[qq + 4 * u], v[u], o);
+  for (int s0 = 4 * kPreQ; s0 < S; s0 += 4 * kPreQ) {
+#pragma unroll
+    for (int u = 0; u < kPreQ; ++u) {
+      const int s = s0 + qq + 4 * u;
+      v[u] = s < S ? parts[s * kPartStride + 4 + d] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPreQ; ++u)
+      if (s0 + qq + 4 * u < S) o = fmaf(sm.w[s0 + qq + 4 * u], v[u], o);
+  }
+  sm.red[qq][d] = o;
+  __syncthreads();
+  if (qq == 0)
+    sm.o[d] = ((sm.red[0][d] + sm.red[1][d]) + (sm.red[2][d] + sm.red[3][d])) * sm.linv;
+  float* out = a.out + (static_cast<size_t>(b) * a.H + kv * G + h) * kDim;
+  if (!stage) {
+    if (qq == 0) out[d] = sm.o[d];
+    return;
+  }
+  const bool ok = mbar_wait_bounded(bar, 0);
+  if (__syncthreads_or(!ok)) {      // also orders sm.o and sm.red before the reuse below
+    if (tid == 0) {
+      atomicOr(a.status, KVQ_STATUS_TIMEOUT);
+      mbar_drain(bar, 0);
+    }
+    return;
+  }
+  // y R_V^T: thread (qq, d) sums j in quarter qq
+  float r = 0.0f;
+#pragma unroll 8
+  for (int jj = 0; jj < kDim / 4; ++jj) {
+    const int j = qq * (kDim / 4) + jj;
+    r = fmaf(sm.o[j], sm.Rt[j * kDim + d], r);
+  }
+  sm.red[qq][d] = r;
+  __syncthreads();
+  if (qq == 0) out[d] = (sm.red[0][d] + sm.red[1][d]) + (sm.red[2][d] + sm.red[3][d]);
+}
+
 // Dequantise positions [start, start+len) of one sequence: CTA per (position,
 // KV head), thread d per element, following the record layout of include/kvq.h.
 __global__ void __launch_bounds__(128) dequant_kernel(const uint8_t* __restrict__ pool,
@@ -1574,6 +1696,11 @@ cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     e = launch_dependent(combine_kernel<true>, dim3(a.batch, a.Hkv), dim3(kCombineThreads),
                          sizeof(CombineWindowSmem), st, a);
+  } else if (a.combine_per_head) {
+    e = set_smem_attr<HeadCombineSmem>(combine_head_kernel);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(combine_head_kernel, dim3(a.batch, a.Hkv, a.G), dim3(kCombineThreads),
+                         sizeof(HeadCombineSmem), st, a);
   } else {
     e = set_smem_attr<CombineSmem>(combine_kernel<false>);
     if (e != cudaSuccess) return e;
@@ -1597,6 +1724,8 @@ cudaError_t launch_transpose(const float* in, float* out, int count, cudaStream_
   transpose_kernel<<<grid, block, 0, st>>>(in, out);
   return cudaGetLastError();
 }
+
+int combine_head_ctas_per_sm() { return kHeadCombineCtasPerSm; }
 
 int decode_int2_ctas_per_sm() {
   if (set_smem_attr<Int2Smem>(decode_int2_kernel) != cudaSuccess) return 1;

@@ -49,6 +49,7 @@ struct DecodeArgs {
   const float* RVt;          // [Hkv][D][D] transposed value rotations
   const float* RV;           // [Hkv][D][D] value rotations
   int rotate_out;            // 1: out = o_rot R_V^T, 0: out = o_rot
+  int combine_per_head = 0;  // 1: the combine takes one CTA per query head (no window)
   uint32_t* status;
   float log2_scale;          // sm_scale * log2(e)
   // BF16 window (sink + recent tokens); window = 0 for a plain decode
@@ -116,6 +117,7 @@ int optr_loss_grad(int H, int T, int Nq, int G, int Dm, const uint16_t* K, const
                    const float* A_value, int which, float* loss, float* grad, void* workspace,
                    cudaStream_t st);
 int decode_int2_ctas_per_sm();
+int combine_head_ctas_per_sm();
 int decode_bf16_ctas_per_sm();
 // Makes `dev` the calling thread's current device while the guard lives and
 // gives the caller's device back afterwards, so that no entry point changes
