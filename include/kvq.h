@@ -228,8 +228,14 @@ size_t kvq_workspace_bytes(const kvq_handle* h, int batch, int num_splits);
  * k~, v~ are the dequantised cache entries.  The mean term q . mu is the same
  * for every t and is left out (it does not change softmax).  Positions in
  * [0, seq_lens[b]) must have been appended.  seq_lens[b] == 0 gives out = 0.
- * The context is cut into num_splits page-aligned chunks per (sequence, KV
- * head) whose partial softmax states are merged with a log-sum-exp combine.
+ * The context is cut into page-aligned chunks whose partial softmax states are
+ * merged with a log-sum-exp combine: num_splits chunks per (sequence, KV head)
+ * when the batch's batch * num_splits chunks fit one wave of decode CTAs;
+ * otherwise, with two or more sequences, those batch * num_splits chunks are
+ * shared out over the sequences in proportion to their lengths (one chunk
+ * size for the whole batch, so long and short sequences finish together; a
+ * batch of equal lengths gets the same chunks either way).  The result does
+ * not depend on the chunking beyond fp32 rounding.
  *   q          : device bf16 [batch][H][D].
  *   page_table : device int32 [batch][max_pages].
  *   seq_lens   : device int32 [batch].

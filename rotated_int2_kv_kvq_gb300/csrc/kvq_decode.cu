@@ -56,6 +56,8 @@ DecodeWs decode_ws_layout(int batch, int Hkv, int H, int splits, bool int2) {
   if (int2) o += up(static_cast<size_t>(batch) * Hkv * kQMeta * 4);
   w.part_off = o;
   o += up(static_cast<size_t>(batch) * H * splits * kPartStride * 4);
+  w.sched_off = o;
+  if (int2) o += up(static_cast<size_t>(batch) * splits * 16 + static_cast<size_t>(batch) * 8);
   w.total = o;
   return w;
 }
@@ -233,11 +235,108 @@ __device__ __forceinline__ void qprep_cta(const DecodeArgs& a, const float* __re
   qprep_tail(a, sm.qs, sm.qr, sm.e, mu, log2_scale, b, kv);
 }
 
+// ---------------------------------------------------------------------------
+// Length-balanced decode schedule (a.balanced), written by one extra CTA of
+// the query-preparation kernel (128 threads) after its dependency wait: the
+// smallest chunk size P (pages) such that the batch's chunks, ceil(n_b / P) for
+// a sequence of n_b pages, number at most batch * splits (the decode grid) and
+// at most kMaxSplits per sequence, and at least 8 pages unless no sequence is
+// that long; then each sequence's chunk count, the first partial slot of each
+// sequence (prefix sum) and the CTA -> (sequence, chunk) map.  A sequence with
+// an invalid length gets no chunk (its output is 0) and sets
+// KVQ_STATUS_BAD_SEQLEN.  With equal lengths the chunks are those of the plain
+// schedule (the same split count per sequence).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int block_sum128(int v, int* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  __syncthreads();                       // red may still be read from a previous call
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  return (red[0] + red[1]) + (red[2] + red[3]);
+}
+
+__device__ void schedule_cta(const DecodeArgs& a) {
+  __shared__ int red[4];
+  __shared__ int scan[128];
+  const int tid = threadIdx.x, B = a.batch;
+  const int C = a.batch * a.splits;            // decode CTAs along x
+  griddep_wait();                              // seq_lens may come from a predecessor
+  // pages of each sequence, kept in sched_nsplit until the chunk size is known
+  int nmax = 0;
+  for (int b = tid; b < B; b += 128) {
+    const int len = a.seq_lens[b];
+    int n = 0;
+    if (len < 0 || len > a.max_pages * kPage) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
+    else n = (len + kPage - 1) / kPage;
+    a.sched_nsplit[b] = n;
+    nmax = max(nmax, n);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) nmax = max(nmax, __shfl_xor_sync(0xffffffffu, nmax, off));
+  if ((tid & 31) == 0) red[tid >> 5] = nmax;
+  __syncthreads();
+  nmax = max(max(red[0], red[1]), max(red[2], red[3]));
+  // smallest P in [1, max(nmax, 1)] with sum_b ceil(n_b / P) <= C and
+  // ceil(nmax / P) <= kMaxSplits (P = nmax always qualifies: one chunk each)
+  int lo = 1, hi = max(nmax, 1);
+  while (lo < hi) {                            // uniform across the CTA
+    const int P = (lo + hi) >> 1;
+    int cnt = 0;
+    for (int b = tid; b < B; b += 128) cnt += (a.sched_nsplit[b] + P - 1) / P;
+    cnt = block_sum128(cnt, red);
+    if (cnt <= C && (nmax + P - 1) / P <= kMaxSplits) hi = P;
+    else lo = P + 1;
+  }
+  const int P = max(lo, min(8, max(nmax, 1)));
+  // chunk counts and their exclusive prefix: thread t takes sequences
+  // [t * per, (t + 1) * per)
+  const int per = (B + 127) / 128;
+  const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += (a.sched_nsplit[b] + P - 1) / P;
+  scan[tid] = local;
+  __syncthreads();
+  if (tid < 32) {                              // warp 0 scans the 128 partial sums
+    int v[4], sum = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) { v[k] = scan[4 * tid + k]; sum += v[k]; }
+    int x = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (tid >= off) x += y;
+    }
+    int run = x - sum;                         // exclusive prefix of this lane's four
+#pragma unroll
+    for (int k = 0; k < 4; ++k) { scan[4 * tid + k] = run; run += v[k]; }
+  }
+  __syncthreads();
+  int base = scan[tid];
+  for (int b = b0; b < b1; ++b) {
+    const int ns = (a.sched_nsplit[b] + P - 1) / P;
+    a.sched_nsplit[b] = ns;
+    a.sched_base[b] = base;
+    for (int k = 0; k < ns; ++k) a.sched_map[base + k] = make_int4(b, k, base, P);
+    base += ns;
+  }
+  // the last thread's running prefix is the total chunk count; CTAs past it
+  // get no chunk
+  __syncthreads();
+  if (tid == 127) red[0] = base;
+  __syncthreads();
+  for (int c = red[0] + tid; c < C; c += 128) a.sched_map[c] = make_int4(-1, 0, 0, 0);
+}
+
 __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* __restrict__ RK,
                                                     const float* __restrict__ mu,
                                                     float log2_scale) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   griddep_launch_dependents();
+  if (blockIdx.x == a.batch) {       // the extra column of a balanced decode
+    if (blockIdx.y == 0) schedule_cta(a);
+    return;
+  }
   qprep_cta(a, RK, mu, log2_scale, *reinterpret_cast<QprepSmem*>(smem_raw), blockIdx.x, blockIdx.y);
 }
 
@@ -270,6 +369,10 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int b = blockIdx.x, kv = blockIdx.y, i = threadIdx.x;
   griddep_launch_dependents();
+  if (b == a.batch) {                // the extra column of a balanced decode
+    if (kv == 0 && blockIdx.z == 0) schedule_cta(a);
+    return;
+  }
   if (blockIdx.z == 1) {
     qprep_cta(a, st.q_rotated ? nullptr : st.RK, st.mu, a.log2_scale,
               reinterpret_cast<StepPrepSmem*>(smem_raw)->query, b, kv);
@@ -688,12 +791,16 @@ __device__ __forceinline__ void issue_warp_stage(Int2Smem& sm, const int* idw, i
                pool_kv + static_cast<uint64_t>(static_cast<uint32_t>(id[u])) * stride, kInt2Rec, bar);
 }
 
+// kBalanced: CTA (c, hg) takes the chunk that the balanced schedule assigns to
+// c (DecodeArgs::sched_map); otherwise CTA (split, hg, b) takes chunk `split`
+// of sequence b, chunk_pages pages each.
+template <bool kBalanced>
 __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Int2Smem& sm = *reinterpret_cast<Int2Smem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int split = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  const int hg = blockIdx.y;
   const int HPC = a.hpc, GPH = kW / HPC;
   const int hl = warp / GPH, gi = warp % GPH;
   const int kv = hg * HPC + hl;
@@ -703,17 +810,36 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     fence_mbar_init();
   }
   griddep_wait();      // inputs (pool, tables, rotated queries) come from predecessors
+  int split, b, chunk_pages, slot0;
+  if constexpr (kBalanced) {
+    const int4 m = a.sched_map[blockIdx.x];
+    if (m.x < 0) return;             // no chunk for this CTA (nothing issued yet)
+    b = m.x;
+    split = m.y;
+    slot0 = m.z;
+    chunk_pages = m.w;
+  } else {
+    split = blockIdx.x;
+    b = blockIdx.z;
+    slot0 = 0;
+    chunk_pages = a.chunk_pages;
+  }
+  // split partial of head `head` (of sequence b)
+  auto part_of = [&](int head) -> float* {
+    return kBalanced ? a.part + (static_cast<size_t>(slot0 + split) * a.H + head) * kPartStride
+                     : a.part + ((static_cast<size_t>(b) * a.H + head) * a.splits + split) * kPartStride;
+  };
 
   // INT2 tokens: positions [lo, hi); with a BF16 window the first win_sink and
   // the last win_recent positions are left to the window pass.
   const int lo = a.win_sink;
-  const int p0 = max(split * a.chunk_pages, lo / kPage);
+  const int p0 = max(split * chunk_pages, lo / kPage);
   const int32_t* ptab = a.page_table + static_cast<size_t>(b) * a.max_pages;
   // The first sub-chunk's page ids are loaded together with seq_len (one round
   // trip instead of two): every entry of the split's chunk inside the table,
   // of which those below the sequence's end are used.
   constexpr int kIdsPerThread = kMaxIds / (kW * 32);
-  const int nspec = min(kMaxIds, max(0, min(split * a.chunk_pages + a.chunk_pages, a.max_pages) - p0));
+  const int nspec = min(kMaxIds, max(0, min(split * chunk_pages + chunk_pages, a.max_pages) - p0));
   int spec[kIdsPerThread];
 #pragma unroll
   for (int r = 0; r < kIdsPerThread; ++r) {
@@ -727,7 +853,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
   }
   const int hi = max(seq_len - a.win_recent, 0);
   const int n_pages = (hi + kPage - 1) / kPage;      // <= max_pages, so npg <= nspec
-  const int npg = max(0, min(split * a.chunk_pages + a.chunk_pages, n_pages) - p0);
+  const int npg = max(0, min(split * chunk_pages + chunk_pages, n_pages) - p0);
 
   // B fragments of the rotated query and the head's logit constants
   uint32_t qf[16];
@@ -884,8 +1010,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
     // merge below with a single term: an empty head gives (-inf, 0, 0), and
     // "+ 0" turns a -0 into the +0 that merge's fmaf(1, o, 0) gives.
     if (t < a.G) {
-      float* p = a.part + ((static_cast<size_t>(b) * a.H + kv * a.G + t) * a.splits + split) *
-                              kPartStride;
+      float* p = part_of(kv * a.G + t);
       const bool any = ws.m_run > -INFINITY;
       const float zr = ws.z_run * 0x1p-6f;
 #pragma unroll
@@ -934,8 +1059,7 @@ __global__ void __launch_bounds__(kW * 32, 2) decode_int2_kernel(DecodeArgs a) {
           o = fmaf(f, sm.mg.o[w][h][d], o);
         }
       }
-      float* p = a.part + ((static_cast<size_t>(b) * a.H + (hg * HPC + h2) * a.G + h) * a.splits + split) *
-                              kPartStride;
+      float* p = part_of((hg * HPC + h2) * a.G + h);
       p[4 + d] = o;
       if (d == 0) {
         p[0] = M;
@@ -1316,7 +1440,8 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs 
   const int b = blockIdx.x, kv = blockIdx.y, tid = threadIdx.x;
   const int h = tid / kDim, d = tid % kDim;       // thread (h, d)
   const int warp = tid >> 5, lane = tid & 31;
-  const int S = a.splits, G = a.G;
+  int S = a.splits;
+  const int G = a.G;
   const uint32_t bar = smem_u32(&sm.bar);
   // Let the next kernel in the stream launch now: the kernels of this library
   // read nothing this one writes before their own griddepcontrol.wait, so the
@@ -1335,16 +1460,28 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs 
   float owin = 0.0f;
   if constexpr (kWindow) owin = window_partial(a, ws, b, kv);
   griddep_wait();       // the partials come from the decode kernel
+  // balanced schedule: sequence b's splits are partial slots sched_base[b] ...
+  // (all heads of a slot side by side); otherwise b's splits of a head are adjacent
+  int pbase = 0;
+  if (a.balanced) {
+    S = a.sched_nsplit[b];
+    pbase = a.sched_base[b];
+  }
+  const int pstride = a.balanced ? a.H * kPartStride : kPartStride;   // floats between splits
+  auto head_parts = [&](int head) -> const float* {
+    return a.balanced ? a.part + (static_cast<size_t>(pbase) * a.H + head) * kPartStride
+                      : a.part + (static_cast<size_t>(b) * a.H + head) * a.splits * kPartStride;
+  };
   // Thread (h, d) loads element d of its head's first kPre split partials now,
   // so that these loads and the (m, l) loads below share one round trip.
   constexpr int kPre = 48;
-  const float* parts_h = a.part + (static_cast<size_t>(b) * a.H + kv * G + h) * S * kPartStride;
+  const float* parts_h = head_parts(kv * G + h);
   float v[kPre];
 #pragma unroll
-  for (int u = 0; u < kPre; ++u) v[u] = (h < G && u < S) ? parts_h[u * kPartStride + 4 + d] : 0.0f;
+  for (int u = 0; u < kPre; ++u) v[u] = (h < G && u < S) ? parts_h[u * pstride + 4 + d] : 0.0f;
   if (kWindow) __syncthreads();   // ws.M / ws.L
   if (warp < G) {
-    const float* parts = a.part + (static_cast<size_t>(b) * a.H + kv * G + warp) * S * kPartStride;
+    const float* parts = head_parts(kv * G + warp);
     // INT2 logits were taken against centred keys: with a window, add q.mu back
     const float qmu =
         kWindow ? a.qmeta[(static_cast<size_t>(b) * a.Hkv + kv) * kQMeta + 8 + warp] : 0.0f;
@@ -1355,11 +1492,11 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs 
 #pragma unroll
     for (int k = 0; k < kML; ++k) {
       const int j = lane + 32 * k;
-      mk[k] = j < S ? parts[j * kPartStride] : -INFINITY;
-      lk[k] = j < S ? parts[j * kPartStride + 1] : 0.0f;
+      mk[k] = j < S ? parts[j * pstride] : -INFINITY;
+      lk[k] = j < S ? parts[j * pstride + 1] : 0.0f;
     }
     float M = fmaxf(mk[0], mk[1]);
-    for (int j = lane + 32 * kML; j < S; j += 32) M = fmaxf(M, parts[j * kPartStride]);
+    for (int j = lane + 32 * kML; j < S; j += 32) M = fmaxf(M, parts[j * pstride]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     if (kWindow) M = fmaxf(M + qmu, ws.M[warp]);
@@ -1374,8 +1511,8 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs 
       }
     }
     for (int j = lane + 32 * kML; j < S; j += 32) {
-      const float mj = parts[j * kPartStride];
-      const float lj = parts[j * kPartStride + 1];
+      const float mj = parts[j * pstride];
+      const float lj = parts[j * pstride + 1];
       const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj + qmu - M);
       sm.w[warp][j] = w;
       L = fmaf(w, lj, L);
@@ -1400,7 +1537,7 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs 
       if (u < S) o = fmaf(sm.w[h][u], v[u], o);
     for (int j0 = kPre; j0 < S; j0 += kPre) {
 #pragma unroll
-      for (int u = 0; u < kPre; ++u) v[u] = j0 + u < S ? parts_h[(j0 + u) * kPartStride + 4 + d] : 0.0f;
+      for (int u = 0; u < kPre; ++u) v[u] = j0 + u < S ? parts_h[(j0 + u) * pstride + 4 + d] : 0.0f;
 #pragma unroll
       for (int u = 0; u < kPre; ++u)
         if (j0 + u < S) o = fmaf(sm.w[h][j0 + u], v[u], o);
@@ -1468,7 +1605,8 @@ __global__ void __launch_bounds__(kCombineThreads, kHeadCombineCtasPerSm)
   const int b = blockIdx.x, kv = blockIdx.y, h = blockIdx.z, tid = threadIdx.x;
   const int qq = tid / kDim, d = tid % kDim;
   const int warp = tid >> 5, lane = tid & 31;
-  const int S = a.splits, G = a.G;
+  int S = a.splits;
+  const int G = a.G;
   const uint32_t bar = smem_u32(&sm.bar);
   griddep_launch_dependents();      // as in combine_kernel
   const bool stage = a.rotate_out != 0;
@@ -1479,13 +1617,25 @@ __global__ void __launch_bounds__(kCombineThreads, kHeadCombineCtasPerSm)
     bulk_g2s(smem_u32(sm.Rt), a.RVt + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
   }
   griddep_wait();       // the partials come from the decode kernel
-  const float* parts = a.part + (static_cast<size_t>(b) * a.H + kv * G + h) * S * kPartStride;
+  // balanced schedule: sequence b's splits are partial slots sched_base[b] ...
+  // (all heads of a slot side by side); otherwise b's splits of a head are adjacent
+  int pbase = 0;
+  if (a.balanced) {
+    S = a.sched_nsplit[b];
+    pbase = a.sched_base[b];
+  }
+  const int pstride = a.balanced ? a.H * kPartStride : kPartStride;   // floats between splits
+  auto head_parts = [&](int head) -> const float* {
+    return a.balanced ? a.part + (static_cast<size_t>(pbase) * a.H + head) * kPartStride
+                      : a.part + (static_cast<size_t>(b) * a.H + head) * a.splits * kPartStride;
+  };
+  const float* parts = head_parts(kv * G + h);
   constexpr int kPreQ = 16;         // splits qq + 4u, u < kPreQ, loaded in the first round trip
   float v[kPreQ];
 #pragma unroll
   for (int u = 0; u < kPreQ; ++u) {
     const int s = qq + 4 * u;
-    v[u] = s < S ? parts[s * kPartStride + 4 + d] : 0.0f;
+    v[u] = s < S ? parts[s * pstride + 4 + d] : 0.0f;
   }
   if (warp == 0) {
     constexpr int kML = 2;
@@ -1493,11 +1643,11 @@ __global__ void __launch_bounds__(kCombineThreads, kHeadCombineCtasPerSm)
 #pragma unroll
     for (int k = 0; k < kML; ++k) {
       const int j = lane + 32 * k;
-      mk[k] = j < S ? parts[j * kPartStride] : -INFINITY;
-      lk[k] = j < S ? parts[j * kPartStride + 1] : 0.0f;
+      mk[k] = j < S ? parts[j * pstride] : -INFINITY;
+      lk[k] = j < S ? parts[j * pstride + 1] : 0.0f;
     }
     float M = fmaxf(mk[0], mk[1]);
-    for (int j = lane + 32 * kML; j < S; j += 32) M = fmaxf(M, parts[j * kPartStride]);
+    for (int j = lane + 32 * kML; j < S; j += 32) M = fmaxf(M, parts[j * pstride]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.0f;
@@ -1511,8 +1661,8 @@ __global__ void __launch_bounds__(kCombineThreads, kHeadCombineCtasPerSm)
       }
     }
     for (int j = lane + 32 * kML; j < S; j += 32) {
-      const float mj = parts[j * kPartStride];
-      const float lj = parts[j * kPartStride + 1];
+      const float mj = parts[j * pstride];
+      const float lj = parts[j * pstride + 1];
       const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj - M);
       sm.w[j] = w;
       L = fmaf(w, lj, L);
@@ -1530,7 +1680,7 @@ __global__ void __launch_bounds__(kCombineThreads, kHeadCombineCtasPerSm)
 #pragma unroll
     for (int u = 0; u < kPreQ; ++u) {
       const int s = s0 + qq + 4 * u;
-      v[u] = s < S ? parts[s * kPartStride + 4 + d] : 0.0f;
+      v[u] = s < S ? parts[s * pstride + 4 + d] : 0.0f;
     }
 #pragma unroll
     for (int u = 0; u < kPreQ; ++u)
@@ -1619,9 +1769,13 @@ __global__ void transpose_kernel(const float* __restrict__ in, float* __restrict
     dst[(bx + k) * kDim + by + threadIdx.x] = tile[threadIdx.x][k];
 }
 
-template <typename Smem, typename Kern>
-cudaError_t set_smem_attr(Kern kern) {
+// Dynamic shared-memory size and carve-out of kernel kKern, set once per
+// device (one flag set per kernel: each instantiation of this template is
+// its own kernel).
+template <typename Smem, auto kKern>
+cudaError_t set_smem_attr() {
   static bool done[64] = {};
+  const auto kern = kKern;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
@@ -1657,32 +1811,40 @@ cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_
 
 cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, const float* mu, float sm_scale,
                          cudaStream_t st) {
-  cudaError_t e = set_smem_attr<QprepSmem>(qprep_kernel);
+  cudaError_t e = set_smem_attr<QprepSmem, qprep_kernel>();
   if (e != cudaSuccess) return e;
-  dim3 grid(a.batch, a.Hkv);
+  dim3 grid(a.batch + (a.balanced ? 1 : 0), a.Hkv);
   e = launch_dependent(qprep_kernel, grid, dim3(128), sizeof(QprepSmem), st, a, RK, mu,
                        sm_scale * kLog2e);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_step_prep(const DecodeArgs& a, const StepArgs& sa, cudaStream_t st) {
-  cudaError_t e = set_smem_attr<StepPrepSmem>(step_prep_kernel);
+  cudaError_t e = set_smem_attr<StepPrepSmem, step_prep_kernel>();
   if (e != cudaSuccess) return e;
-  e = launch_dependent(step_prep_kernel, dim3(a.batch, a.Hkv, 2), dim3(128), sizeof(StepPrepSmem),
-                       st, a, sa);
+  e = launch_dependent(step_prep_kernel, dim3(a.batch + (a.balanced ? 1 : 0), a.Hkv, 2), dim3(128),
+                       sizeof(StepPrepSmem), st, a, sa);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t st) {
-  cudaError_t e = set_smem_attr<Int2Smem>(decode_int2_kernel);
-  if (e != cudaSuccess) return e;
-  dim3 grid(a.splits, a.Hkv / a.hpc, a.batch);
-  e = launch_dependent(decode_int2_kernel, grid, dim3(kW * 32), sizeof(Int2Smem), st, a);
+  cudaError_t e;
+  if (a.balanced) {
+    e = set_smem_attr<Int2Smem, decode_int2_kernel<true>>();
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(decode_int2_kernel<true>, dim3(a.batch * a.splits, a.Hkv / a.hpc, 1),
+                         dim3(kW * 32), sizeof(Int2Smem), st, a);
+  } else {
+    e = set_smem_attr<Int2Smem, decode_int2_kernel<false>>();
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(decode_int2_kernel<false>, dim3(a.splits, a.Hkv / a.hpc, a.batch),
+                         dim3(kW * 32), sizeof(Int2Smem), st, a);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t st) {
-  cudaError_t e = set_smem_attr<Bf16Smem>(decode_bf16_kernel);
+  cudaError_t e = set_smem_attr<Bf16Smem, decode_bf16_kernel>();
   if (e != cudaSuccess) return e;
   dim3 grid(a.splits, a.Hkv, a.batch);
   e = launch_dependent(decode_bf16_kernel, grid, dim3(kDecodeThreads), sizeof(Bf16Smem), st, a);
@@ -1692,17 +1854,17 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t st) {
 cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st) {
   cudaError_t e;
   if (a.window) {
-    e = set_smem_attr<CombineWindowSmem>(combine_kernel<true>);
+    e = set_smem_attr<CombineWindowSmem, combine_kernel<true>>();
     if (e != cudaSuccess) return e;
     e = launch_dependent(combine_kernel<true>, dim3(a.batch, a.Hkv), dim3(kCombineThreads),
                          sizeof(CombineWindowSmem), st, a);
   } else if (a.combine_per_head) {
-    e = set_smem_attr<HeadCombineSmem>(combine_head_kernel);
+    e = set_smem_attr<HeadCombineSmem, combine_head_kernel>();
     if (e != cudaSuccess) return e;
     e = launch_dependent(combine_head_kernel, dim3(a.batch, a.Hkv, a.G), dim3(kCombineThreads),
                          sizeof(HeadCombineSmem), st, a);
   } else {
-    e = set_smem_attr<CombineSmem>(combine_kernel<false>);
+    e = set_smem_attr<CombineSmem, combine_kernel<false>>();
     if (e != cudaSuccess) return e;
     e = launch_dependent(combine_kernel<false>, dim3(a.batch, a.Hkv), dim3(kCombineThreads),
                          sizeof(CombineSmem), st, a);
@@ -1728,16 +1890,16 @@ cudaError_t launch_transpose(const float* in, float* out, int count, cudaStream_
 int combine_head_ctas_per_sm() { return kHeadCombineCtasPerSm; }
 
 int decode_int2_ctas_per_sm() {
-  if (set_smem_attr<Int2Smem>(decode_int2_kernel) != cudaSuccess) return 1;
+  if (set_smem_attr<Int2Smem, decode_int2_kernel<false>>() != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel, kW * 32,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<false>, kW * 32,
                                                     sizeof(Int2Smem)) != cudaSuccess || n < 1)
     return 1;
   return n;
 }
 
 int decode_bf16_ctas_per_sm() {
-  if (set_smem_attr<Bf16Smem>(decode_bf16_kernel) != cudaSuccess) return 1;
+  if (set_smem_attr<Bf16Smem, decode_bf16_kernel>() != cudaSuccess) return 1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_bf16_kernel, kDecodeThreads,
                                                     sizeof(Bf16Smem)) != cudaSuccess || n < 1)

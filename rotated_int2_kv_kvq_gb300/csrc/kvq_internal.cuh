@@ -27,7 +27,7 @@ constexpr int kDecodeThreads = kDecodeWarps * 32;
 
 // Workspace layout of one decode call (offsets in bytes, each 256-aligned).
 struct DecodeWs {
-  size_t qfrag_off, qmeta_off, part_off, total;
+  size_t qfrag_off, qmeta_off, part_off, sched_off, total;
 };
 DecodeWs decode_ws_layout(int batch, int Hkv, int H, int splits, bool int2);
 
@@ -50,6 +50,17 @@ struct DecodeArgs {
   const float* RV;           // [Hkv][D][D] value rotations
   int rotate_out;            // 1: out = o_rot R_V^T, 0: out = o_rot
   int combine_per_head = 0;  // 1: the combine takes one CTA per query head (no window)
+  // Length-balanced schedule (balanced = 1): the decode grid's batch * splits
+  // CTAs are shared out over the sequences in chunks of one common size, in
+  // proportion to their page counts.  sched_map[c] = {b, chunk index, first
+  // partial slot of b, chunk pages} of CTA c (b = -1: no chunk); sequence b's
+  // partials sit in slots sched_base[b] .. sched_base[b] + sched_nsplit[b] - 1,
+  // partial (slot, head) at part[(slot * H + head) * kPartStride].  The table
+  // is written by an extra CTA of the query-preparation kernel.
+  int balanced = 0;
+  int4* sched_map = nullptr;   // [batch * splits]
+  int* sched_nsplit = nullptr; // [batch]
+  int* sched_base = nullptr;   // [batch]
   uint32_t* status;
   float log2_scale;          // sm_scale * log2(e)
   // BF16 window (sink + recent tokens); window = 0 for a plain decode

@@ -171,6 +171,31 @@ def test_kv_head_counts_sharing_a_cta(Hkv, splits):
     assert c.status() == 0
 
 
+@pytest.mark.parametrize("Hkv,splits", [(8, 128), (2, 200)])
+def test_balanced_schedule(Hkv, splits):
+    """Several sequences whose batch x splits CTAs exceed one wave take the
+    length-balanced schedule: one chunk size for the batch, chunks per
+    sequence in proportion to its length, partials in per-sequence slots.
+    Lengths include an empty sequence, a one-page one and page-boundary cases;
+    with Hkv = 2 two KV heads share a CTA (four warps per head, merged through
+    shared memory)."""
+    wl = W.WORKLOADS["qwen3_8b_32k"]
+    lens = [3001, 0, 17, 1200, 2999, 16, 600]
+    B = len(lens)
+    pt, _ = W.page_table(wl)
+    pt = pt[:B].copy()
+    c = Cache(wl, page_table=pt, num_pool_pages=int(pt.max()) + 1, num_heads=4 * Hkv,
+              num_kv_heads=Hkv)
+    c.append_range([b for b in range(B) if lens[b] > 0], 0, [L for L in lens if L > 0])
+    q = W.queries(wl, 0, 70 + Hkv, batch=B)[:, :4 * Hkv].copy()
+    got = c.decode(q, lens, splits)
+    pairs = [[b, h] for b in range(B) for h in range(4 * Hkv)]
+    want = c.oracle_decode(c.pool_host(), q, lens, pairs)
+    assert np.all(got[1] == 0.0), "an empty sequence decodes to zeros"
+    assert_close_attention(got.reshape(-1, 128), want, f"balanced Hkv={Hkv} splits={splits}")
+    assert c.status() == 0
+
+
 @pytest.mark.parametrize("Hkv", [8, 2])
 def test_single_split_long_context(Hkv):
     """One split over 21,000 tokens: 1,313 pages, more than the 1,024 page ids
