@@ -239,7 +239,8 @@ __device__ __forceinline__ void qprep_cta(const DecodeArgs& a, const float* __re
 // Length-balanced decode schedule (a.balanced), written by one extra CTA of
 // the query-preparation kernel (128 threads) after its dependency wait: the
 // smallest chunk size P (pages) such that the batch's chunks, ceil(n_b / P) for
-// a sequence of n_b pages, number at most batch * splits (the decode grid) and
+// a sequence of n_b pages, number at most a.sched_ctas (whole waves of the
+// decode grid's batch * splits CTAs) and
 // at most kMaxSplits per sequence, and at least 8 pages unless no sequence is
 // that long; then each sequence's chunk count, the first partial slot of each
 // sequence (prefix sum) and the CTA -> (sequence, chunk) map.  A sequence with
@@ -260,7 +261,8 @@ __device__ void schedule_cta(const DecodeArgs& a) {
   __shared__ int red[4];
   __shared__ int scan[128];
   const int tid = threadIdx.x, B = a.batch;
-  const int C = a.batch * a.splits;            // decode CTAs along x
+  const int C = a.batch * a.splits;            // decode CTAs along x (map entries)
+  const int Cuse = min(C, a.sched_ctas);        // chunks used: whole waves of CTAs
   griddep_wait();                              // seq_lens may come from a predecessor
   // pages of each sequence, kept in sched_nsplit until the chunk size is known
   int nmax = 0;
@@ -285,7 +287,7 @@ __device__ void schedule_cta(const DecodeArgs& a) {
     int cnt = 0;
     for (int b = tid; b < B; b += 128) cnt += (a.sched_nsplit[b] + P - 1) / P;
     cnt = block_sum128(cnt, red);
-    if (cnt <= C && (nmax + P - 1) / P <= kMaxSplits) hi = P;
+    if (cnt <= Cuse && (nmax + P - 1) / P <= kMaxSplits) hi = P;
     else lo = P + 1;
   }
   const int P = max(lo, min(8, max(nmax, 1)));

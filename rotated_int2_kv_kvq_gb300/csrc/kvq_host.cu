@@ -232,10 +232,11 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
     a.sched_nsplit = reinterpret_cast<int*>(ws + w.sched_off + static_cast<size_t>(batch) * splits * 16);
     a.sched_base = a.sched_nsplit + batch;
     const long slots = static_cast<long>(h->num_sms) * h->ctas_int2;
-    a.balanced = (!win.on && batch >= 2 &&
-                  static_cast<long>(batch) * splits * (a.Hkv / a.hpc) > slots)
-                     ? 1
-                     : 0;
+    const long ctas = static_cast<long>(batch) * splits * (a.Hkv / a.hpc);
+    a.balanced = (!win.on && batch >= 2 && ctas > slots) ? 1 : 0;
+    // whole waves only: chunks of one size that spill a few CTAs into a last,
+    // partial wave would double the makespan
+    a.sched_ctas = a.balanced ? static_cast<int>((ctas / slots) * slots / (a.Hkv / a.hpc)) : 0;
   }
   a.combine_per_head =
       (int2 && !win.on &&

@@ -58,6 +58,7 @@ struct DecodeArgs {
   // partial (slot, head) at part[(slot * H + head) * kPartStride].  The table
   // is written by an extra CTA of the query-preparation kernel.
   int balanced = 0;
+  int sched_ctas = 0;          // chunks the balanced schedule may use: whole waves of CTAs
   int4* sched_map = nullptr;   // [batch * splits]
   int* sched_nsplit = nullptr; // [batch]
   int* sched_base = nullptr;   // [batch]
