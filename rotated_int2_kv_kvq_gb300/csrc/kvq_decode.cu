@@ -97,10 +97,11 @@ __host__ __device__ constexpr int code_bit(int P) { return P < 2 ? 2 * P + 6 : (
 // issued before the kernel waits for its predecessor; q, which a preceding
 // kernel may still be writing, is read only after that wait.
 // ---------------------------------------------------------------------------
+template <int NB>
 struct QprepSmem {
   float R[kDim * kDim];
-  float qs[kMaxG][kDim];
-  float qr[kMaxG][kDim];
+  float qs[NB][kMaxG][kDim];
+  float qr[NB][kMaxG][kDim];
   int e[kMaxG];
   uint64_t bar;
 };
@@ -174,12 +175,15 @@ __device__ __forceinline__ void qprep_tail(const DecodeArgs& a, float (&qs)[kMax
   }
 }
 
-// One CTA per (sequence, KV head); thread i computes element i of the G
-// rotated query vectors, one fmaf chain over j = 0..127 each, with the query
-// elements read four j at a time (one broadcast load per vector).
+// One CTA per (group of NB sequences, KV head): R_K is staged once; thread i
+// computes element i of the G rotated query vectors of each sequence, one fmaf
+// chain over j = 0..127 each (the chains of the group's sequences side by
+// side), with the query elements read four j at a time (one broadcast load per
+// vector).  Sequences b0 .. b0 + nb - 1 (nb <= NB) are prepared.
+template <int NB>
 __device__ __forceinline__ void qprep_cta(const DecodeArgs& a, const float* __restrict__ RK,
                                           const float* __restrict__ mu, float log2_scale,
-                                          QprepSmem& sm, int b, int kv) {
+                                          QprepSmem<NB>& sm, int b0, int nb, int kv) {
   const int i = threadIdx.x;
   const int G = a.G;
   const bool rotate = RK != nullptr;
@@ -193,14 +197,16 @@ __device__ __forceinline__ void qprep_cta(const DecodeArgs& a, const float* __re
   __syncthreads();     // the barrier is initialised before any thread waits on it
   griddep_wait();      // q may come from the preceding kernel
 #pragma unroll
-  for (int h = 0; h < kMaxG; ++h) {
-    float x = 0.0f;
-    if (h < G) {
-      const uint16_t bits = a.q[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + i];
-      x = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+  for (int u = 0; u < NB; ++u)
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) {
+      float x = 0.0f;
+      if (h < G && u < nb) {
+        const uint16_t bits = a.q[(static_cast<size_t>(b0 + u) * a.H + kv * G + h) * kDim + i];
+        x = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+      }
+      sm.qs[u][h][i] = x;
     }
-    sm.qs[h][i] = x;
-  }
   if (rotate) {
     const bool ok = mbar_wait_bounded(bar, 0);
     if (__syncthreads_or(!ok)) {
@@ -210,29 +216,42 @@ __device__ __forceinline__ void qprep_cta(const DecodeArgs& a, const float* __re
       }
       return;
     }
-    float acc[kMaxG] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float acc[NB][kMaxG];
+#pragma unroll
+    for (int u = 0; u < NB; ++u)
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) acc[u][h] = 0.0f;
 #pragma unroll 2
     for (int j0 = 0; j0 < kDim; j0 += 4) {
       float r[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) r[u] = sm.R[(j0 + u) * kDim + i];
+      for (int k = 0; k < 4; ++k) r[k] = sm.R[(j0 + k) * kDim + i];
 #pragma unroll
-      for (int h = 0; h < kMaxG; ++h) {
-        const float4 x = *reinterpret_cast<const float4*>(&sm.qs[h][j0]);
-        acc[h] = fmaf(x.x, r[0], acc[h]);
-        acc[h] = fmaf(x.y, r[1], acc[h]);
-        acc[h] = fmaf(x.z, r[2], acc[h]);
-        acc[h] = fmaf(x.w, r[3], acc[h]);
-      }
+      for (int u = 0; u < NB; ++u)
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h) {
+          const float4 x = *reinterpret_cast<const float4*>(&sm.qs[u][h][j0]);
+          acc[u][h] = fmaf(x.x, r[0], acc[u][h]);
+          acc[u][h] = fmaf(x.y, r[1], acc[u][h]);
+          acc[u][h] = fmaf(x.z, r[2], acc[u][h]);
+          acc[u][h] = fmaf(x.w, r[3], acc[u][h]);
+        }
     }
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h) sm.qr[h][i] = acc[h];
+    for (int u = 0; u < NB; ++u)
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) sm.qr[u][h][i] = acc[u][h];
   } else {
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h) sm.qr[h][i] = sm.qs[h][i];
+    for (int u = 0; u < NB; ++u)
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) sm.qr[u][h][i] = sm.qs[u][h][i];
   }
   __syncthreads();
-  qprep_tail(a, sm.qs, sm.qr, sm.e, mu, log2_scale, b, kv);
+  for (int u = 0; u < nb; ++u) {
+    if (u > 0) __syncthreads();        // sm.e of the previous sequence has been read
+    qprep_tail(a, sm.qs[u], sm.qr[u], sm.e, mu, log2_scale, b0 + u, kv);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -330,16 +349,19 @@ __device__ void schedule_cta(const DecodeArgs& a) {
   for (int c = red[0] + tid; c < C; c += 128) a.sched_map[c] = make_int4(-1, 0, 0, 0);
 }
 
+template <int NB>
 __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* __restrict__ RK,
                                                     const float* __restrict__ mu,
                                                     float log2_scale) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   griddep_launch_dependents();
-  if (blockIdx.x == a.batch) {       // the extra column of a balanced decode
+  const int b0 = blockIdx.x * NB;
+  if (b0 >= a.batch) {               // the extra column of a balanced decode
     if (blockIdx.y == 0) schedule_cta(a);
     return;
   }
-  qprep_cta(a, RK, mu, log2_scale, *reinterpret_cast<QprepSmem*>(smem_raw), blockIdx.x, blockIdx.y);
+  qprep_cta<NB>(a, RK, mu, log2_scale, *reinterpret_cast<QprepSmem<NB>*>(smem_raw), b0,
+                min(NB, a.batch - b0), blockIdx.y);
 }
 
 // ---------------------------------------------------------------------------
@@ -353,34 +375,41 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
 // CTA waits for its predecessor; the token, q and the tables are read, and the
 // pool written, only after that wait.
 // ---------------------------------------------------------------------------
+template <int NB>
 struct StepSmem {
   float RK[kDim * kDim];
   float RV[kDim * kDim];
-  alignas(16) float x[2][kDim];   // centred key, value
-  float red[2][2][4];             // [K|V][max|min][warp]
-  uint8_t codes[2][kDim];
+  alignas(16) float x[NB][2][kDim];   // centred key, value of each sequence
+  float red[NB][2][2][4];             // [sequence][K|V][max|min][warp]
+  uint8_t codes[NB][2][kDim];
   uint64_t bar;
 };
 
+template <int NB>
 union StepPrepSmem {
-  StepSmem append;
-  QprepSmem query;
+  StepSmem<NB> append;
+  QprepSmem<NB> query;
 };
 
+// CTA (group of NB sequences, kv, role); role 0 appends the new tokens of the
+// group's sequences for KV head kv (R_K and R_V staged once), role 1 prepares
+// their queries.
+template <int NB>
 __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs st) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  const int b = blockIdx.x, kv = blockIdx.y, i = threadIdx.x;
+  const int b0 = blockIdx.x * NB, kv = blockIdx.y, i = threadIdx.x;
   griddep_launch_dependents();
-  if (b == a.batch) {                // the extra column of a balanced decode
+  if (b0 >= a.batch) {               // the extra column of a balanced decode
     if (kv == 0 && blockIdx.z == 0) schedule_cta(a);
     return;
   }
+  const int nb = min(NB, a.batch - b0);
   if (blockIdx.z == 1) {
-    qprep_cta(a, st.q_rotated ? nullptr : st.RK, st.mu, a.log2_scale,
-              reinterpret_cast<StepPrepSmem*>(smem_raw)->query, b, kv);
+    qprep_cta<NB>(a, st.q_rotated ? nullptr : st.RK, st.mu, a.log2_scale,
+                  reinterpret_cast<StepPrepSmem<NB>*>(smem_raw)->query, b0, nb, kv);
     return;
   }
-  StepSmem& sm = reinterpret_cast<StepPrepSmem*>(smem_raw)->append;
+  StepSmem<NB>& sm = reinterpret_cast<StepPrepSmem<NB>*>(smem_raw)->append;
   const int warp = i >> 5, lane = i & 31;
   const uint32_t bar = smem_u32(&sm.bar);
   if (i == 0) {
@@ -391,48 +420,61 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
     bulk_g2s(smem_u32(sm.RV), st.RV + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
   }
   __syncthreads();
-  griddep_wait();      // token and tables may come from preceding kernels
+  griddep_wait();      // tokens and tables may come from preceding kernels
 
-  // the token first, so that its loads overlap the table lookups below
-  const size_t src = (static_cast<size_t>(b) * a.Hkv + kv) * kDim + i;
-  const uint16_t kbits = st.K[src], vbits = st.V[src];
   const float mui = st.mu[static_cast<size_t>(kv) * kDim + i];
-  // the record slot of the new token, or none
-  const int seq_len = a.seq_lens[b];
-  const int p = seq_len - 1;
-  uint8_t* rec = nullptr;
-  if (seq_len > a.max_pages * kPage) {
-    if (i == 0 && kv == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
-  } else if (p >= 0) {
-    const int page = a.page_table[static_cast<size_t>(b) * a.max_pages + p / kPage];
-    if (page >= 0 && page < a.num_pool_pages)
-      rec = st.pool + (static_cast<size_t>(page) * a.Hkv + kv) * kInt2Rec;
-    else if (i == 0)
-      atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
-  }
-  sm.x[0][i] = __fsub_rn(__uint_as_float(static_cast<uint32_t>(kbits) << 16), mui);
-  sm.x[1][i] = __uint_as_float(static_cast<uint32_t>(vbits) << 16);
-  if (st.bf16_pool != nullptr && p >= 0 && seq_len <= a.max_pages * kPage) {
-    // the BF16 window cache's copy of the token (same placement as the BF16
-    // append kernel: fragment order of the BF16 page record)
-    const int page = st.bf16_page_table[static_cast<size_t>(b) * a.max_pages + p / kPage];
-    if (page >= 0 && page < st.bf16_num_pool_pages) {
-      uint8_t* base = st.bf16_pool + (static_cast<size_t>(page) * a.Hkv + kv) * kBf16Rec;
-      const int tau = p % kPage;
-      {
-        const int w = i >> 4, r = i & 15, h = r >> 3, t = (r >> 1) & 3, e = r & 1;
-        const int L = 4 * (tau & 7) + t, reg = (tau >> 3) + 2 * h;
-        *reinterpret_cast<uint16_t*>(base + 512 * w + 16 * L + 4 * reg + 2 * e) = kbits;
+  uint8_t* rec[NB];    // the record of each sequence's new token, or none
+  int pos[NB];         // its position
+#pragma unroll
+  for (int u = 0; u < NB; ++u) {
+    rec[u] = nullptr;
+    pos[u] = -1;
+    float xk = 0.0f, xv = 0.0f;
+    if (u < nb) {
+      const int b = b0 + u;
+      // the token first, so that its loads overlap the table lookups below
+      const size_t src = (static_cast<size_t>(b) * a.Hkv + kv) * kDim + i;
+      const uint16_t kbits = st.K[src], vbits = st.V[src];
+      const int seq_len = a.seq_lens[b];
+      const int p = seq_len - 1;
+      if (seq_len > a.max_pages * kPage) {
+        if (i == 0 && kv == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
+      } else if (p >= 0) {
+        const int page = a.page_table[static_cast<size_t>(b) * a.max_pages + p / kPage];
+        if (page >= 0 && page < a.num_pool_pages) {
+          rec[u] = st.pool + (static_cast<size_t>(page) * a.Hkv + kv) * kInt2Rec;
+          pos[u] = p;
+        } else if (i == 0) {
+          atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+        }
       }
-      {
-        const int m = i >> 4, r = i & 15, g = r & 7, dh = r >> 3;
-        const int t = (tau & 7) >> 1, e = tau & 1, th = tau >> 3;
-        const int L = 4 * g + t, reg = 2 * th + dh;
-        *reinterpret_cast<uint16_t*>(base + 4096 + 512 * m + 16 * L + 4 * reg + 2 * e) = vbits;
+      xk = __fsub_rn(__uint_as_float(static_cast<uint32_t>(kbits) << 16), mui);
+      xv = __uint_as_float(static_cast<uint32_t>(vbits) << 16);
+      if (st.bf16_pool != nullptr && p >= 0 && seq_len <= a.max_pages * kPage) {
+        // the BF16 window cache's copy of the token (same placement as the BF16
+        // append kernel: fragment order of the BF16 page record)
+        const int page = st.bf16_page_table[static_cast<size_t>(b) * a.max_pages + p / kPage];
+        if (page >= 0 && page < st.bf16_num_pool_pages) {
+          uint8_t* base = st.bf16_pool + (static_cast<size_t>(page) * a.Hkv + kv) * kBf16Rec;
+          const int tau = p % kPage;
+          {
+            const int w = i >> 4, r = i & 15, h = r >> 3, t = (r >> 1) & 3, e = r & 1;
+            const int L = 4 * (tau & 7) + t, reg = (tau >> 3) + 2 * h;
+            *reinterpret_cast<uint16_t*>(base + 512 * w + 16 * L + 4 * reg + 2 * e) = kbits;
+          }
+          {
+            const int m = i >> 4, r = i & 15, g = r & 7, dh = r >> 3;
+            const int t = (tau & 7) >> 1, e = tau & 1, th = tau >> 3;
+            const int L = 4 * g + t, reg = 2 * th + dh;
+            *reinterpret_cast<uint16_t*>(base + 4096 + 512 * m + 16 * L + 4 * reg + 2 * e) = vbits;
+          }
+        } else if (i == 0) {
+          atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+        }
       }
-    } else if (i == 0) {
-      atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
     }
+    sm.x[u][0][i] = xk;
+    sm.x[u][1][i] = xv;
   }
   const bool ok = mbar_wait_bounded(bar, 0);
   if (__syncthreads_or(!ok)) {
@@ -442,25 +484,38 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
     }
     return;
   }
-  // r_i = fmaf chains over j = 0..127, the vector elements read four j at a time
-  float rk = 0.0f, rv = 0.0f;
+  // r_i = fmaf chains over j = 0..127, the vector elements read four j at a
+  // time; the chains of the group's sequences side by side
+  float rk[NB], rv[NB];
+#pragma unroll
+  for (int u = 0; u < NB; ++u) rk[u] = rv[u] = 0.0f;
 #pragma unroll 2
   for (int j0 = 0; j0 < kDim; j0 += 4) {
-    const float4 xk = *reinterpret_cast<const float4*>(&sm.x[0][j0]);
-    const float4 xv = *reinterpret_cast<const float4*>(&sm.x[1][j0]);
-    rk = fmaf(xk.x, sm.RK[(j0 + 0) * kDim + i], rk);
-    rv = fmaf(xv.x, sm.RV[(j0 + 0) * kDim + i], rv);
-    rk = fmaf(xk.y, sm.RK[(j0 + 1) * kDim + i], rk);
-    rv = fmaf(xv.y, sm.RV[(j0 + 1) * kDim + i], rv);
-    rk = fmaf(xk.z, sm.RK[(j0 + 2) * kDim + i], rk);
-    rv = fmaf(xv.z, sm.RV[(j0 + 2) * kDim + i], rv);
-    rk = fmaf(xk.w, sm.RK[(j0 + 3) * kDim + i], rk);
-    rv = fmaf(xv.w, sm.RV[(j0 + 3) * kDim + i], rv);
+    float k4[4], v4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      k4[k] = sm.RK[(j0 + k) * kDim + i];
+      v4[k] = sm.RV[(j0 + k) * kDim + i];
+    }
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const float4 xk = *reinterpret_cast<const float4*>(&sm.x[u][0][j0]);
+      const float4 xv = *reinterpret_cast<const float4*>(&sm.x[u][1][j0]);
+      rk[u] = fmaf(xk.x, k4[0], rk[u]);
+      rv[u] = fmaf(xv.x, v4[0], rv[u]);
+      rk[u] = fmaf(xk.y, k4[1], rk[u]);
+      rv[u] = fmaf(xv.y, v4[1], rv[u]);
+      rk[u] = fmaf(xk.z, k4[2], rk[u]);
+      rv[u] = fmaf(xv.z, v4[2], rv[u]);
+      rk[u] = fmaf(xk.w, k4[3], rk[u]);
+      rv[u] = fmaf(xv.w, v4[3], rv[u]);
+    }
   }
 
-  // max / min of the rotated key and value over the whole vector
-  {
-    float mk = rk, nk = rk, mv = rv, nv = rv;
+  // max / min of each rotated key and value over the whole vector
+#pragma unroll
+  for (int u = 0; u < NB; ++u) {
+    float mk = rk[u], nk = rk[u], mv = rv[u], nv = rv[u];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
@@ -469,40 +524,45 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
       nv = fminf(nv, __shfl_xor_sync(0xffffffffu, nv, off));
     }
     if (lane == 0) {
-      sm.red[0][0][warp] = mk;
-      sm.red[0][1][warp] = nk;
-      sm.red[1][0][warp] = mv;
-      sm.red[1][1][warp] = nv;
+      sm.red[u][0][0][warp] = mk;
+      sm.red[u][0][1][warp] = nk;
+      sm.red[u][1][0][warp] = mv;
+      sm.red[u][1][1][warp] = nv;
     }
   }
   __syncthreads();
-  uint32_t szw[2];
+  uint32_t szw[NB][2];
 #pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    const float mx = fmaxf(fmaxf(sm.red[which][0][0], sm.red[which][0][1]),
-                           fmaxf(sm.red[which][0][2], sm.red[which][0][3]));
-    const float mn = fminf(fminf(sm.red[which][1][0], sm.red[which][1][1]),
-                           fminf(sm.red[which][1][2], sm.red[which][1][3]));
-    const float clip = which ? st.clip_v : st.clip_k;
-    const float mxc = __fmul_rn(clip, mx);
-    const float mnc = __fmul_rn(clip, mn);
-    const float s32 = __fdiv_rn(__fsub_rn(mxc, mnc), 3.0f);
-    const __half sh = __float2half_rn(s32);
-    const __half zh = __float2half_rn(mnc);
-    const float sc = __half2float(sh), z = __half2float(zh);
-    uint32_t code = 0;
-    if (sc != 0.0f) {
-      const float t = __fdiv_rn(__fsub_rn(which ? rv : rk, z), sc);
-      code = static_cast<uint32_t>(fminf(fmaxf(rintf(t), 0.0f), 3.0f));
+  for (int u = 0; u < NB; ++u)
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const float mx = fmaxf(fmaxf(sm.red[u][which][0][0], sm.red[u][which][0][1]),
+                             fmaxf(sm.red[u][which][0][2], sm.red[u][which][0][3]));
+      const float mn = fminf(fminf(sm.red[u][which][1][0], sm.red[u][which][1][1]),
+                             fminf(sm.red[u][which][1][2], sm.red[u][which][1][3]));
+      const float clip = which ? st.clip_v : st.clip_k;
+      const float mxc = __fmul_rn(clip, mx);
+      const float mnc = __fmul_rn(clip, mn);
+      const float s32 = __fdiv_rn(__fsub_rn(mxc, mnc), 3.0f);
+      const __half sh = __float2half_rn(s32);
+      const __half zh = __float2half_rn(mnc);
+      const float sc = __half2float(sh), z = __half2float(zh);
+      uint32_t code = 0;
+      if (sc != 0.0f) {
+        const float t = __fdiv_rn(__fsub_rn(which ? rv[u] : rk[u], z), sc);
+        code = static_cast<uint32_t>(fminf(fmaxf(rintf(t), 0.0f), 3.0f));
+      }
+      sm.codes[u][which][i] = static_cast<uint8_t>(code);
+      szw[u][which] = static_cast<uint32_t>(__half_as_ushort(sh)) |
+                      (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
     }
-    sm.codes[which][i] = static_cast<uint8_t>(code);
-    szw[which] = static_cast<uint32_t>(__half_as_ushort(sh)) |
-                 (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
-  }
   __syncthreads();
-  // scatter into the page record (layout in include/kvq.h)
-  if (rec != nullptr) {
-    const int tau = p % kPage;
+  // scatter into the page records (layout in include/kvq.h)
+#pragma unroll
+  for (int u = 0; u < NB; ++u) {
+    if (rec[u] == nullptr) continue;
+    uint8_t* const r = rec[u];
+    const int tau = pos[u] % kPage;
     if (i < 8) {
       // keys: word h of lane group t of row tau & 7
       const int t = i & 3, h = i >> 2;
@@ -510,23 +570,23 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         const int d = 16 * w + 2 * t + 8 * h;
-        wv |= static_cast<uint32_t>(sm.codes[0][d]) << (2 * w);
-        wv |= static_cast<uint32_t>(sm.codes[0][d + 1]) << (16 + 2 * w);
+        wv |= static_cast<uint32_t>(sm.codes[u][0][d]) << (2 * w);
+        wv |= static_cast<uint32_t>(sm.codes[u][0][d + 1]) << (16 + 2 * w);
       }
-      *reinterpret_cast<uint32_t*>(rec + 16 * (4 * (tau & 7) + t) + 8 * (tau >> 3) + 4 * h) = wv;
+      *reinterpret_cast<uint32_t*>(r + 16 * (4 * (tau & 7) + t) + 8 * (tau >> 3) + 4 * h) = wv;
     } else if (i < 24) {
       // values: the token's 16-bit half of word (2 th + dh) of lane 4 g + t
       const int k = i - 8, g = k >> 1, dh = k & 1;
       uint32_t hv = 0;
 #pragma unroll
-      for (int m = 0; m < 8; ++m) hv |= static_cast<uint32_t>(sm.codes[1][16 * m + g + 8 * dh]) << (2 * m);
+      for (int m = 0; m < 8; ++m) hv |= static_cast<uint32_t>(sm.codes[u][1][16 * m + g + 8 * dh]) << (2 * m);
       const int t = (tau & 7) >> 1, e = tau & 1, th = tau >> 3;
-      *reinterpret_cast<uint16_t*>(rec + 512 + 16 * (4 * g + t) + 4 * (2 * th + dh) + 2 * e) =
+      *reinterpret_cast<uint16_t*>(r + 512 + 16 * (4 * g + t) + 4 * (2 * th + dh) + 2 * e) =
           static_cast<uint16_t>(hv);
     } else if (i < 26) {
       const int which = i - 24;
-      *reinterpret_cast<uint32_t*>(rec + 1024 + 16 * (tau & 7) + 8 * which + 4 * (tau >> 3)) =
-          which ? szw[1] : szw[0];
+      *reinterpret_cast<uint32_t*>(r + 1024 + 16 * (tau & 7) + 8 * which + 4 * (tau >> 3)) =
+          which ? szw[u][1] : szw[u][0];
     }
   }
 }
@@ -1811,22 +1871,38 @@ cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_
 
 }  // namespace
 
-cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, const float* mu, float sm_scale,
-                         cudaStream_t st) {
-  cudaError_t e = set_smem_attr<QprepSmem, qprep_kernel>();
+template <int NB>
+cudaError_t launch_qprep_nb(const DecodeArgs& a, const float* RK, const float* mu, float sm_scale,
+                            cudaStream_t st) {
+  cudaError_t e = set_smem_attr<QprepSmem<NB>, qprep_kernel<NB>>();
   if (e != cudaSuccess) return e;
-  dim3 grid(a.batch + (a.balanced ? 1 : 0), a.Hkv);
-  e = launch_dependent(qprep_kernel, grid, dim3(128), sizeof(QprepSmem), st, a, RK, mu,
+  dim3 grid((a.batch + NB - 1) / NB + (a.balanced ? 1 : 0), a.Hkv);
+  e = launch_dependent(qprep_kernel<NB>, grid, dim3(128), sizeof(QprepSmem<NB>), st, a, RK, mu,
                        sm_scale * kLog2e);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_step_prep(const DecodeArgs& a, const StepArgs& sa, cudaStream_t st) {
-  cudaError_t e = set_smem_attr<StepPrepSmem, step_prep_kernel>();
+cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, const float* mu, float sm_scale,
+                         cudaStream_t st) {
+  if (a.prep_nb >= 4) return launch_qprep_nb<4>(a, RK, mu, sm_scale, st);
+  if (a.prep_nb == 2) return launch_qprep_nb<2>(a, RK, mu, sm_scale, st);
+  return launch_qprep_nb<1>(a, RK, mu, sm_scale, st);
+}
+
+template <int NB>
+cudaError_t launch_step_prep_nb(const DecodeArgs& a, const StepArgs& sa, cudaStream_t st) {
+  cudaError_t e = set_smem_attr<StepPrepSmem<NB>, step_prep_kernel<NB>>();
   if (e != cudaSuccess) return e;
-  e = launch_dependent(step_prep_kernel, dim3(a.batch + (a.balanced ? 1 : 0), a.Hkv, 2), dim3(128),
-                       sizeof(StepPrepSmem), st, a, sa);
+  e = launch_dependent(step_prep_kernel<NB>,
+                       dim3((a.batch + NB - 1) / NB + (a.balanced ? 1 : 0), a.Hkv, 2), dim3(128),
+                       sizeof(StepPrepSmem<NB>), st, a, sa);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_step_prep(const DecodeArgs& a, const StepArgs& sa, cudaStream_t st) {
+  if (a.prep_nb >= 4) return launch_step_prep_nb<4>(a, sa, st);
+  if (a.prep_nb == 2) return launch_step_prep_nb<2>(a, sa, st);
+  return launch_step_prep_nb<1>(a, sa, st);
 }
 
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t st) {

@@ -57,6 +57,7 @@ struct DecodeArgs {
   // partials sit in slots sched_base[b] .. sched_base[b] + sched_nsplit[b] - 1,
   // partial (slot, head) at part[(slot * H + head) * kPartStride].  The table
   // is written by an extra CTA of the query-preparation kernel.
+  int prep_nb = 1;            // sequences per query-preparation / step-preparation CTA (1, 2, 4)
   int balanced = 0;
   int sched_ctas = 0;          // chunks the balanced schedule may use: whole waves of CTAs
   int4* sched_map = nullptr;   // [batch * splits]

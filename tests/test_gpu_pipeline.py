@@ -76,6 +76,41 @@ def test_append_decode_equals_append_then_decode(name, splits):
     assert a.status() == 0 and b.status() == 0
 
 
+@pytest.mark.parametrize("B", [24, 48])
+def test_append_decode_large_batch(B):
+    """Batches whose per-sequence preparation CTAs would exceed one wave: the
+    query and step preparation take 2 (B = 24) or 4 (B = 48) sequences per
+    CTA; B = 48 also takes the length-balanced decode schedule.  Fused step
+    against append + decode (pools byte for byte, outputs bit for bit) and
+    against the float64 oracle."""
+    wl = W.WORKLOADS["ragged_64"]
+    pt, npool = W.page_table(wl)
+    pt = pt[:B].copy()
+    rng = np.random.default_rng(5 + B)
+    cap = (pt >= 0).sum(axis=1) * 16 - 2          # room for the two new tokens
+    lens = rng.integers(1, 2500, size=B)
+    lens[:6] = [0, 1, 15, 16, 17, 2047]
+    lens = np.minimum(lens, cap)
+    kw = dict(page_table=pt, num_pool_pages=int(pt.max()) + 1)
+    a, b = _pair(wl, lens, **kw)
+    for step in range(2):
+        Kn, Vn = _new_tokens(wl, lens, a.Hkv)
+        q = W.queries(wl, 0, 60 + step)[:B].copy()
+        lens_after = lens + 1
+        if step == 1:
+            lens_after[0] = 0          # sequence 0 takes no token this step
+        got = _fused(a, Kn, Vn, q, lens_after, 0)
+        want = _separate(b, Kn, Vn, q, lens_after, 0)
+        assert np.array_equal(a.pool_host(), b.pool_host()), f"pool differs at step {step}"
+        assert np.array_equal(got, want), f"output differs at step {step}"
+        lens = np.maximum(lens_after, lens)
+    pairs = [[int(x), int(y)] for x, y in zip(rng.integers(0, B, 12), rng.integers(0, wl.num_heads, 12))]
+    oracle_out = a.oracle_decode(a.pool_host(), q, lens_after, pairs)
+    assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], oracle_out,
+                           f"large batch B={B}")
+    assert a.status() == 0 and b.status() == 0
+
+
 def test_append_decode_rotated_query_and_gqa():
     wl = W.WORKLOADS["tiny_1k"]
     for G, q_rot in ((1, False), (2, False), (4, True)):
