@@ -1494,8 +1494,10 @@ __device__ float window_partial(const DecodeArgs& a, WindowSmem& ws, int b, int 
   return o;
 }
 
-template <bool kWindow>
-__global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs a) {
+// kLight: two CTAs per SM (at most 64 registers a thread, 16 partials
+// preloaded) for grids of more than one wave of one-per-SM CTAs.
+template <bool kWindow, bool kLight = false>
+__global__ void __launch_bounds__(kCombineThreads, kLight ? 2 : 1) combine_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   CombineSmem& sm = *reinterpret_cast<CombineSmem*>(smem_raw);
   WindowSmem& ws = *reinterpret_cast<WindowSmem*>(smem_raw + sizeof(CombineSmem));
@@ -1536,7 +1538,7 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs 
   };
   // Thread (h, d) loads element d of its head's first kPre split partials now,
   // so that these loads and the (m, l) loads below share one round trip.
-  constexpr int kPre = 48;
+  constexpr int kPre = kLight ? 16 : 48;
   const float* parts_h = head_parts(kv * G + h);
   float v[kPre];
 #pragma unroll
@@ -1941,6 +1943,11 @@ cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     e = launch_dependent(combine_head_kernel, dim3(a.batch, a.Hkv, a.G), dim3(kCombineThreads),
                          sizeof(HeadCombineSmem), st, a);
+  } else if (a.combine_light) {
+    e = set_smem_attr<CombineSmem, combine_kernel<false, true>>();
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(combine_kernel<false, true>, dim3(a.batch, a.Hkv), dim3(kCombineThreads),
+                         sizeof(CombineSmem), st, a);
   } else {
     e = set_smem_attr<CombineSmem, combine_kernel<false>>();
     if (e != cudaSuccess) return e;
