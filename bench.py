@@ -963,6 +963,32 @@ def measure_full_stack(K, torch, steps, warmup, local=0, dist=None, clocks_on=Tr
     return res, clk
 
 
+def run_workload(args):
+    """One of the other workloads alone (the sub-objects of the default line's
+    `configs`), on one GPU: `--splits` fixes the split count (default: the
+    automatic one; long_128k: 64, 128 and 256)."""
+    import torch
+
+    from rotated_int2_kv_kvq_gb300 import kvq as K
+
+    K.load_library()
+    wl = W.WORKLOADS[args.workload]
+    splits = [args.splits] if args.splits else ([64, 128, 256] if wl.name == "long_128k" else [0])
+    peak, peak_kind = measured_peaks()
+    r = measure_workload(K, torch, wl, splits, max(20, args.steps), max(3, args.warmup),
+                         l2_bytes(torch), peak, 0.0 if args.no_cpu else 3.0)
+    first = r["by_splits"][0] if "by_splits" in r else r
+    line = {
+        "metric": f"{wl.name}: INT2 decode step, cache GB/s", "value": first["cache_gbs"],
+        "unit": UNIT, "n_gpus": 1, "steps": max(20, args.steps), "warmup": max(3, args.warmup),
+        "ms_per_step": first["us_per_step"] * 1e-3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int2 codes, fp16 mma, fp32 accumulate",
+        "data": "synthetic", "config": {"workload": wl.name}, "peak_kind": peak_kind,
+        "result": r,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_full_stack(args):
     import torch
 
@@ -1094,6 +1120,8 @@ def main():
         run_full_stack(args)
     elif args.workload == "optr_calib":
         run_optr(args)
+    elif args.workload in ("tiny_1k", "long_128k", "ragged_64"):
+        run_workload(args)
     else:
         run_ours(args)
 
