@@ -276,21 +276,25 @@ __device__ __forceinline__ int block_sum128(int v, int* red) {
   return (red[0] + red[1]) + (red[2] + red[3]);
 }
 
-__device__ void schedule_cta(const DecodeArgs& a) {
+// nsm: the kernel's (otherwise unused) dynamic shared memory, nsm_len ints:
+// the page counts live there when the batch fits, else in sched_nsplit.
+__device__ void schedule_cta(const DecodeArgs& a, int* nsm, int nsm_len) {
   __shared__ int red[4];
   __shared__ int scan[128];
   const int tid = threadIdx.x, B = a.batch;
   const int C = a.batch * a.splits;            // decode CTAs along x (map entries)
   const int Cuse = min(C, a.sched_ctas);        // chunks used: whole waves of CTAs
   griddep_wait();                              // seq_lens may come from a predecessor
-  // pages of each sequence, kept in sched_nsplit until the chunk size is known
+  // pages of each sequence, kept in shared memory (or sched_nsplit) until the
+  // chunk size is known
+  int* const np = B <= nsm_len ? nsm : a.sched_nsplit;
   int nmax = 0;
   for (int b = tid; b < B; b += 128) {
     const int len = a.seq_lens[b];
     int n = 0;
     if (len < 0 || len > a.max_pages * kPage) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
     else n = (len + kPage - 1) / kPage;
-    a.sched_nsplit[b] = n;
+    np[b] = n;
     nmax = max(nmax, n);
   }
 #pragma unroll
@@ -304,7 +308,7 @@ __device__ void schedule_cta(const DecodeArgs& a) {
   while (lo < hi) {                            // uniform across the CTA
     const int P = (lo + hi) >> 1;
     int cnt = 0;
-    for (int b = tid; b < B; b += 128) cnt += (a.sched_nsplit[b] + P - 1) / P;
+    for (int b = tid; b < B; b += 128) cnt += (np[b] + P - 1) / P;
     cnt = block_sum128(cnt, red);
     if (cnt <= Cuse && (nmax + P - 1) / P <= kMaxSplits) hi = P;
     else lo = P + 1;
@@ -315,7 +319,7 @@ __device__ void schedule_cta(const DecodeArgs& a) {
   const int per = (B + 127) / 128;
   const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
   int local = 0;
-  for (int b = b0; b < b1; ++b) local += (a.sched_nsplit[b] + P - 1) / P;
+  for (int b = b0; b < b1; ++b) local += (np[b] + P - 1) / P;
   scan[tid] = local;
   __syncthreads();
   if (tid < 32) {                              // warp 0 scans the 128 partial sums
@@ -335,7 +339,7 @@ __device__ void schedule_cta(const DecodeArgs& a) {
   __syncthreads();
   int base = scan[tid];
   for (int b = b0; b < b1; ++b) {
-    const int ns = (a.sched_nsplit[b] + P - 1) / P;
+    const int ns = (np[b] + P - 1) / P;
     a.sched_nsplit[b] = ns;
     a.sched_base[b] = base;
     for (int k = 0; k < ns; ++k) a.sched_map[base + k] = make_int4(b, k, base, P);
@@ -357,7 +361,8 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
   griddep_launch_dependents();
   const int b0 = blockIdx.x * NB;
   if (b0 >= a.batch) {               // the extra column of a balanced decode
-    if (blockIdx.y == 0) schedule_cta(a);
+    if (blockIdx.y == 0)
+      schedule_cta(a, reinterpret_cast<int*>(smem_raw), static_cast<int>(sizeof(QprepSmem<NB>) / 4));
     return;
   }
   qprep_cta<NB>(a, RK, mu, log2_scale, *reinterpret_cast<QprepSmem<NB>*>(smem_raw), b0,
@@ -377,11 +382,10 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
 // ---------------------------------------------------------------------------
 template <int NB>
 struct StepSmem {
-  float RK[kDim * kDim];
-  float RV[kDim * kDim];
-  alignas(16) float x[NB][2][kDim];   // centred key, value of each sequence
-  float red[NB][2][2][4];             // [sequence][K|V][max|min][warp]
-  uint8_t codes[NB][2][kDim];
+  float R[kDim * kDim];              // R_K (key role) or R_V (value role)
+  alignas(16) float x[NB][kDim];     // the centred key or the value of each sequence
+  float red[NB][2][4];               // [sequence][max|min][warp]
+  uint8_t codes[NB][kDim];
   uint64_t bar;
 };
 
@@ -391,65 +395,68 @@ union StepPrepSmem {
   QprepSmem<NB> query;
 };
 
-// CTA (group of NB sequences, kv, role); role 0 appends the new tokens of the
-// group's sequences for KV head kv (R_K and R_V staged once), role 1 prepares
-// their queries.
+// CTA (group of NB sequences, kv, role): role 0 appends the new keys of the
+// group's sequences for KV head kv, role 1 their new values (each role stages
+// its one rotation matrix, so every CTA of the launch needs at most one
+// matrix of shared memory and two fit on an SM), role 2 prepares their queries.
 template <int NB>
 __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs st) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int b0 = blockIdx.x * NB, kv = blockIdx.y, i = threadIdx.x;
   griddep_launch_dependents();
   if (b0 >= a.batch) {               // the extra column of a balanced decode
-    if (kv == 0 && blockIdx.z == 0) schedule_cta(a);
+    if (kv == 0 && blockIdx.z == 0)
+      schedule_cta(a, reinterpret_cast<int*>(smem_raw), static_cast<int>(sizeof(StepPrepSmem<NB>) / 4));
     return;
   }
   const int nb = min(NB, a.batch - b0);
-  if (blockIdx.z == 1) {
+  if (blockIdx.z == 2) {
     qprep_cta<NB>(a, st.q_rotated ? nullptr : st.RK, st.mu, a.log2_scale,
                   reinterpret_cast<StepPrepSmem<NB>*>(smem_raw)->query, b0, nb, kv);
     return;
   }
+  const int which = blockIdx.z;      // 0 keys, 1 values
   StepSmem<NB>& sm = reinterpret_cast<StepPrepSmem<NB>*>(smem_raw)->append;
   const int warp = i >> 5, lane = i & 31;
   const uint32_t bar = smem_u32(&sm.bar);
   if (i == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar, 2 * kDim * kDim * 4);
-    bulk_g2s(smem_u32(sm.RK), st.RK + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
-    bulk_g2s(smem_u32(sm.RV), st.RV + static_cast<size_t>(kv) * kDim * kDim, kDim * kDim * 4, bar);
+    mbar_arrive_expect_tx(bar, kDim * kDim * 4);
+    bulk_g2s(smem_u32(sm.R), (which ? st.RV : st.RK) + static_cast<size_t>(kv) * kDim * kDim,
+             kDim * kDim * 4, bar);
   }
   __syncthreads();
   griddep_wait();      // tokens and tables may come from preceding kernels
 
-  const float mui = st.mu[static_cast<size_t>(kv) * kDim + i];
+  const float mui = which ? 0.0f : st.mu[static_cast<size_t>(kv) * kDim + i];
+  const uint16_t* X = which ? st.V : st.K;
   uint8_t* rec[NB];    // the record of each sequence's new token, or none
   int pos[NB];         // its position
 #pragma unroll
   for (int u = 0; u < NB; ++u) {
     rec[u] = nullptr;
     pos[u] = -1;
-    float xk = 0.0f, xv = 0.0f;
+    float x = 0.0f;
     if (u < nb) {
       const int b = b0 + u;
-      // the token first, so that its loads overlap the table lookups below
-      const size_t src = (static_cast<size_t>(b) * a.Hkv + kv) * kDim + i;
-      const uint16_t kbits = st.K[src], vbits = st.V[src];
+      // the token first, so that its load overlaps the table lookups below
+      const uint16_t bits = X[(static_cast<size_t>(b) * a.Hkv + kv) * kDim + i];
       const int seq_len = a.seq_lens[b];
       const int p = seq_len - 1;
       if (seq_len > a.max_pages * kPage) {
-        if (i == 0 && kv == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
+        if (i == 0 && kv == 0 && which == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
       } else if (p >= 0) {
         const int page = a.page_table[static_cast<size_t>(b) * a.max_pages + p / kPage];
         if (page >= 0 && page < a.num_pool_pages) {
           rec[u] = st.pool + (static_cast<size_t>(page) * a.Hkv + kv) * kInt2Rec;
           pos[u] = p;
-        } else if (i == 0) {
+        } else if (i == 0 && which == 0) {
           atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
         }
       }
-      xk = __fsub_rn(__uint_as_float(static_cast<uint32_t>(kbits) << 16), mui);
-      xv = __uint_as_float(static_cast<uint32_t>(vbits) << 16);
+      const float xf = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+      x = which ? xf : __fsub_rn(xf, mui);
       if (st.bf16_pool != nullptr && p >= 0 && seq_len <= a.max_pages * kPage) {
         // the BF16 window cache's copy of the token (same placement as the BF16
         // append kernel: fragment order of the BF16 page record)
@@ -457,24 +464,22 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
         if (page >= 0 && page < st.bf16_num_pool_pages) {
           uint8_t* base = st.bf16_pool + (static_cast<size_t>(page) * a.Hkv + kv) * kBf16Rec;
           const int tau = p % kPage;
-          {
+          if (which == 0) {
             const int w = i >> 4, r = i & 15, h = r >> 3, t = (r >> 1) & 3, e = r & 1;
             const int L = 4 * (tau & 7) + t, reg = (tau >> 3) + 2 * h;
-            *reinterpret_cast<uint16_t*>(base + 512 * w + 16 * L + 4 * reg + 2 * e) = kbits;
-          }
-          {
+            *reinterpret_cast<uint16_t*>(base + 512 * w + 16 * L + 4 * reg + 2 * e) = bits;
+          } else {
             const int m = i >> 4, r = i & 15, g = r & 7, dh = r >> 3;
             const int t = (tau & 7) >> 1, e = tau & 1, th = tau >> 3;
             const int L = 4 * g + t, reg = 2 * th + dh;
-            *reinterpret_cast<uint16_t*>(base + 4096 + 512 * m + 16 * L + 4 * reg + 2 * e) = vbits;
+            *reinterpret_cast<uint16_t*>(base + 4096 + 512 * m + 16 * L + 4 * reg + 2 * e) = bits;
           }
-        } else if (i == 0) {
+        } else if (i == 0 && which == 0) {
           atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
         }
       }
     }
-    sm.x[u][0][i] = xk;
-    sm.x[u][1][i] = xv;
+    sm.x[u][i] = x;
   }
   const bool ok = mbar_wait_bounded(bar, 0);
   if (__syncthreads_or(!ok)) {
@@ -484,109 +489,93 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
     }
     return;
   }
-  // r_i = fmaf chains over j = 0..127, the vector elements read four j at a
-  // time; the chains of the group's sequences side by side
-  float rk[NB], rv[NB];
+  // r_i = fmaf chain over j = 0..127 per sequence, the vector elements read
+  // four j at a time; the chains of the group's sequences side by side
+  float r[NB];
 #pragma unroll
-  for (int u = 0; u < NB; ++u) rk[u] = rv[u] = 0.0f;
+  for (int u = 0; u < NB; ++u) r[u] = 0.0f;
 #pragma unroll 2
   for (int j0 = 0; j0 < kDim; j0 += 4) {
-    float k4[4], v4[4];
+    float r4[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      k4[k] = sm.RK[(j0 + k) * kDim + i];
-      v4[k] = sm.RV[(j0 + k) * kDim + i];
-    }
+    for (int k = 0; k < 4; ++k) r4[k] = sm.R[(j0 + k) * kDim + i];
 #pragma unroll
     for (int u = 0; u < NB; ++u) {
-      const float4 xk = *reinterpret_cast<const float4*>(&sm.x[u][0][j0]);
-      const float4 xv = *reinterpret_cast<const float4*>(&sm.x[u][1][j0]);
-      rk[u] = fmaf(xk.x, k4[0], rk[u]);
-      rv[u] = fmaf(xv.x, v4[0], rv[u]);
-      rk[u] = fmaf(xk.y, k4[1], rk[u]);
-      rv[u] = fmaf(xv.y, v4[1], rv[u]);
-      rk[u] = fmaf(xk.z, k4[2], rk[u]);
-      rv[u] = fmaf(xv.z, v4[2], rv[u]);
-      rk[u] = fmaf(xk.w, k4[3], rk[u]);
-      rv[u] = fmaf(xv.w, v4[3], rv[u]);
+      const float4 x = *reinterpret_cast<const float4*>(&sm.x[u][j0]);
+      r[u] = fmaf(x.x, r4[0], r[u]);
+      r[u] = fmaf(x.y, r4[1], r[u]);
+      r[u] = fmaf(x.z, r4[2], r[u]);
+      r[u] = fmaf(x.w, r4[3], r[u]);
     }
   }
 
-  // max / min of each rotated key and value over the whole vector
+  // max / min of each rotated vector over its 128 elements
 #pragma unroll
   for (int u = 0; u < NB; ++u) {
-    float mk = rk[u], nk = rk[u], mv = rv[u], nv = rv[u];
+    float mx = r[u], mn = r[u];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
-      nk = fminf(nk, __shfl_xor_sync(0xffffffffu, nk, off));
-      mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
-      nv = fminf(nv, __shfl_xor_sync(0xffffffffu, nv, off));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
     }
     if (lane == 0) {
-      sm.red[u][0][0][warp] = mk;
-      sm.red[u][0][1][warp] = nk;
-      sm.red[u][1][0][warp] = mv;
-      sm.red[u][1][1][warp] = nv;
+      sm.red[u][0][warp] = mx;
+      sm.red[u][1][warp] = mn;
     }
   }
   __syncthreads();
-  uint32_t szw[NB][2];
+  uint32_t szw[NB];
+  const float clip = which ? st.clip_v : st.clip_k;
 #pragma unroll
-  for (int u = 0; u < NB; ++u)
-#pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const float mx = fmaxf(fmaxf(sm.red[u][which][0][0], sm.red[u][which][0][1]),
-                             fmaxf(sm.red[u][which][0][2], sm.red[u][which][0][3]));
-      const float mn = fminf(fminf(sm.red[u][which][1][0], sm.red[u][which][1][1]),
-                             fminf(sm.red[u][which][1][2], sm.red[u][which][1][3]));
-      const float clip = which ? st.clip_v : st.clip_k;
-      const float mxc = __fmul_rn(clip, mx);
-      const float mnc = __fmul_rn(clip, mn);
-      const float s32 = __fdiv_rn(__fsub_rn(mxc, mnc), 3.0f);
-      const __half sh = __float2half_rn(s32);
-      const __half zh = __float2half_rn(mnc);
-      const float sc = __half2float(sh), z = __half2float(zh);
-      uint32_t code = 0;
-      if (sc != 0.0f) {
-        const float t = __fdiv_rn(__fsub_rn(which ? rv[u] : rk[u], z), sc);
-        code = static_cast<uint32_t>(fminf(fmaxf(rintf(t), 0.0f), 3.0f));
-      }
-      sm.codes[u][which][i] = static_cast<uint8_t>(code);
-      szw[u][which] = static_cast<uint32_t>(__half_as_ushort(sh)) |
-                      (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
+  for (int u = 0; u < NB; ++u) {
+    const float mx = fmaxf(fmaxf(sm.red[u][0][0], sm.red[u][0][1]),
+                           fmaxf(sm.red[u][0][2], sm.red[u][0][3]));
+    const float mn = fminf(fminf(sm.red[u][1][0], sm.red[u][1][1]),
+                           fminf(sm.red[u][1][2], sm.red[u][1][3]));
+    const float mxc = __fmul_rn(clip, mx);
+    const float mnc = __fmul_rn(clip, mn);
+    const float s32 = __fdiv_rn(__fsub_rn(mxc, mnc), 3.0f);
+    const __half sh = __float2half_rn(s32);
+    const __half zh = __float2half_rn(mnc);
+    const float sc = __half2float(sh), z = __half2float(zh);
+    uint32_t code = 0;
+    if (sc != 0.0f) {
+      const float t = __fdiv_rn(__fsub_rn(r[u], z), sc);
+      code = static_cast<uint32_t>(fminf(fmaxf(rintf(t), 0.0f), 3.0f));
     }
+    sm.codes[u][i] = static_cast<uint8_t>(code);
+    szw[u] = static_cast<uint32_t>(__half_as_ushort(sh)) |
+             (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
+  }
   __syncthreads();
-  // scatter into the page records (layout in include/kvq.h)
+  // scatter this role's half of each page record (layout in include/kvq.h)
 #pragma unroll
   for (int u = 0; u < NB; ++u) {
     if (rec[u] == nullptr) continue;
-    uint8_t* const r = rec[u];
+    uint8_t* const rp = rec[u];
     const int tau = pos[u] % kPage;
-    if (i < 8) {
+    if (which == 0 && i < 8) {
       // keys: word h of lane group t of row tau & 7
       const int t = i & 3, h = i >> 2;
       uint32_t wv = 0;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         const int d = 16 * w + 2 * t + 8 * h;
-        wv |= static_cast<uint32_t>(sm.codes[u][0][d]) << (2 * w);
-        wv |= static_cast<uint32_t>(sm.codes[u][0][d + 1]) << (16 + 2 * w);
+        wv |= static_cast<uint32_t>(sm.codes[u][d]) << (2 * w);
+        wv |= static_cast<uint32_t>(sm.codes[u][d + 1]) << (16 + 2 * w);
       }
-      *reinterpret_cast<uint32_t*>(r + 16 * (4 * (tau & 7) + t) + 8 * (tau >> 3) + 4 * h) = wv;
-    } else if (i < 24) {
+      *reinterpret_cast<uint32_t*>(rp + 16 * (4 * (tau & 7) + t) + 8 * (tau >> 3) + 4 * h) = wv;
+    } else if (which == 1 && i < 16) {
       // values: the token's 16-bit half of word (2 th + dh) of lane 4 g + t
-      const int k = i - 8, g = k >> 1, dh = k & 1;
+      const int g = i >> 1, dh = i & 1;
       uint32_t hv = 0;
 #pragma unroll
-      for (int m = 0; m < 8; ++m) hv |= static_cast<uint32_t>(sm.codes[u][1][16 * m + g + 8 * dh]) << (2 * m);
+      for (int m = 0; m < 8; ++m) hv |= static_cast<uint32_t>(sm.codes[u][16 * m + g + 8 * dh]) << (2 * m);
       const int t = (tau & 7) >> 1, e = tau & 1, th = tau >> 3;
-      *reinterpret_cast<uint16_t*>(r + 512 + 16 * (4 * g + t) + 4 * (2 * th + dh) + 2 * e) =
+      *reinterpret_cast<uint16_t*>(rp + 512 + 16 * (4 * g + t) + 4 * (2 * th + dh) + 2 * e) =
           static_cast<uint16_t>(hv);
-    } else if (i < 26) {
-      const int which = i - 24;
-      *reinterpret_cast<uint32_t*>(r + 1024 + 16 * (tau & 7) + 8 * which + 4 * (tau >> 3)) =
-          which ? szw[u][1] : szw[u][0];
+    } else if (i == 32) {
+      *reinterpret_cast<uint32_t*>(rp + 1024 + 16 * (tau & 7) + 8 * which + 4 * (tau >> 3)) = szw[u];
     }
   }
 }
@@ -1886,6 +1875,7 @@ cudaError_t launch_qprep_nb(const DecodeArgs& a, const float* RK, const float* m
 
 cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, const float* mu, float sm_scale,
                          cudaStream_t st) {
+  if (a.prep_nb >= 8) return launch_qprep_nb<8>(a, RK, mu, sm_scale, st);
   if (a.prep_nb >= 4) return launch_qprep_nb<4>(a, RK, mu, sm_scale, st);
   if (a.prep_nb == 2) return launch_qprep_nb<2>(a, RK, mu, sm_scale, st);
   return launch_qprep_nb<1>(a, RK, mu, sm_scale, st);
@@ -1896,12 +1886,13 @@ cudaError_t launch_step_prep_nb(const DecodeArgs& a, const StepArgs& sa, cudaStr
   cudaError_t e = set_smem_attr<StepPrepSmem<NB>, step_prep_kernel<NB>>();
   if (e != cudaSuccess) return e;
   e = launch_dependent(step_prep_kernel<NB>,
-                       dim3((a.batch + NB - 1) / NB + (a.balanced ? 1 : 0), a.Hkv, 2), dim3(128),
+                       dim3((a.batch + NB - 1) / NB + (a.balanced ? 1 : 0), a.Hkv, 3), dim3(128),
                        sizeof(StepPrepSmem<NB>), st, a, sa);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_step_prep(const DecodeArgs& a, const StepArgs& sa, cudaStream_t st) {
+  if (a.prep_nb >= 8) return launch_step_prep_nb<8>(a, sa, st);
   if (a.prep_nb >= 4) return launch_step_prep_nb<4>(a, sa, st);
   if (a.prep_nb == 2) return launch_step_prep_nb<2>(a, sa, st);
   return launch_step_prep_nb<1>(a, sa, st);
@@ -1973,6 +1964,26 @@ cudaError_t launch_transpose(const float* in, float* out, int count, cudaStream_
 }
 
 int combine_head_ctas_per_sm() { return kHeadCombineCtasPerSm; }
+
+template <int NB>
+static int step_prep_ctas_per_sm_nb() {
+  if (set_smem_attr<StepPrepSmem<NB>, step_prep_kernel<NB>>() != cudaSuccess) return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_prep_kernel<NB>, 128,
+                                                    sizeof(StepPrepSmem<NB>)) != cudaSuccess ||
+      n < 1)
+    return 1;
+  return n;
+}
+
+int step_prep_ctas_per_sm(int nb) {
+  switch (nb) {
+    case 8: return step_prep_ctas_per_sm_nb<8>();
+    case 4: return step_prep_ctas_per_sm_nb<4>();
+    case 2: return step_prep_ctas_per_sm_nb<2>();
+    default: return step_prep_ctas_per_sm_nb<1>();
+  }
+}
 
 int decode_int2_ctas_per_sm() {
   if (set_smem_attr<Int2Smem, decode_int2_kernel<false>>() != cudaSuccess) return 1;

@@ -16,6 +16,7 @@ struct kvq_handle {
   int device = 0;
   int num_sms = 1;
   int ctas_int2 = 1, ctas_bf16 = 1;
+  int ctas_prep[4] = {1, 1, 1, 1};  // step-preparation CTAs per SM, 1/2/4/8 sequences each
   uint32_t* status = nullptr;      // device
   float* bank = nullptr;           // device: R [2][Hkv][D][D], RVt [Hkv][D][D], mu [Hkv][D]
   bool ready = false;
@@ -255,14 +256,17 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
     // partial wave would double the makespan
     a.sched_ctas = a.balanced ? static_cast<int>((ctas / slots) * slots / (a.Hkv / a.hpc)) : 0;
   }
-  // Sequences per preparation CTA: the fewest (1, 2 or 4) that bring the
-  // batch * Hkv append CTAs (one per SM: they stage R_K and R_V) down to one
-  // wave, so that a large batch does not stage the rotations once per sequence
-  // (64-sequence ragged step: 189.4 -> 187.0 us).
+  // Sequences per preparation CTA: the fewest (1, 2, 4 or 8) that bring the
+  // step preparation's 3 * batch * Hkv / nb CTAs (key append, value append,
+  // query; each stages one rotation matrix) down to one wave, so that a large
+  // batch neither stages the rotations once per sequence nor runs its
+  // preparation in several waves.
   a.prep_nb = 1;
-  while (a.prep_nb < 4 &&
-         static_cast<long>((batch + a.prep_nb - 1) / a.prep_nb) * a.Hkv > h->num_sms)
+  for (int k = 0; k < 3; ++k) {
+    const long ctas = 3L * ((batch + a.prep_nb - 1) / a.prep_nb) * a.Hkv;
+    if (ctas <= static_cast<long>(h->num_sms) * h->ctas_prep[k]) break;
     a.prep_nb *= 2;
+  }
   // two KV-head combine CTAs per SM when one per SM would take more than a wave
   // (64-sequence ragged step: 186.6 -> 183.6 us)
   a.combine_light = (!win.on &&
@@ -389,6 +393,7 @@ int kvq_create(const kvq_layout* layout, kvq_handle** out) {
   }
   h->ctas_int2 = kvq::decode_int2_ctas_per_sm();
   h->ctas_bf16 = kvq::decode_bf16_ctas_per_sm();
+  for (int k = 0; k < 4; ++k) h->ctas_prep[k] = kvq::step_prep_ctas_per_sm(1 << k);
   *out = h;
   return KVQ_OK;
 }

@@ -58,7 +58,7 @@ struct DecodeArgs {
   // partials sit in slots sched_base[b] .. sched_base[b] + sched_nsplit[b] - 1,
   // partial (slot, head) at part[(slot * H + head) * kPartStride].  The table
   // is written by an extra CTA of the query-preparation kernel.
-  int prep_nb = 1;            // sequences per query-preparation / step-preparation CTA (1, 2, 4)
+  int prep_nb = 1;            // sequences per query-preparation / step-preparation CTA (1, 2, 4, 8)
   int balanced = 0;
   int sched_ctas = 0;          // chunks the balanced schedule may use: whole waves of CTAs
   int4* sched_map = nullptr;   // [batch * splits]
@@ -132,6 +132,7 @@ int optr_loss_grad(int H, int T, int Nq, int G, int Dm, const uint16_t* K, const
                    cudaStream_t st);
 int decode_int2_ctas_per_sm();
 int combine_head_ctas_per_sm();
+int step_prep_ctas_per_sm(int nb);  // nb = 1, 2, 4 or 8 sequences per CTA
 int decode_bf16_ctas_per_sm();
 // Makes `dev` the calling thread's current device while the guard lives and
 // gives the caller's device back afterwards, so that no entry point changes
