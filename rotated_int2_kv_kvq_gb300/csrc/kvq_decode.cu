@@ -389,16 +389,25 @@ struct StepSmem {
   uint64_t bar;
 };
 
+// Sequences per query CTA of a step preparation whose append CTAs take NB:
+// the query rotation costs G times the append's per sequence, so its groups
+// stay small and more of its CTAs share the wave.
+template <int NB>
+__host__ __device__ constexpr int step_query_nb() { return NB < 2 ? NB : 2; }
+template <int NB>
+__host__ __device__ constexpr int step_roles() { return 2 + NB / step_query_nb<NB>(); }
+
 template <int NB>
 union StepPrepSmem {
   StepSmem<NB> append;
-  QprepSmem<NB> query;
+  QprepSmem<step_query_nb<NB>()> query;
 };
 
 // CTA (group of NB sequences, kv, role): role 0 appends the new keys of the
-// group's sequences for KV head kv, role 1 their new values (each role stages
-// its one rotation matrix, so every CTA of the launch needs at most one
-// matrix of shared memory and two fit on an SM), role 2 prepares their queries.
+// group's sequences for KV head kv, role 1 their new values, roles 2, 3, ...
+// prepare their queries, step_query_nb<NB>() sequences each (every role
+// stages its one rotation matrix, so every CTA of the launch needs at most
+// one matrix of shared memory and several fit on an SM).
 template <int NB>
 __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs st) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -410,9 +419,13 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
     return;
   }
   const int nb = min(NB, a.batch - b0);
-  if (blockIdx.z == 2) {
-    qprep_cta<NB>(a, st.q_rotated ? nullptr : st.RK, st.mu, a.log2_scale,
-                  reinterpret_cast<StepPrepSmem<NB>*>(smem_raw)->query, b0, nb, kv);
+  if (blockIdx.z >= 2) {
+    constexpr int NBQ = step_query_nb<NB>();
+    const int bq = b0 + (blockIdx.z - 2) * NBQ;
+    if (bq < a.batch)
+      qprep_cta<NBQ>(a, st.q_rotated ? nullptr : st.RK, st.mu, a.log2_scale,
+                     reinterpret_cast<StepPrepSmem<NB>*>(smem_raw)->query, bq,
+                     min(NBQ, a.batch - bq), kv);
     return;
   }
   const int which = blockIdx.z;      // 0 keys, 1 values
@@ -1875,9 +1888,8 @@ cudaError_t launch_qprep_nb(const DecodeArgs& a, const float* RK, const float* m
 
 cudaError_t launch_qprep(const DecodeArgs& a, const float* RK, const float* mu, float sm_scale,
                          cudaStream_t st) {
-  if (a.prep_nb >= 8) return launch_qprep_nb<8>(a, RK, mu, sm_scale, st);
-  if (a.prep_nb >= 4) return launch_qprep_nb<4>(a, RK, mu, sm_scale, st);
-  if (a.prep_nb == 2) return launch_qprep_nb<2>(a, RK, mu, sm_scale, st);
+  // the query groups of the step preparation with the same prep_nb
+  if (a.prep_nb >= 2) return launch_qprep_nb<2>(a, RK, mu, sm_scale, st);
   return launch_qprep_nb<1>(a, RK, mu, sm_scale, st);
 }
 
@@ -1886,7 +1898,8 @@ cudaError_t launch_step_prep_nb(const DecodeArgs& a, const StepArgs& sa, cudaStr
   cudaError_t e = set_smem_attr<StepPrepSmem<NB>, step_prep_kernel<NB>>();
   if (e != cudaSuccess) return e;
   e = launch_dependent(step_prep_kernel<NB>,
-                       dim3((a.batch + NB - 1) / NB + (a.balanced ? 1 : 0), a.Hkv, 3), dim3(128),
+                       dim3((a.batch + NB - 1) / NB + (a.balanced ? 1 : 0), a.Hkv, step_roles<NB>()),
+                       dim3(128),
                        sizeof(StepPrepSmem<NB>), st, a, sa);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

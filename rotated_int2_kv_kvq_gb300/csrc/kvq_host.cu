@@ -256,14 +256,15 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
     // partial wave would double the makespan
     a.sched_ctas = a.balanced ? static_cast<int>((ctas / slots) * slots / (a.Hkv / a.hpc)) : 0;
   }
-  // Sequences per preparation CTA: the fewest (1, 2, 4 or 8) that bring the
-  // step preparation's 3 * batch * Hkv / nb CTAs (key append, value append,
-  // query; each stages one rotation matrix) down to one wave, so that a large
-  // batch neither stages the rotations once per sequence nor runs its
-  // preparation in several waves.
+  // Sequences per append CTA of the step preparation: the fewest (1, 2, 4 or
+  // 8) that bring its ceil(batch / nb) * Hkv * (2 + nb / min(nb, 2)) CTAs (key
+  // append, value append, queries two sequences at a time; each stages one
+  // rotation matrix) down to one wave, so that a large batch neither stages
+  // the rotations once per sequence nor runs its preparation in several waves.
   a.prep_nb = 1;
   for (int k = 0; k < 3; ++k) {
-    const long ctas = 3L * ((batch + a.prep_nb - 1) / a.prep_nb) * a.Hkv;
+    const long roles = 2 + (a.prep_nb < 2 ? 1 : a.prep_nb / 2);
+    const long ctas = roles * ((batch + a.prep_nb - 1) / a.prep_nb) * a.Hkv;
     if (ctas <= static_cast<long>(h->num_sms) * h->ctas_prep[k]) break;
     a.prep_nb *= 2;
   }

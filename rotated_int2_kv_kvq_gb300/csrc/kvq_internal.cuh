@@ -58,7 +58,7 @@ struct DecodeArgs {
   // partials sit in slots sched_base[b] .. sched_base[b] + sched_nsplit[b] - 1,
   // partial (slot, head) at part[(slot * H + head) * kPartStride].  The table
   // is written by an extra CTA of the query-preparation kernel.
-  int prep_nb = 1;            // sequences per query-preparation / step-preparation CTA (1, 2, 4, 8)
+  int prep_nb = 1;            // sequences per step-preparation append CTA (1, 2, 4, 8); query CTAs take min(prep_nb, 2)
   int balanced = 0;
   int sched_ctas = 0;          // chunks the balanced schedule may use: whole waves of CTAs
   int4* sched_map = nullptr;   // [batch * splits]
