@@ -393,3 +393,31 @@ def test_full_stack_sampled_layers(layer):
                          Ktok, Vtok)
     assert_boundary_count(near, 300, f"full stack layer {layer}")
     assert c.status() == 0
+
+
+@pytest.mark.parametrize("out_rotated,G,splits", [(True, 4, 3), (False, 2, 0)])
+def test_light_combine_large_batch(out_rotated, G, splits):
+    """More (sequence, KV head) pairs than one wave of one-per-SM KV-head
+    combine CTAs: the combine at two CTAs per SM, checked on every (sequence,
+    head) output against the oracle.  Odd batch, plain and rotated-basis
+    output, G = 2 (half of each CTA's head threads idle), an empty sequence
+    (output 0)."""
+    wl = W.WORKLOADS["ragged_64"]
+    B, Hkv = 21, 8
+    pt, _ = W.page_table(wl)
+    pt = pt[:B].copy()
+    c = Cache(wl, out_rotated=out_rotated, page_table=pt, num_pool_pages=int(pt.max()) + 1,
+              num_heads=Hkv * G, num_kv_heads=Hkv)
+    rng = np.random.default_rng(40 + G)
+    lens = rng.integers(1, 400, size=B)
+    lens[3], lens[B - 1] = 0, 77
+    lens = np.minimum(lens, (pt >= 0).sum(axis=1) * 16)
+    c.append_range(range(B), 0, [int(x) for x in lens])
+    q = W.queries(wl, 0, 70)[:B, :Hkv * G].copy()
+    got = c.decode(q, lens, splits)
+    assert c.status() == 0
+    assert np.all(got[3] == 0.0)
+    pairs = [[b, h] for b in range(B) if lens[b] > 0 for h in range(Hkv * G)]
+    want = c.oracle_decode(c.pool_host(), q, lens, pairs)
+    assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want,
+                           f"two-per-SM combine, out_rotated={out_rotated}, G={G}")

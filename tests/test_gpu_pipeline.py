@@ -76,13 +76,15 @@ def test_append_decode_equals_append_then_decode(name, splits):
     assert a.status() == 0 and b.status() == 0
 
 
-@pytest.mark.parametrize("B", [24, 48])
+@pytest.mark.parametrize("B", [24, 25, 48])
 def test_append_decode_large_batch(B):
     """Batches whose per-sequence preparation CTAs would exceed one wave: the
-    query and step preparation take 2 (B = 24) or 4 (B = 48) sequences per
-    CTA; B = 48 also takes the length-balanced decode schedule.  Fused step
-    against append + decode (pools byte for byte, outputs bit for bit) and
-    against the float64 oracle."""
+    step preparation groups 2 (B = 24, 25) or 4 (B = 48) sequences per append
+    CTA (B = 25 ends with a group of one); B = 48 also takes the
+    length-balanced decode schedule; all three take the KV-head combine at two
+    CTAs per SM.  Fused step against append + decode (pools byte for byte,
+    outputs bit for bit) and against the float64 oracle, on sampled (sequence,
+    head) pairs plus every head of the last sequence and of sequence 1."""
     wl = W.WORKLOADS["ragged_64"]
     pt, npool = W.page_table(wl)
     pt = pt[:B].copy()
@@ -105,6 +107,7 @@ def test_append_decode_large_batch(B):
         assert np.array_equal(got, want), f"output differs at step {step}"
         lens = np.maximum(lens_after, lens)
     pairs = [[int(x), int(y)] for x, y in zip(rng.integers(0, B, 12), rng.integers(0, wl.num_heads, 12))]
+    pairs += [[bb, hh] for bb in (1, B - 1) for hh in range(wl.num_heads)]
     oracle_out = a.oracle_decode(a.pool_host(), q, lens_after, pairs)
     assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], oracle_out,
                            f"large batch B={B}")
