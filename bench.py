@@ -1103,7 +1103,7 @@ def run_optr(args):
                      "unit": "TFLOP/s", "frac": flops / sec / 1e12 / nominal, "traffic": None,
                      "peak_kind": "fp32 FMA nominal: 152 SMs x 128 lanes x 2 x 2.07 GHz",
                      "note": "products with 64-multiple M and N (except those by a 128 x 128 "
-                             "matrix) run as bf16 x 3 on mma.sync tensor cores, the rest in "
+                             "matrix) run on mma.sync tensor cores with each fp32 operand split into three bf16 parts (six products), the rest in "
                              "fp32; achieved counts the algorithmic fp32 flops once"},
         "losses": {"key": [float(h[0, 0].mean()), float(h[0, -1].mean())],
                    "value": [float(h[1, 0].mean()), float(h[1, -1].mean())]},

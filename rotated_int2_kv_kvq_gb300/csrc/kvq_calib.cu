@@ -249,14 +249,20 @@ __global__ void __launch_bounds__((BM / 4) * (BM / 4)) gemm_tile_kernel(Gemm g) 
 
 // ---------------------------------------------------------------------------
 // The same product on the tensor cores, for the large GEMMs (M and N multiples
-// of 64, K of 32): every fp32 operand x is split into two bf16 parts, hi =
-// bf16(x) and lo = bf16(x - hi), as it is staged into shared memory, and
-// op(A) op(B) is taken as Ah Bh + Ah Bl + Al Bh with mma.sync.m16n8k16 (bf16
-// in, fp32 accumulate).  The dropped Al Bl term and the residual of the split
-// are about 2^-16 of each product.  64 x 64 output tile, 32-deep k-slices
-// double-buffered (the next slice's fp32 loads in flight during the current
-// slice's products), 4 warps of 32 x 32; fragments come from shared memory by
-// ldmatrix (the transposing form for an operand kept [k][row]).
+// of 64, K of 32): every fp32 operand x is split into three bf16 parts as it
+// is staged into shared memory, hi = bf16(x), mid = bf16(x - hi), lo =
+// bf16(x - hi - mid) (both differences exact in fp32), and op(A) op(B) is
+// taken as the six products of parts whose orders add up to at most 2^-16
+// (lo hi, hi lo, mid mid, mid hi, hi mid, hi hi, smallest first) with
+// mma.sync.m16n8k16 (bf16 in, fp32 accumulate).  What is dropped (mid lo, lo
+// mid, lo lo and the split's residual) is about 2^-24 of each product, the
+// rounding of an fp32 product; with hi and lo only (three products) the
+// products kept about 2^-16, which let a 40-step calibration of the value
+// objective stall on one head where the float64 oracle falls to half.
+// 64 x 64 output tile, 32-deep k-slices (the next slice's fp32 loads in
+// flight during the current slice's products), 4 warps of 32 x 32; fragments
+// come from shared memory by ldmatrix (the transposing form for an operand
+// kept [k][row]).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -273,12 +279,18 @@ __device__ __forceinline__ void mma_bf16_acc(float (&d)[4], const uint32_t (&a)[
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// hi and lo bf16 parts of x, packed with y's: {lo16 = part of x, hi16 = part of y}
-__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
+// hi, mid and lo bf16 parts of x, packed with y's: {lo16 = part of x, hi16 =
+// part of y}
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& mid,
+                                             uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
   const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+  const float rx = x - hf.x, ry = y - hf.y;
+  const __nv_bfloat162 m = __floats2bfloat162_rn(rx, ry);
+  const float2 mf = __bfloat1622float2(m);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(rx - mf.x, ry - mf.y);
   hi = *reinterpret_cast<const uint32_t*>(&h);
+  mid = *reinterpret_cast<const uint32_t*>(&m);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
@@ -299,8 +311,8 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(Gemm g) {
   // one ldmatrix in different banks, and every staging store is 8 bytes.
   constexpr int RK = BK + 8, RR = BM + 8, PLANE = BM * RK;
   static_assert(BK * RR <= PLANE, "a [k][row] tile fits a plane");
-  __shared__ __align__(16) uint16_t sA[2][2][PLANE];    // [buffer][hi, lo]
-  __shared__ __align__(16) uint16_t sB[2][2][PLANE];
+  __shared__ __align__(16) uint16_t sA[3][PLANE];    // [hi, mid, lo]
+  __shared__ __align__(16) uint16_t sB[3][PLANE];
   const int bz = blockIdx.z / g.ksplit, kz = blockIdx.z % g.ksplit;
   const int kbeg = kz * g.kchunk, kend = min(g.K, kbeg + g.kchunk);
   const float* A = g.A + bz * g.sA;
@@ -327,20 +339,21 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(Gemm g) {
                                                     n0 + 4 * (f % 16));
     }
   };
-  auto put = [&](uint16_t* H, uint16_t* L, const float4& v, int f, bool kfast) {
+  auto put = [&](uint16_t (*P)[PLANE], const float4& v, int f, bool kfast) {
     const int off = kfast ? (f / 8) * RK + 4 * (f % 8) : (f / 16) * RR + 4 * (f % 16);
-    uint32_t h0, l0, h1, l1;
-    split_bf16x2(v.x, v.y, h0, l0);
-    split_bf16x2(v.z, v.w, h1, l1);
-    *reinterpret_cast<uint2*>(H + off) = make_uint2(h0, h1);
-    *reinterpret_cast<uint2*>(L + off) = make_uint2(l0, l1);
+    uint32_t h0, m0, l0, h1, m1, l1;
+    split_bf16x2(v.x, v.y, h0, m0, l0);
+    split_bf16x2(v.z, v.w, h1, m1, l1);
+    *reinterpret_cast<uint2*>(P[0] + off) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(P[1] + off) = make_uint2(m0, m1);
+    *reinterpret_cast<uint2*>(P[2] + off) = make_uint2(l0, l1);
   };
-  auto store = [&](int buf) {
+  auto store = [&]() {
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
       const int f = tid + 128 * p;
-      put(sA[buf][0], sA[buf][1], ra[p], f, kA);
-      put(sB[buf][0], sB[buf][1], rb[p], f, kB);
+      put(sA, ra[p], f, kA);
+      put(sB, rb[p], f, kB);
     }
   };
   float acc[2][4][4];
@@ -350,10 +363,9 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(Gemm g) {
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.0f;
-  int buf = 0;
   if (kbeg < kend) {
     load(kbeg);
-    store(0);
+    store();
   }
   __syncthreads();
   // Element offsets this lane gives ldmatrix.  A (m16 x k16 tile at row r0,
@@ -375,45 +387,45 @@ __global__ void __launch_bounds__(128) gemm_tc_kernel(Gemm g) {
     if (more) load(k0 + BK);
 #pragma unroll
     for (int ks = 0; ks < BK; ks += 16) {
-      uint32_t ah[2][4], al[2][4], bh[4][2], bl[4][2];
+      uint32_t af[3][2][4], bf[3][4][2];     // [hi, mid, lo] fragments
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const int o = a_off(wm + 16 * mt, ks);
-        const uint32_t h = static_cast<uint32_t>(__cvta_generic_to_shared(sA[buf][0] + o));
-        const uint32_t l = static_cast<uint32_t>(__cvta_generic_to_shared(sA[buf][1] + o));
-        if (kA) {
-          ldsm_x4(h, ah[mt][0], ah[mt][1], ah[mt][2], ah[mt][3]);
-          ldsm_x4(l, al[mt][0], al[mt][1], al[mt][2], al[mt][3]);
-        } else {
-          ldsm_x4_t(h, ah[mt][0], ah[mt][1], ah[mt][2], ah[mt][3]);
-          ldsm_x4_t(l, al[mt][0], al[mt][1], al[mt][2], al[mt][3]);
+      for (int pl = 0; pl < 3; ++pl) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const uint32_t ad =
+              static_cast<uint32_t>(__cvta_generic_to_shared(sA[pl] + a_off(wm + 16 * mt, ks)));
+          if (kA) ldsm_x4(ad, af[pl][mt][0], af[pl][mt][1], af[pl][mt][2], af[pl][mt][3]);
+          else ldsm_x4_t(ad, af[pl][mt][0], af[pl][mt][1], af[pl][mt][2], af[pl][mt][3]);
         }
-      }
 #pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        const int o = b_off(wn + 16 * np, ks);
-        const uint32_t h = static_cast<uint32_t>(__cvta_generic_to_shared(sB[buf][0] + o));
-        const uint32_t l = static_cast<uint32_t>(__cvta_generic_to_shared(sB[buf][1] + o));
-        if (kB) {
-          ldsm_x4(h, bh[2 * np][0], bh[2 * np][1], bh[2 * np + 1][0], bh[2 * np + 1][1]);
-          ldsm_x4(l, bl[2 * np][0], bl[2 * np][1], bl[2 * np + 1][0], bl[2 * np + 1][1]);
-        } else {
-          ldsm_x4_t(h, bh[2 * np][0], bh[2 * np][1], bh[2 * np + 1][0], bh[2 * np + 1][1]);
-          ldsm_x4_t(l, bl[2 * np][0], bl[2 * np][1], bl[2 * np + 1][0], bl[2 * np + 1][1]);
+        for (int np = 0; np < 2; ++np) {
+          const uint32_t bd =
+              static_cast<uint32_t>(__cvta_generic_to_shared(sB[pl] + b_off(wn + 16 * np, ks)));
+          if (kB)
+            ldsm_x4(bd, bf[pl][2 * np][0], bf[pl][2 * np][1], bf[pl][2 * np + 1][0],
+                    bf[pl][2 * np + 1][1]);
+          else
+            ldsm_x4_t(bd, bf[pl][2 * np][0], bf[pl][2 * np][1], bf[pl][2 * np + 1][0],
+                      bf[pl][2 * np + 1][1]);
         }
       }
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-          mma_bf16_acc(acc[mt][nt], al[mt], bh[nt][0], bh[nt][1]);
-          mma_bf16_acc(acc[mt][nt], ah[mt], bl[nt][0], bl[nt][1]);
-          mma_bf16_acc(acc[mt][nt], ah[mt], bh[nt][0], bh[nt][1]);
+          mma_bf16_acc(acc[mt][nt], af[2][mt], bf[0][nt][0], bf[0][nt][1]);   // lo hi
+          mma_bf16_acc(acc[mt][nt], af[0][mt], bf[2][nt][0], bf[2][nt][1]);   // hi lo
+          mma_bf16_acc(acc[mt][nt], af[1][mt], bf[1][nt][0], bf[1][nt][1]);   // mid mid
+          mma_bf16_acc(acc[mt][nt], af[1][mt], bf[0][nt][0], bf[0][nt][1]);   // mid hi
+          mma_bf16_acc(acc[mt][nt], af[0][mt], bf[1][nt][0], bf[1][nt][1]);   // hi mid
+          mma_bf16_acc(acc[mt][nt], af[0][mt], bf[0][nt][0], bf[0][nt][1]);   // hi hi
         }
     }
-    if (more) store(buf ^ 1);     // the other buffer was last read before the previous barrier
-    __syncthreads();
-    buf ^= 1;
+    __syncthreads();              // every warp is done with this slice's planes
+    if (more) {
+      store();
+      __syncthreads();
+    }
   }
   const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
