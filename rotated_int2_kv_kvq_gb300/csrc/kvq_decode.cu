@@ -370,14 +370,15 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
 }
 
 // ---------------------------------------------------------------------------
-// Append + query preparation in one launch (kvq_append_decode), CTA (b, kv,
-// role).  Role 0 quantises sequence b's new token (position seq_lens[b] - 1)
-// for KV head kv into its page record, with exactly the fp32 operation
-// sequence of the append kernel (centre, fmaf chain over j = 0..127 in order,
-// max/min, clip, fp16 scale/zero, rint codes); role 1 prepares the rotated
-// query exactly like qprep_kernel.  The two halves share nothing, so they run
-// side by side on separate SMs.  Rotation matrices are bulk-copied before the
-// CTA waits for its predecessor; the token, q and the tables are read, and the
+// Append + query preparation in one launch (kvq_append_decode), CTA (group of
+// sequences, kv, role).  Roles 0 and 1 quantise the new key and the new value
+// (position seq_lens[b] - 1) of each sequence b of the group for KV head kv
+// into its page record, with exactly the fp32 operation sequence of the
+// append kernel (centre the key, fmaf chain over j = 0..127 in order,
+// max/min, clip, fp16 scale/zero, rint codes); the other roles prepare the
+// rotated queries exactly like qprep_kernel.  The roles share nothing, so
+// they run side by side.  Rotation matrices are bulk-copied before the CTA
+// waits for its predecessor; the token, q and the tables are read, and the
 // pool written, only after that wait.
 // ---------------------------------------------------------------------------
 template <int NB>
