@@ -384,9 +384,13 @@ __global__ void __launch_bounds__(128) qprep_kernel(DecodeArgs a, const float* _
 template <int NB>
 struct StepSmem {
   float R[kDim * kDim];              // R_K (key role) or R_V (value role)
-  alignas(16) float x[NB][kDim];     // the centred key or the value of each sequence
+  alignas(16) float x[NB][kDim];     // the centred key or the value of each sequence, then its rotation
   float red[NB][2][4];               // [sequence][max|min][warp]
   uint8_t codes[NB][kDim];
+  uint8_t* rec[NB];                  // the page record of the sequence's new token, or none
+  uint8_t* bf16_rec[NB];             // its BF16 window record, or none
+  int tau[NB];                       // the token's row in its page
+  uint32_t szw[NB];                  // fp16 scale | fp16 zero << 16
   uint64_t bar;
 };
 
@@ -445,55 +449,70 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
 
   const float mui = which ? 0.0f : st.mu[static_cast<size_t>(kv) * kDim + i];
   const uint16_t* X = which ? st.V : st.K;
-  uint8_t* rec[NB];    // the record of each sequence's new token, or none
-  int pos[NB];         // its position
+  // element i of each sequence's token, then (lane u of warp 0) the page
+  // lookups of sequence u, in the same round trip; per-sequence loops below
+  // run from shared memory, so that the kernel's code stays small
+  uint16_t bits[NB];
 #pragma unroll
-  for (int u = 0; u < NB; ++u) {
-    rec[u] = nullptr;
-    pos[u] = -1;
-    float x = 0.0f;
+  for (int u = 0; u < NB; ++u)
+    bits[u] = u < nb ? X[(static_cast<size_t>(b0 + u) * a.Hkv + kv) * kDim + i] : 0;
+  if (warp == 0 && lane < NB) {
+    const int u = lane;
+    uint8_t* rec = nullptr;
+    uint8_t* brec = nullptr;
+    int tau = 0;
     if (u < nb) {
       const int b = b0 + u;
-      // the token first, so that its load overlaps the table lookups below
-      const uint16_t bits = X[(static_cast<size_t>(b) * a.Hkv + kv) * kDim + i];
       const int seq_len = a.seq_lens[b];
       const int p = seq_len - 1;
       if (seq_len > a.max_pages * kPage) {
-        if (i == 0 && kv == 0 && which == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
+        if (kv == 0 && which == 0) atomicOr(a.status, KVQ_STATUS_BAD_SEQLEN);
       } else if (p >= 0) {
+        tau = p % kPage;
         const int page = a.page_table[static_cast<size_t>(b) * a.max_pages + p / kPage];
-        if (page >= 0 && page < a.num_pool_pages) {
-          rec[u] = st.pool + (static_cast<size_t>(page) * a.Hkv + kv) * kInt2Rec;
-          pos[u] = p;
-        } else if (i == 0 && which == 0) {
+        if (page >= 0 && page < a.num_pool_pages)
+          rec = st.pool + (static_cast<size_t>(page) * a.Hkv + kv) * kInt2Rec;
+        else if (which == 0)
           atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
-        }
-      }
-      const float xf = __uint_as_float(static_cast<uint32_t>(bits) << 16);
-      x = which ? xf : __fsub_rn(xf, mui);
-      if (st.bf16_pool != nullptr && p >= 0 && seq_len <= a.max_pages * kPage) {
-        // the BF16 window cache's copy of the token (same placement as the BF16
-        // append kernel: fragment order of the BF16 page record)
-        const int page = st.bf16_page_table[static_cast<size_t>(b) * a.max_pages + p / kPage];
-        if (page >= 0 && page < st.bf16_num_pool_pages) {
-          uint8_t* base = st.bf16_pool + (static_cast<size_t>(page) * a.Hkv + kv) * kBf16Rec;
-          const int tau = p % kPage;
-          if (which == 0) {
-            const int w = i >> 4, r = i & 15, h = r >> 3, t = (r >> 1) & 3, e = r & 1;
-            const int L = 4 * (tau & 7) + t, reg = (tau >> 3) + 2 * h;
-            *reinterpret_cast<uint16_t*>(base + 512 * w + 16 * L + 4 * reg + 2 * e) = bits;
-          } else {
-            const int m = i >> 4, r = i & 15, g = r & 7, dh = r >> 3;
-            const int t = (tau & 7) >> 1, e = tau & 1, th = tau >> 3;
-            const int L = 4 * g + t, reg = 2 * th + dh;
-            *reinterpret_cast<uint16_t*>(base + 4096 + 512 * m + 16 * L + 4 * reg + 2 * e) = bits;
-          }
-        } else if (i == 0 && which == 0) {
-          atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
+        if (st.bf16_pool != nullptr) {
+          const int bpage = st.bf16_page_table[static_cast<size_t>(b) * a.max_pages + p / kPage];
+          if (bpage >= 0 && bpage < st.bf16_num_pool_pages)
+            brec = st.bf16_pool + (static_cast<size_t>(bpage) * a.Hkv + kv) * kBf16Rec;
+          else if (which == 0)
+            atomicOr(a.status, KVQ_STATUS_BAD_PAGE);
         }
       }
     }
-    sm.x[u][i] = x;
+    sm.rec[u] = rec;
+    sm.bf16_rec[u] = brec;
+    sm.tau[u] = tau;
+  }
+#pragma unroll
+  for (int u = 0; u < NB; ++u) {
+    const float xf = __uint_as_float(static_cast<uint32_t>(bits[u]) << 16);
+    sm.x[u][i] = u < nb ? (which ? xf : __fsub_rn(xf, mui)) : 0.0f;
+  }
+  __syncthreads();
+  // the BF16 window cache's copy of each token (same placement as the BF16
+  // append kernel: fragment order of the BF16 page record)
+  if (st.bf16_pool != nullptr) {
+#pragma unroll 1
+    for (int u = 0; u < nb; ++u) {
+      uint8_t* base = sm.bf16_rec[u];
+      if (base == nullptr) continue;
+      const int tau = sm.tau[u];
+      const uint16_t bu = X[(static_cast<size_t>(b0 + u) * a.Hkv + kv) * kDim + i];
+      if (which == 0) {
+        const int w = i >> 4, r = i & 15, h = r >> 3, t = (r >> 1) & 3, e = r & 1;
+        const int L = 4 * (tau & 7) + t, reg = (tau >> 3) + 2 * h;
+        *reinterpret_cast<uint16_t*>(base + 512 * w + 16 * L + 4 * reg + 2 * e) = bu;
+      } else {
+        const int m = i >> 4, r = i & 15, g = r & 7, dh = r >> 3;
+        const int t = (tau & 7) >> 1, e = tau & 1, th = tau >> 3;
+        const int L = 4 * g + t, reg = 2 * th + dh;
+        *reinterpret_cast<uint16_t*>(base + 4096 + 512 * m + 16 * L + 4 * reg + 2 * e) = bu;
+      }
+    }
   }
   const bool ok = mbar_wait_bounded(bar, 0);
   if (__syncthreads_or(!ok)) {
@@ -505,28 +524,32 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
   }
   // r_i = fmaf chain over j = 0..127 per sequence, the vector elements read
   // four j at a time; the chains of the group's sequences side by side
-  float r[NB];
+  {
+    float r[NB];
 #pragma unroll
-  for (int u = 0; u < NB; ++u) r[u] = 0.0f;
+    for (int u = 0; u < NB; ++u) r[u] = 0.0f;
 #pragma unroll 2
-  for (int j0 = 0; j0 < kDim; j0 += 4) {
-    float r4[4];
+    for (int j0 = 0; j0 < kDim; j0 += 4) {
+      float r4[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) r4[k] = sm.R[(j0 + k) * kDim + i];
+      for (int k = 0; k < 4; ++k) r4[k] = sm.R[(j0 + k) * kDim + i];
 #pragma unroll
-    for (int u = 0; u < NB; ++u) {
-      const float4 x = *reinterpret_cast<const float4*>(&sm.x[u][j0]);
-      r[u] = fmaf(x.x, r4[0], r[u]);
-      r[u] = fmaf(x.y, r4[1], r[u]);
-      r[u] = fmaf(x.z, r4[2], r[u]);
-      r[u] = fmaf(x.w, r4[3], r[u]);
+      for (int u = 0; u < NB; ++u) {
+        const float4 x = *reinterpret_cast<const float4*>(&sm.x[u][j0]);
+        r[u] = fmaf(x.x, r4[0], r[u]);
+        r[u] = fmaf(x.y, r4[1], r[u]);
+        r[u] = fmaf(x.z, r4[2], r[u]);
+        r[u] = fmaf(x.w, r4[3], r[u]);
+      }
     }
-  }
-
-  // max / min of each rotated vector over its 128 elements
+    __syncthreads();                 // every thread is done reading the vectors
 #pragma unroll
-  for (int u = 0; u < NB; ++u) {
-    float mx = r[u], mn = r[u];
+    for (int u = 0; u < NB; ++u) sm.x[u][i] = r[u];
+  }
+  // max / min of each rotated vector over its 128 elements
+#pragma unroll 1
+  for (int u = 0; u < nb; ++u) {
+    float mx = sm.x[u][i], mn = mx;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -538,10 +561,9 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
     }
   }
   __syncthreads();
-  uint32_t szw[NB];
   const float clip = which ? st.clip_v : st.clip_k;
-#pragma unroll
-  for (int u = 0; u < NB; ++u) {
+#pragma unroll 1
+  for (int u = 0; u < nb; ++u) {
     const float mx = fmaxf(fmaxf(sm.red[u][0][0], sm.red[u][0][1]),
                            fmaxf(sm.red[u][0][2], sm.red[u][0][3]));
     const float mn = fminf(fminf(sm.red[u][1][0], sm.red[u][1][1]),
@@ -554,20 +576,21 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
     const float sc = __half2float(sh), z = __half2float(zh);
     uint32_t code = 0;
     if (sc != 0.0f) {
-      const float t = __fdiv_rn(__fsub_rn(r[u], z), sc);
+      const float t = __fdiv_rn(__fsub_rn(sm.x[u][i], z), sc);
       code = static_cast<uint32_t>(fminf(fmaxf(rintf(t), 0.0f), 3.0f));
     }
     sm.codes[u][i] = static_cast<uint8_t>(code);
-    szw[u] = static_cast<uint32_t>(__half_as_ushort(sh)) |
-             (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
+    if (i == 0)
+      sm.szw[u] = static_cast<uint32_t>(__half_as_ushort(sh)) |
+                  (static_cast<uint32_t>(__half_as_ushort(zh)) << 16);
   }
   __syncthreads();
   // scatter this role's half of each page record (layout in include/kvq.h)
-#pragma unroll
-  for (int u = 0; u < NB; ++u) {
-    if (rec[u] == nullptr) continue;
-    uint8_t* const rp = rec[u];
-    const int tau = pos[u] % kPage;
+#pragma unroll 1
+  for (int u = 0; u < nb; ++u) {
+    uint8_t* const rp = sm.rec[u];
+    if (rp == nullptr) continue;
+    const int tau = sm.tau[u];
     if (which == 0 && i < 8) {
       // keys: word h of lane group t of row tau & 7
       const int t = i & 3, h = i >> 2;
@@ -589,7 +612,8 @@ __global__ void __launch_bounds__(128) step_prep_kernel(DecodeArgs a, StepArgs s
       *reinterpret_cast<uint16_t*>(rp + 512 + 16 * (4 * g + t) + 4 * (2 * th + dh) + 2 * e) =
           static_cast<uint16_t>(hv);
     } else if (i == 32) {
-      *reinterpret_cast<uint32_t*>(rp + 1024 + 16 * (tau & 7) + 8 * which + 4 * (tau >> 3)) = szw[u];
+      *reinterpret_cast<uint32_t*>(rp + 1024 + 16 * (tau & 7) + 8 * which + 4 * (tau >> 3)) =
+          sm.szw[u];
     }
   }
 }
