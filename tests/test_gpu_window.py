@@ -166,19 +166,31 @@ def _step_tokens(wl, lens, Hkv):
     return Kn, Vn
 
 
-@pytest.mark.parametrize("sink,recent,splits", [(64, 256, 0), (5, 37, 3)])
-def test_append_decode_window_equals_separate_calls(sink, recent, splits):
+@pytest.mark.parametrize("sink,recent,splits,B", [(64, 256, 0, 16), (5, 37, 3, 16),
+                                                   (64, 256, 0, 41)])
+def test_append_decode_window_equals_separate_calls(sink, recent, splits, B):
     """kvq_append_decode_window against kvq_append + kvq_bf16_append +
     kvq_decode_window on identical caches: both pools byte for byte and the
     outputs bit for bit, over three steps with ragged lengths and a sequence
-    that takes no token in one step."""
+    that takes no token in one step.  B = 41: the step preparation groups
+    several sequences per append CTA (the last group short), each writing its
+    tokens' BF16 copies too."""
     from kvq_testlib import i32, u16
     from rotated_int2_kv_kvq_gb300 import kvq as K
-    wl = W.WORKLOADS["qwen3_8b_32k"]
-    lens = np.concatenate([np.array([0, 1, 15, 16, 17, 300, 1000, 2047]), np.array([700] * 8)])
+    if B == 16:
+        wl = W.WORKLOADS["qwen3_8b_32k"]
+        kw = {}
+        lens = np.concatenate([np.array([0, 1, 15, 16, 17, 300, 1000, 2047]), np.array([700] * 8)])
+    else:
+        wl = W.WORKLOADS["ragged_64"]
+        rng = np.random.default_rng(B)
+        pt = rng.permutation(B * 48).astype(np.int32).reshape(B, 48)   # 768 tokens each
+        kw = dict(page_table=pt, num_pool_pages=B * 48)
+        lens = rng.integers(1, 700, size=B)
+        lens[:6] = [0, 1, 15, 16, 17, 300]
     pairs = []
     for _ in range(2):
-        ci, cb = Cache(wl), Cache(wl, kind="bf16")
+        ci, cb = Cache(wl, **kw), Cache(wl, kind="bf16", **kw)
         Ks, Vs = ci.append_range(range(len(lens)), 0, [int(x) for x in lens])
         for b, L in enumerate(lens):
             if L:
@@ -186,10 +198,10 @@ def test_append_decode_window_equals_separate_calls(sink, recent, splits):
                           np.arange(L))
         pairs.append((ci, cb))
     (a, ab), (s, sb) = pairs
-    B = len(lens)
+    assert B == len(lens)
     for step in range(3):
         Kn, Vn = _step_tokens(wl, lens, a.Hkv)
-        q = W.queries(wl, 0, 60 + step)
+        q = W.queries(wl, 0, 60 + step)[:B].copy()
         lens_after = lens + 1
         if step == 1:
             lens_after[0] = 0              # sequence 0 takes no token this step
