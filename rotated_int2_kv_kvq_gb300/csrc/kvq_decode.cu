@@ -1521,10 +1521,8 @@ __device__ float window_partial(const DecodeArgs& a, WindowSmem& ws, int b, int 
   return o;
 }
 
-// kLight: two CTAs per SM (at most 64 registers a thread, 16 partials
-// preloaded) for grids of more than one wave of one-per-SM CTAs.
-template <bool kWindow, bool kLight = false>
-__global__ void __launch_bounds__(kCombineThreads, kLight ? 2 : 1) combine_kernel(DecodeArgs a) {
+template <bool kWindow>
+__global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   CombineSmem& sm = *reinterpret_cast<CombineSmem*>(smem_raw);
   WindowSmem& ws = *reinterpret_cast<WindowSmem*>(smem_raw + sizeof(CombineSmem));
@@ -1565,7 +1563,7 @@ __global__ void __launch_bounds__(kCombineThreads, kLight ? 2 : 1) combine_kerne
   };
   // Thread (h, d) loads element d of its head's first kPre split partials now,
   // so that these loads and the (m, l) loads below share one round trip.
-  constexpr int kPre = kLight ? 16 : 48;
+  constexpr int kPre = 48;
   const float* parts_h = head_parts(kv * G + h);
   float v[kPre];
 #pragma unroll
@@ -1669,6 +1667,152 @@ __global__ void __launch_bounds__(kCombineThreads, kLight ? 2 : 1) combine_kerne
     else if (h < G) o = (a.rotate_out ? fmaf(sm.ww[h], owin, r) : fmaf(sm.ww[h], r, o)) * sm.linv[h];
   }
   if (h < G) a.out[(static_cast<size_t>(b) * a.H + kv * G + h) * kDim + d] = o;
+}
+
+// The KV-head combine in 256-thread CTAs (four per SM, so that a batch of up
+// to 4 x #SMs (sequence, KV head) pairs takes one wave), with the same
+// arithmetic in the same order as combine_kernel<false>.  Merge: the two warps
+// of head h = tid / 64 each compute the head's (m, l) weights over the splits
+// (lane j holds splits j and j + 32) and thread (h, p) merges elements 2p and
+// 2p + 1, taking each weight from its lane by a shuffle, so no barrier
+// separates the weights from the merge.  Basis change: R_V^T is read from
+// global memory (L2) rather than staged, thread (q, p) = (tid / 64, tid % 64)
+// sums quarter q of j for elements 2p, 2p + 1 of all G heads.
+constexpr int kC4Threads = 256;
+constexpr int kC4Pre = 12;
+struct Combine4Smem {
+  alignas(16) float ot[kDim][kMaxG];   // the G merged outputs, element-major
+  float red[4][kMaxG][kDim];           // per-quarter sums of the basis change
+};
+
+__global__ void __launch_bounds__(kC4Threads, 4) combine4_kernel(DecodeArgs a) {
+  __shared__ Combine4Smem sm;
+  const int b = blockIdx.x, kv = blockIdx.y, tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int G = a.G;
+  griddep_launch_dependents();
+  griddep_wait();       // the partials come from the decode kernel
+  int S = a.splits, pbase = 0;
+  if (a.balanced) {
+    S = a.sched_nsplit[b];
+    pbase = a.sched_base[b];
+  }
+  const int pstride = a.balanced ? a.H * kPartStride : kPartStride;
+  const int h = tid >> 6, p = tid & 63;
+  const bool live = h < G;              // uniform across each warp
+  float2 o = make_float2(0.0f, 0.0f);
+  if (live) {
+    const float* parts =
+        a.balanced ? a.part + (static_cast<size_t>(pbase) * a.H + kv * G + h) * kPartStride
+                   : a.part + (static_cast<size_t>(b) * a.H + kv * G + h) * a.splits * kPartStride;
+    const float* pv = parts + 4 + 2 * p;
+    // the first kC4Pre partials and the (m, l) of splits lane, lane + 32 in one
+    // round trip
+    float2 v[kC4Pre];
+#pragma unroll
+    for (int k = 0; k < kC4Pre; ++k)
+      v[k] = k < S ? *reinterpret_cast<const float2*>(pv + k * pstride) : make_float2(0.0f, 0.0f);
+    float mk[2], lk[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int j = lane + 32 * k;
+      mk[k] = j < S ? parts[j * pstride] : -INFINITY;
+      lk[k] = j < S ? parts[j * pstride + 1] : 0.0f;
+    }
+    float M = fmaxf(mk[0], mk[1]);
+    for (int j = lane + 64; j < S; j += 32) M = fmaxf(M, parts[j * pstride]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float wk[2];
+    float L = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int j = lane + 32 * k;
+      wk[k] = (j < S && mk[k] != -INFINITY) ? fast_exp2(mk[k] - M) : 0.0f;
+      if (j < S) L = fmaf(wk[k], lk[k], L);
+    }
+    for (int j = lane + 64; j < S; j += 32) {
+      const float mj = parts[j * pstride];
+      const float lj = parts[j * pstride + 1];
+      const float w = (mj == -INFINITY) ? 0.0f : fast_exp2(mj - M);
+      L = fmaf(w, lj, L);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float linv = (L > 0.0f) ? 1.0f / L : 0.0f;
+    // weight of split j: lane j % 32 of wk[j / 32] (recomputed past 64 splits)
+    auto weight = [&](int j) -> float {
+      if (j < 64) return __shfl_sync(0xffffffffu, j < 32 ? wk[0] : wk[1], j & 31);
+      const float mj = parts[j * pstride];
+      return (mj == -INFINITY) ? 0.0f : fast_exp2(mj - M);
+    };
+#pragma unroll
+    for (int k = 0; k < kC4Pre; ++k) {
+      if (k < S) {
+        const float w = weight(k);
+        o.x = fmaf(w, v[k].x, o.x);
+        o.y = fmaf(w, v[k].y, o.y);
+      }
+    }
+    for (int j0 = kC4Pre; j0 < S; j0 += kC4Pre) {
+#pragma unroll
+      for (int k = 0; k < kC4Pre; ++k)
+        v[k] = j0 + k < S ? *reinterpret_cast<const float2*>(pv + (j0 + k) * pstride)
+                          : make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int k = 0; k < kC4Pre; ++k) {
+        if (j0 + k < S) {
+          const float w = weight(j0 + k);
+          o.x = fmaf(w, v[k].x, o.x);
+          o.y = fmaf(w, v[k].y, o.y);
+        }
+      }
+    }
+    o.x *= linv;
+    o.y *= linv;
+  }
+  float* out = a.out + (static_cast<size_t>(b) * a.H + kv * G + h) * kDim + 2 * p;
+  if (!a.rotate_out) {
+    if (live) *reinterpret_cast<float2*>(out) = o;
+    return;
+  }
+  sm.ot[2 * p][h] = o.x;
+  sm.ot[2 * p + 1][h] = o.y;
+  __syncthreads();
+  {
+    const int q = tid >> 6;
+    const float* Rt = a.RVt + static_cast<size_t>(kv) * kDim * kDim + 2 * p;
+    float r[kMaxG][2];
+#pragma unroll
+    for (int hh = 0; hh < kMaxG; ++hh) r[hh][0] = r[hh][1] = 0.0f;
+#pragma unroll 8
+    for (int jj = 0; jj < kDim / 4; ++jj) {
+      const int j = q * (kDim / 4) + jj;
+      const float4 ov = *reinterpret_cast<const float4*>(sm.ot[j]);
+      const float2 rt = __ldg(reinterpret_cast<const float2*>(Rt + j * kDim));
+      r[0][0] = fmaf(ov.x, rt.x, r[0][0]);
+      r[0][1] = fmaf(ov.x, rt.y, r[0][1]);
+      r[1][0] = fmaf(ov.y, rt.x, r[1][0]);
+      r[1][1] = fmaf(ov.y, rt.y, r[1][1]);
+      r[2][0] = fmaf(ov.z, rt.x, r[2][0]);
+      r[2][1] = fmaf(ov.z, rt.y, r[2][1]);
+      r[3][0] = fmaf(ov.w, rt.x, r[3][0]);
+      r[3][1] = fmaf(ov.w, rt.y, r[3][1]);
+    }
+#pragma unroll
+    for (int hh = 0; hh < kMaxG; ++hh) {
+      sm.red[q][hh][2 * p] = r[hh][0];
+      sm.red[q][hh][2 * p + 1] = r[hh][1];
+    }
+  }
+  __syncthreads();
+  if (live) {
+    float2 y;
+    y.x = (sm.red[0][h][2 * p] + sm.red[1][h][2 * p]) + (sm.red[2][h][2 * p] + sm.red[3][h][2 * p]);
+    y.y = (sm.red[0][h][2 * p + 1] + sm.red[1][h][2 * p + 1]) +
+          (sm.red[2][h][2 * p + 1] + sm.red[3][h][2 * p + 1]);
+    *reinterpret_cast<float2*>(out) = y;
+  }
 }
 
 // The same combine with one CTA per query head (b, kv, h), for calls whose
@@ -1972,11 +2116,8 @@ cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     e = launch_dependent(combine_head_kernel, dim3(a.batch, a.Hkv, a.G), dim3(kCombineThreads),
                          sizeof(HeadCombineSmem), st, a);
-  } else if (a.combine_light) {
-    e = set_smem_attr<CombineSmem, combine_kernel<false, true>>();
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(combine_kernel<false, true>, dim3(a.batch, a.Hkv), dim3(kCombineThreads),
-                         sizeof(CombineSmem), st, a);
+  } else if (a.combine_small) {
+    e = launch_dependent(combine4_kernel, dim3(a.batch, a.Hkv), dim3(kC4Threads), 0, st, a);
   } else {
     e = set_smem_attr<CombineSmem, combine_kernel<false>>();
     if (e != cudaSuccess) return e;

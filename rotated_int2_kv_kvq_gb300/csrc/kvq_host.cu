@@ -268,9 +268,11 @@ int decode_common(kvq_handle* h, bool int2, const void* pool, int num_pool_pages
     if (ctas <= static_cast<long>(h->num_sms) * h->ctas_prep[k]) break;
     a.prep_nb *= 2;
   }
-  // two KV-head combine CTAs per SM when one per SM would take more than a wave
-  // (64-sequence ragged step: 186.6 -> 183.6 us)
-  a.combine_light = (!win.on &&
+  // the KV-head combine in small CTAs (four per SM, R_V^T read from L2) when
+  // one 512-thread CTA per SM would take more than a wave (64-sequence ragged
+  // step: 165.3 -> 163.1 us; at batch 16 x 8 KV heads, one wave either way,
+  // the 512-thread CTAs with R_V^T staged are faster: 82.8 vs 84.1 us)
+  a.combine_small = (!win.on &&
                      static_cast<long>(batch) * a.Hkv > h->num_sms) ? 1 : 0;
   a.combine_per_head =
       (int2 && !win.on &&

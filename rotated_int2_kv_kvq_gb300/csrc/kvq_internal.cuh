@@ -50,7 +50,7 @@ struct DecodeArgs {
   const float* RV;           // [Hkv][D][D] value rotations
   int rotate_out;            // 1: out = o_rot R_V^T, 0: out = o_rot
   int combine_per_head = 0;  // 1: the combine takes one CTA per query head (no window)
-  int combine_light = 0;     // 1: the KV-head combine runs two CTAs per SM (large batches)
+  int combine_small = 0;     // 1: the KV-head combine runs in 256-thread CTAs, four per SM (large batches)
   // Length-balanced schedule (balanced = 1): the decode grid's batch * splits
   // CTAs are shared out over the sequences in chunks of one common size, in
   // proportion to their page counts.  sched_map[c] = {b, chunk index, first

@@ -396,12 +396,12 @@ def test_full_stack_sampled_layers(layer):
 
 
 @pytest.mark.parametrize("out_rotated,G,splits", [(True, 4, 3), (False, 2, 0)])
-def test_light_combine_large_batch(out_rotated, G, splits):
+def test_small_combine_large_batch(out_rotated, G, splits):
     """More (sequence, KV head) pairs than one wave of one-per-SM KV-head
-    combine CTAs: the combine at two CTAs per SM, checked on every (sequence,
-    head) output against the oracle.  Odd batch, plain and rotated-basis
-    output, G = 2 (half of each CTA's head threads idle), an empty sequence
-    (output 0)."""
+    combine CTAs: the combine in 256-thread CTAs (four per SM, R_V^T read from
+    global memory), checked on every (sequence, head) output against the
+    oracle.  Odd batch, plain and rotated-basis output, G = 2 (half of each
+    CTA's head warps idle), an empty sequence (output 0)."""
     wl = W.WORKLOADS["ragged_64"]
     B, Hkv = 21, 8
     pt, _ = W.page_table(wl)
@@ -420,4 +420,4 @@ def test_light_combine_large_batch(out_rotated, G, splits):
     pairs = [[b, h] for b in range(B) if lens[b] > 0 for h in range(Hkv * G)]
     want = c.oracle_decode(c.pool_host(), q, lens, pairs)
     assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want,
-                           f"two-per-SM combine, out_rotated={out_rotated}, G={G}")
+                           f"small-CTA combine, out_rotated={out_rotated}, G={G}")

@@ -81,8 +81,8 @@ def test_append_decode_large_batch(B):
     """Batches whose per-sequence preparation CTAs would exceed one wave: the
     step preparation groups 2 (B = 24, 25) or 4 (B = 48) sequences per append
     CTA (B = 25 ends with a group of one); B = 48 also takes the
-    length-balanced decode schedule; all three take the KV-head combine at two
-    CTAs per SM.  Fused step against append + decode (pools byte for byte,
+    length-balanced decode schedule; all three take the KV-head combine in
+    256-thread CTAs.  Fused step against append + decode (pools byte for byte,
     outputs bit for bit) and against the float64 oracle, on sampled (sequence,
     head) pairs plus every head of the last sequence and of sequence 1."""
     wl = W.WORKLOADS["ragged_64"]
