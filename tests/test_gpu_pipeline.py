@@ -76,13 +76,13 @@ def test_append_decode_equals_append_then_decode(name, splits):
     assert a.status() == 0 and b.status() == 0
 
 
-@pytest.mark.parametrize("B", [24, 25, 48])
+@pytest.mark.parametrize("B", [24, 25, 48, 57, 64])
 def test_append_decode_large_batch(B):
     """Batches whose per-sequence preparation CTAs would exceed one wave: the
-    step preparation groups 2 (B = 24, 25) or 4 (B = 48) sequences per append
-    CTA (B = 25 ends with a group of one); B = 48 also takes the
-    length-balanced decode schedule; all three take the KV-head combine in
-    256-thread CTAs.  Fused step against append + decode (pools byte for byte,
+    step preparation groups 2 (B = 24, 25), 4 (B = 48) or 8 (B = 57, 64)
+    sequences per append CTA (B = 25 and 57 end with a group of one); B = 25
+    decodes on the plain schedule (one wave of 12 splits), the others on the
+    length-balanced one; all take the KV-head combine in 256-thread CTAs.  Fused step against append + decode (pools byte for byte,
     outputs bit for bit) and against the float64 oracle, on sampled (sequence,
     head) pairs plus every head of the last sequence and of sequence 1."""
     wl = W.WORKLOADS["ragged_64"]
