@@ -193,3 +193,33 @@ def test_graph_replay_equals_eager(fused):
     want = c.oracle_decode(c.pool_host(), q[1], lens, pairs)
     got = graph.out[1].cpu().numpy().astype(np.float64)
     assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want, "graph")
+
+
+@pytest.mark.parametrize("G,B", [(1, 16), (2, 16), (2, 40)])
+def test_append_decode_group_sizes(G, B):
+    """The fused step with G = 1 and 2 query heads per KV head (the query CTAs
+    leave the unused head columns of their fragments empty): against append +
+    decode bit for bit and against the float64 oracle on every head of two
+    sequences.  B = 40: groups of four sequences per append CTA."""
+    wl = W.WORKLOADS["ragged_64"]
+    Hkv = 8
+    rng = np.random.default_rng(70 + 10 * G + B)
+    pt = rng.permutation(B * 64).astype(np.int32).reshape(B, 64)     # 1024 tokens each
+    kw = dict(page_table=pt, num_pool_pages=B * 64, num_heads=Hkv * G, num_kv_heads=Hkv)
+    lens = rng.integers(1, 1000, size=B)
+    lens[:4] = [0, 1, 16, 17]
+    a, b = _pair(wl, lens, **kw)
+    for step in range(2):
+        Kn, Vn = _new_tokens(wl, lens, Hkv)
+        q = W.queries(wl, 0, 80 + step)[:B, :Hkv * G].copy()
+        lens_after = lens + 1
+        got = _fused(a, Kn, Vn, q, lens_after, 0)
+        want = _separate(b, Kn, Vn, q, lens_after, 0)
+        assert np.array_equal(a.pool_host(), b.pool_host()), f"pool differs at step {step}"
+        assert np.array_equal(got, want), f"output differs at step {step}"
+        lens = lens_after
+    pairs = [[bb, hh] for bb in (2, B - 1) for hh in range(Hkv * G)]
+    want = a.oracle_decode(a.pool_host(), q, lens, pairs)
+    assert_close_attention(got[[p[0] for p in pairs], [p[1] for p in pairs]], want,
+                           f"fused step G={G} B={B}")
+    assert a.status() == 0 and b.status() == 0
